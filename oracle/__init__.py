@@ -1,0 +1,217 @@
+"""CPU oracle of the quantized tensor-activation codec -- TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product (the CUDA library and its
+Python binding) never imports it, and the two share no code: the oracle is
+plain single-threaded C (``qta_oracle.c``) wrapped here with ctypes and numpy.
+
+Every function follows a passage of the pages (cited in ``qta_oracle.c``):
+TACO (FP8 E4M3, block Hadamard, dual-scale), EQuARX (block-symmetric int8,
+dequantize to FP32 before adding) and Flash Communication (asymmetric
+group-128 INT4/INT8, two-step all-reduce).
+"""
+from __future__ import annotations
+
+import ctypes
+import functools
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "qta_oracle.c")
+_HDR = os.path.join(_HERE, "qta_oracle.h")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "liboracle.so")
+
+# dtype / scheme / mode codes of the C oracle
+BF16, FP16, FP32 = 0, 1, 2
+TACO_FP8, INT8_SYM, INT4_ASYM, INT8_ASYM = 0, 1, 2, 3
+DELAYED, CURRENT = 0, 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so with strict IEEE binary32 semantics."""
+    os.makedirs(_BUILD, exist_ok=True)
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_HDR))
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= newest:
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+           "-fexcess-precision=standard", "-fPIC", "-shared", "-Wall", "-Wextra",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ctypes.CDLL(build())
+            i64, i32, vp, fp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p
+            L.orc_e4m3_encode.argtypes = [ctypes.c_float]
+            L.orc_e4m3_encode.restype = ctypes.c_uint8
+            L.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+            L.orc_e4m3_decode.restype = ctypes.c_float
+            L.orc_f32_to_bf16.argtypes = [ctypes.c_float]
+            L.orc_f32_to_bf16.restype = ctypes.c_uint16
+            L.orc_f32_to_f16.argtypes = [ctypes.c_float]
+            L.orc_f32_to_f16.restype = ctypes.c_uint16
+            L.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
+            L.orc_f16_to_f32.restype = ctypes.c_float
+            L.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
+            L.orc_bf16_to_f32.restype = ctypes.c_float
+            for name in ("orc_e4m3_encode_array", "orc_f32_to_bf16_array", "orc_f32_to_f16_array"):
+                getattr(L, name).argtypes = [vp, vp, i64]
+                getattr(L, name).restype = None
+            L.orc_fwht.argtypes = [fp, i32]
+            L.orc_fwht_rows.argtypes = [fp, i64, i32]
+            L.orc_scale_from_amax.argtypes = [ctypes.c_float]
+            L.orc_scale_from_amax.restype = ctypes.c_float
+            L.orc_taco_update_scale.argtypes = [fp, i64]
+            L.orc_compress.argtypes = [i32, i32, vp, i32, i64, i64, i64, fp, i32, vp, vp, vp]
+            L.orc_compress.restype = i32
+            L.orc_decompress.argtypes = [i32, i32, vp, vp, vp, fp, i64, i64, i64, vp, i32]
+            L.orc_decompress.restype = i32
+            L.orc_reduce.argtypes = [i32, i32, i32, vp, vp, vp, vp, i64, i64, i64, i64, fp]
+            L.orc_reduce.restype = i32
+            _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+# ---------------------------------------------------------------- formats
+def e4m3_encode(v) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(v.shape, dtype=np.uint8)
+    lib().orc_e4m3_encode_array(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+@functools.lru_cache(maxsize=None)
+def _e4m3_table() -> np.ndarray:
+    return np.array([lib().orc_e4m3_decode(i) for i in range(256)], dtype=np.float32)
+
+
+@functools.lru_cache(maxsize=None)
+def _f16_table() -> np.ndarray:
+    L = lib()
+    return np.array([L.orc_f16_to_f32(i) for i in range(65536)], dtype=np.float32)
+
+
+def e4m3_decode(c) -> np.ndarray:
+    return _e4m3_table()[np.asarray(c, dtype=np.uint8)]
+
+
+def f32_to_bf16(v) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(v.shape, dtype=np.uint16)
+    lib().orc_f32_to_bf16_array(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def f32_to_f16(v) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(v.shape, dtype=np.uint16)
+    lib().orc_f32_to_f16_array(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def bf16_to_f32(h) -> np.ndarray:
+    h = np.asarray(h, dtype=np.uint16)
+    return (h.astype(np.uint32) << 16).view(np.float32)
+
+
+def f16_to_f32(h) -> np.ndarray:
+    return _f16_table()[np.asarray(h, dtype=np.uint16)]
+
+
+# ---------------------------------------------------------------- transform
+def fwht(y, B: int) -> np.ndarray:
+    """Unnormalised block Hadamard over consecutive blocks of B (in a copy)."""
+    y = np.array(y, dtype=np.float32, copy=True).reshape(-1)
+    assert y.size % B == 0
+    lib().orc_fwht_rows(_ptr(y), y.size // B, B)
+    return y
+
+
+def scale_from_amax(amax: float) -> float:
+    return lib().orc_scale_from_amax(float(amax))
+
+
+def taco_update_scale(state: np.ndarray) -> None:
+    assert state.dtype == np.float32 and state.flags.c_contiguous
+    lib().orc_taco_update_scale(_ptr(state), state.size // 2)
+
+
+# ---------------------------------------------------------------- codec
+def codes_nbytes(scheme: int, n_elems: int) -> int:
+    return n_elems // 2 if scheme == INT4_ASYM else n_elems
+
+
+def compress(scheme: int, B: int, x: np.ndarray, in_dtype: int, batch: int, rows: int,
+             cols: int, state: np.ndarray | None = None, mode: int = DELAYED):
+    """Returns (codes, scales, zeros); updates ``state`` in place for TACO."""
+    E = batch * rows * cols
+    x = np.ascontiguousarray(x)
+    assert x.size == E
+    codes = np.zeros(codes_nbytes(scheme, E), dtype=np.int8 if scheme == INT8_SYM else np.uint8)
+    zeros = None
+    if scheme == TACO_FP8:
+        scales = np.zeros(E // B, dtype=np.uint8)
+        assert state is not None and state.dtype == np.float32 and state.size == 2 * batch
+    elif scheme == INT8_SYM:
+        scales = np.zeros(E // 64, dtype=np.float32)
+    else:
+        scales = np.zeros(E // 128, dtype=np.uint16)
+        zeros = np.zeros(E // 128, dtype=np.uint16)
+    rc = lib().orc_compress(scheme, B, _ptr(x), in_dtype, batch, rows, cols,
+                            _ptr(state), mode, _ptr(codes), _ptr(scales), _ptr(zeros))
+    if rc:
+        raise ValueError(f"oracle compress rejected the arguments ({rc})")
+    return codes, scales, zeros
+
+
+def decompress(scheme: int, B: int, codes, scales, zeros, state, batch: int, rows: int,
+               cols: int, out_dtype: int) -> np.ndarray:
+    E = batch * rows * cols
+    out = np.zeros(E, dtype=np.float32 if out_dtype == FP32 else np.uint16)
+    st = None if state is None else np.ascontiguousarray(state, dtype=np.float32)
+    rc = lib().orc_decompress(scheme, B, _ptr(np.ascontiguousarray(codes)),
+                              _ptr(np.ascontiguousarray(scales)),
+                              _ptr(None if zeros is None else np.ascontiguousarray(zeros)),
+                              _ptr(st), batch, rows, cols, _ptr(out), out_dtype)
+    if rc:
+        raise ValueError(f"oracle decompress rejected the arguments ({rc})")
+    return out
+
+
+def reduce(scheme: int, B: int, shards, rows: int, cols: int, row_begin: int = 0,
+           row_end: int | None = None) -> np.ndarray:
+    """shards: list of (codes, scales, zeros, state) per rank, one tensor each."""
+    if row_end is None:
+        row_end = rows
+    n = len(shards)
+    keep = [tuple(None if a is None else np.ascontiguousarray(a) for a in s) for s in shards]
+    VP = ctypes.c_void_p * n
+    codes = VP(*[_ptr(s[0]) for s in keep])
+    scales = VP(*[_ptr(s[1]) for s in keep])
+    zeros = VP(*[_ptr(s[2]) for s in keep]) if keep[0][2] is not None else None
+    st_keep = [None if s[3] is None else np.ascontiguousarray(s[3], dtype=np.float32) for s in keep]
+    states = VP(*[_ptr(a) for a in st_keep]) if st_keep[0] is not None else None
+    out = np.zeros((row_end - row_begin) * cols, dtype=np.float32)
+    rc = lib().orc_reduce(scheme, B, n, codes, scales, zeros, states, rows, cols,
+                          row_begin, row_end, _ptr(out))
+    if rc:
+        raise ValueError(f"oracle reduce rejected the arguments ({rc})")
+    return out

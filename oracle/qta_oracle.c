@@ -1,0 +1,436 @@
+/*
+ * qta_oracle.c -- the CPU oracle.  TEST INFRASTRUCTURE ONLY (see the header):
+ * plain scalar C, one thread, no blocking or fusion beyond what each method
+ * states, built with -O2 -ffp-contract=off -fno-fast-math so that every
+ * float operation below is one IEEE-754 binary32 operation rounded to
+ * nearest-even, in the order written.
+ *
+ * The pages fix FP32 as the working precision of the method (EQuARX: shards
+ * are dequantized to FP32 and summed in FP32; TACO: FP32 per-tensor scale),
+ * so the oracle computes in binary32; every integer it produces (a code, a
+ * scale byte) is decided in that precision.  Readings of passages the pages
+ * leave open are marked R1..R12 and listed in the design notes.
+ */
+#include "qta_oracle.h"
+
+#include <float.h>
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+static uint32_t f2u(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+static float u2f(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
+
+/* Round the non-negative integer sig * 2^-shift to the nearest integer,
+ * ties to even (R1: every rounding is round-to-nearest-even). */
+static uint32_t rne_shift(uint32_t sig, int shift)
+{
+    if (shift <= 0) return sig << (-shift);
+    if (shift >= 32) return 0; /* sig < 2^24 < half of 2^shift */
+    uint32_t q = sig >> shift;
+    uint32_t rem = sig & ((1u << shift) - 1u);
+    uint32_t half = 1u << (shift - 1);
+    if (rem > half || (rem == half && (q & 1u))) q += 1u;
+    return q;
+}
+
+/* ------------------------------------------------------------------------
+ * FP8 E4M3 (the "E4M3" of [TACO] Fig. 3; the FN variant of the FP8 paper the
+ * TACO page cites: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+ * infinities, 0x7F/0xFF = NaN, largest finite 448, subnormal step 2^-9).
+ * ---------------------------------------------------------------------- */
+float orc_e4m3_decode(uint8_t c)
+{
+    int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    float mag;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        mag = ldexpf((float)m, -9);            /* m/8 * 2^-6 */
+    else
+        mag = ldexpf((float)(8 + m), e - 10);  /* (1+m/8) * 2^(e-7) */
+    return s ? -mag : mag;
+}
+
+/* Encode with round-to-nearest-even onto the E4M3 grid; magnitudes that
+ * round above 448 saturate to 448 ("saturation at 448"), +-Inf -> +-448,
+ * NaN -> 0x7F.  The sign of zero is kept. */
+uint8_t orc_e4m3_encode(float v)
+{
+    uint32_t u = f2u(v);
+    uint8_t sign = (uint8_t)((u >> 31) << 7);
+    uint32_t a = u & 0x7fffffffu;
+    if (a > 0x7f800000u) return 0x7f;
+    if (a == 0x7f800000u) return sign | 0x7e;
+    int ef = (int)(a >> 23);
+    if (ef == 0) return sign; /* binary32 subnormals are < 2^-126: round to 0 */
+    int E = ef - 127;                         /* |v| in [2^E, 2^(E+1)) */
+    uint32_t sig = (a & 0x7fffffu) | 0x800000u; /* |v| = sig * 2^(E-23) */
+    int k = (E < -6 ? -6 : E) - 3;            /* grid step: 2^k */
+    uint32_t n = rne_shift(sig, 23 + k - E);  /* |v| / 2^k rounded */
+    uint32_t code;
+    if (E < -6)
+        code = n;                             /* subnormal: n steps of 2^-9 */
+    else
+        code = (uint32_t)((E + 7) << 3) + n - 8u; /* n in [8,16] */
+    if (code > 0x7eu) code = 0x7eu;           /* satfinite */
+    return sign | (uint8_t)code;
+}
+
+void orc_e4m3_encode_array(const float* v, uint8_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_encode(v[i]);
+}
+
+/* ------------------------------------------------------------------------
+ * bf16 / fp16 (IEEE binary16), round-to-nearest-even, overflow to +-Inf
+ * (R11), NaN to a quiet NaN.
+ * ---------------------------------------------------------------------- */
+float orc_bf16_to_f32(uint16_t h) { return u2f((uint32_t)h << 16); }
+
+uint16_t orc_f32_to_bf16(float v)
+{
+    uint32_t u = f2u(v);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x40u);
+    uint32_t q = u >> 16, rem = u & 0xffffu;
+    if (rem > 0x8000u || (rem == 0x8000u && (q & 1u))) q += 1u; /* carries into exp */
+    return (uint16_t)q;
+}
+
+float orc_f16_to_f32(uint16_t h)
+{
+    int s = h >> 15, e = (h >> 10) & 31, m = h & 1023;
+    float mag;
+    if (e == 31) mag = m ? NAN : INFINITY;
+    else if (e == 0) mag = ldexpf((float)m, -24);
+    else mag = ldexpf((float)(1024 + m), e - 25);
+    return s ? -mag : mag;
+}
+
+uint16_t orc_f32_to_f16(float v)
+{
+    uint32_t u = f2u(v);
+    uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    uint32_t a = u & 0x7fffffffu;
+    if (a > 0x7f800000u) return sign | 0x7e00u;
+    if (a == 0x7f800000u) return sign | 0x7c00u;
+    int ef = (int)(a >> 23);
+    if (ef == 0) return sign;
+    int E = ef - 127;
+    uint32_t sig = (a & 0x7fffffu) | 0x800000u;
+    if (E > 15) return sign | 0x7c00u;
+    int k = (E < -14 ? -14 : E) - 10;
+    uint32_t n = rne_shift(sig, 23 + k - E);
+    uint32_t code = (E < -14) ? n : (uint32_t)((E + 15) << 10) + n - 1024u;
+    if (code >= 0x7c00u) code = 0x7c00u;     /* rounded past 65504 -> Inf */
+    return sign | (uint16_t)code;
+}
+
+void orc_f32_to_bf16_array(const float* v, uint16_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_to_bf16(v[i]);
+}
+
+void orc_f32_to_f16_array(const float* v, uint16_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_to_f16(v[i]);
+}
+
+static float load_elem(const void* x, int dtype, int64_t i)
+{
+    if (dtype == ORC_BF16) return orc_bf16_to_f32(((const uint16_t*)x)[i]);
+    if (dtype == ORC_FP16) return orc_f16_to_f32(((const uint16_t*)x)[i]);
+    return ((const float*)x)[i];
+}
+
+static void store_elem(void* y, int dtype, int64_t i, float v)
+{
+    if (dtype == ORC_BF16) ((uint16_t*)y)[i] = orc_f32_to_bf16(v);
+    else if (dtype == ORC_FP16) ((uint16_t*)y)[i] = orc_f32_to_f16(v);
+    else ((float*)y)[i] = v;
+}
+
+/* ------------------------------------------------------------------------
+ * Block Hadamard ([TACO] Core claim, Fig. 7, Fig. 8: the Hadamard rotation
+ * of the Adaptive Scale-Hadamard transform).  R3: unnormalised Sylvester
+ * matrix, H[i][j] = (-1)^popcount(i & j), applied as the in-place butterfly
+ * with strides h = 1, 2, 4, ..., B/2 in that order; each pair (j, j+h) with
+ * j & h == 0 becomes (a + b, a - b) in binary32.
+ * ---------------------------------------------------------------------- */
+void orc_fwht(float* y, int B)
+{
+    for (int h = 1; h < B; h <<= 1)
+        for (int i = 0; i < B; i += 2 * h)
+            for (int j = i; j < i + h; ++j) {
+                float a = y[j], b = y[j + h];
+                y[j] = a + b;
+                y[j + h] = a - b;
+            }
+}
+
+void orc_fwht_rows(float* y, int64_t nblk, int B)
+{
+    for (int64_t b = 0; b < nblk; ++b) orc_fwht(y + b * B, B);
+}
+
+/* ------------------------------------------------------------------------
+ * Per-tensor FP32 scale of the dual-scale scheme ([TACO] Core claim:
+ * dual-scale quantization keeps FP8 stable across training steps).
+ * R5: S = amax / 448 from the latest amax (history length one); a zero,
+ * non-finite or sub-normal result falls back to S = 1.
+ * ---------------------------------------------------------------------- */
+float orc_scale_from_amax(float amax)
+{
+    float S = amax / 448.0f;
+    if (!(S >= FLT_MIN && S <= FLT_MAX)) S = 1.0f;
+    return S;
+}
+
+void orc_taco_update_scale(float* state, int64_t batch)
+{
+    for (int64_t t = 0; t < batch; ++t) {
+        state[2 * t] = orc_scale_from_amax(state[2 * t + 1]);
+        state[2 * t + 1] = 0.0f;
+    }
+}
+
+/* ---- TACO FP8 compress of one tensor ([TACO] Core claim, Fig. 7) ----
+ * R2: blocks are B contiguous elements along the hidden (last) axis.
+ * R4: block scale r_b = E4M3(a_b / (448 S)) stored as one E4M3 byte relative
+ *     to the per-tensor FP32 scale S; s_b = S * r_b; codes E4M3(y * 1/s_b). */
+static void taco_compress_tensor(const void* x, int dtype, int64_t off, int64_t E,
+                                 int B, float* st, int mode, uint8_t* codes,
+                                 uint8_t* scales, float* y)
+{
+    int64_t nblk = E / B;
+    if (mode == ORC_CURRENT) {
+        float amax = 0.0f;
+        for (int64_t b = 0; b < nblk; ++b) {
+            for (int i = 0; i < B; ++i) y[i] = load_elem(x, dtype, off + b * B + i);
+            orc_fwht(y, B);
+            for (int i = 0; i < B; ++i) amax = fmaxf(amax, fabsf(y[i]));
+        }
+        st[0] = orc_scale_from_amax(amax);
+        st[1] = 0.0f;
+    }
+    float S = st[0];
+    float tinv = 1.0f / (448.0f * S);
+    float amax_t = 0.0f;
+    for (int64_t b = 0; b < nblk; ++b) {
+        for (int i = 0; i < B; ++i) y[i] = load_elem(x, dtype, off + b * B + i);
+        orc_fwht(y, B);
+        float a = 0.0f;
+        for (int i = 0; i < B; ++i) a = fmaxf(a, fabsf(y[i]));
+        amax_t = fmaxf(amax_t, a);
+        uint8_t r = orc_e4m3_encode(a * tinv);
+        if (r == 0 && a > 0.0f) r = 0x01;
+        float sb = S * orc_e4m3_decode(r);
+        float inv = (sb > 0.0f) ? 1.0f / sb : 0.0f;
+        for (int i = 0; i < B; ++i) codes[b * B + i] = orc_e4m3_encode(y[i] * inv);
+        scales[b] = r;
+    }
+    st[1] = fmaxf(st[1], amax_t);
+}
+
+/* ---- block-symmetric INT8, one FP32 scale per 64 ([EQuARX] What carries
+ * the argument: Qp1 computes the absmax metadata, Qp2 scales the data).
+ * R6: the 64 entries of one scale are 64 contiguous elements. */
+static void int8sym_compress_tensor(const void* x, int dtype, int64_t off, int64_t E,
+                                    int8_t* codes, float* scales)
+{
+    for (int64_t b = 0; b < E / 64; ++b) {
+        float a = 0.0f;
+        for (int i = 0; i < 64; ++i) a = fmaxf(a, fabsf(load_elem(x, dtype, off + b * 64 + i)));
+        float s = a / 127.0f;
+        float inv = (a > 0.0f) ? 127.0f / a : 0.0f;
+        for (int i = 0; i < 64; ++i) {
+            float q = rintf(load_elem(x, dtype, off + b * 64 + i) * inv);
+            if (q > 127.0f) q = 127.0f;
+            if (q < -127.0f) q = -127.0f;
+            codes[b * 64 + i] = (int8_t)q;
+        }
+        scales[b] = s;
+    }
+}
+
+/* ---- asymmetric group-128 INT4 / INT8 ([FLASH] What carries the argument,
+ * Assumptions & free parameters: g = 128, fp16 scale + zero-point per group).
+ * R7: min/max affine quantizer with a floating zero-point equal to the group
+ * minimum: s = fp16((max-min)/Q), z = fp16(min), q = clamp(rint((x-z)/s)).
+ * R8: INT4 codes, element 2k in the low nibble of byte k, 2k+1 in the high. */
+static void asym_compress_tensor(const void* x, int dtype, int64_t off, int64_t E,
+                                 int bits, uint8_t* codes, uint16_t* scales,
+                                 uint16_t* zeros)
+{
+    const int G = 128;
+    const float Q = (float)((1 << bits) - 1);
+    for (int64_t g = 0; g < E / G; ++g) {
+        float mn = load_elem(x, dtype, off + g * G), mx = mn;
+        for (int i = 1; i < G; ++i) {
+            float v = load_elem(x, dtype, off + g * G + i);
+            mn = fminf(mn, v);
+            mx = fmaxf(mx, v);
+        }
+        float sf = (mx - mn) / Q;
+        if (sf > 65504.0f) sf = 65504.0f;
+        float zc = mn;
+        if (zc > 65504.0f) zc = 65504.0f;
+        if (zc < -65504.0f) zc = -65504.0f;
+        uint16_t s16 = orc_f32_to_f16(sf), z16 = orc_f32_to_f16(zc);
+        float s = orc_f16_to_f32(s16), z = orc_f16_to_f32(z16);
+        float inv = (s > 0.0f) ? 1.0f / s : 0.0f;
+        for (int i = 0; i < G; ++i) {
+            float q = rintf((load_elem(x, dtype, off + g * G + i) - z) * inv);
+            if (q < 0.0f) q = 0.0f;
+            if (q > Q) q = Q;
+            uint8_t c = (uint8_t)q;
+            int64_t e = g * G + i;
+            if (bits == 8) {
+                codes[e] = c;
+            } else if ((e & 1) == 0) {
+                codes[e >> 1] = c;
+            } else {
+                codes[e >> 1] = (uint8_t)(codes[e >> 1] | (c << 4));
+            }
+        }
+        scales[g] = s16;
+        zeros[g] = z16;
+    }
+}
+
+static int check_shape(int scheme, int B, int64_t batch, int64_t rows, int64_t cols)
+{
+    if (batch < 0 || rows < 0 || cols < 0) return -1;
+    if (scheme == ORC_TACO_FP8) {
+        if (B < 2 || (B & (B - 1)) || B > 4096) return -1;
+    } else if (scheme == ORC_INT8_SYM) {
+        if (B != 64) return -1;
+    } else if (scheme == ORC_INT4_ASYM || scheme == ORC_INT8_ASYM) {
+        if (B != 128) return -1;
+    } else {
+        return -1;
+    }
+    if (cols % B) return -1;
+    return 0;
+}
+
+int orc_compress(int scheme, int B, const void* x, int in_dtype, int64_t batch,
+                 int64_t rows, int64_t cols, float* state, int mode,
+                 void* codes, void* scales, void* zeros)
+{
+    if (check_shape(scheme, B, batch, rows, cols)) return -1;
+    int64_t E = rows * cols;
+    if (scheme == ORC_TACO_FP8) {
+        float* y = (float*)malloc(sizeof(float) * (size_t)B);
+        if (!y) return -2;
+        for (int64_t t = 0; t < batch; ++t)
+            taco_compress_tensor(x, in_dtype, t * E, E, B, state + 2 * t, mode,
+                                 (uint8_t*)codes + t * E, (uint8_t*)scales + t * (E / B), y);
+        free(y);
+    } else if (scheme == ORC_INT8_SYM) {
+        for (int64_t t = 0; t < batch; ++t)
+            int8sym_compress_tensor(x, in_dtype, t * E, E, (int8_t*)codes + t * E,
+                                    (float*)scales + t * (E / 64));
+    } else {
+        int bits = scheme == ORC_INT4_ASYM ? 4 : 8;
+        for (int64_t t = 0; t < batch; ++t)
+            asym_compress_tensor(x, in_dtype, t * E, E, bits,
+                                 (uint8_t*)codes + t * (E * bits / 8),
+                                 (uint16_t*)scales + t * (E / 128), (uint16_t*)zeros + t * (E / 128));
+    }
+    return 0;
+}
+
+/* Dequantized value of element e (flat index within one tensor) in FP32.
+ * TACO: E4M3 code times s_b = S * r_b, before the inverse transform.
+ * INT8: q * s.  ASYM: fmaf(q, s, z) (one rounding, R7). */
+static float dequant(int scheme, int B, const void* codes, const void* scales,
+                     const void* zeros, const float* st, int64_t e)
+{
+    if (scheme == ORC_TACO_FP8) {
+        float sb = st[0] * orc_e4m3_decode(((const uint8_t*)scales)[e / B]);
+        return orc_e4m3_decode(((const uint8_t*)codes)[e]) * sb;
+    }
+    if (scheme == ORC_INT8_SYM)
+        return (float)((const int8_t*)codes)[e] * ((const float*)scales)[e / 64];
+    float s = orc_f16_to_f32(((const uint16_t*)scales)[e / 128]);
+    float z = orc_f16_to_f32(((const uint16_t*)zeros)[e / 128]);
+    int q;
+    if (scheme == ORC_INT8_ASYM)
+        q = ((const uint8_t*)codes)[e];
+    else
+        q = (((const uint8_t*)codes)[e >> 1] >> ((e & 1) * 4)) & 15;
+    return fmaf((float)q, s, z);
+}
+
+/* Decompress: dequantize; for TACO apply the inverse Hadamard (the same
+ * butterfly, then times 1/B, an exact power of two); round to out dtype. */
+int orc_decompress(int scheme, int B, const void* codes, const void* scales,
+                   const void* zeros, const float* state, int64_t batch,
+                   int64_t rows, int64_t cols, void* y, int out_dtype)
+{
+    if (check_shape(scheme, B, batch, rows, cols)) return -1;
+    int64_t E = rows * cols;
+    float* v = (float*)malloc(sizeof(float) * (size_t)B);
+    if (!v) return -2;
+    for (int64_t t = 0; t < batch; ++t) {
+        const uint8_t* c8 = (const uint8_t*)codes;
+        const void* ct;
+        const void* sc;
+        const void* zt = 0;
+        if (scheme == ORC_TACO_FP8) {
+            ct = c8 + t * E;
+            sc = (const uint8_t*)scales + t * (E / B);
+        } else if (scheme == ORC_INT8_SYM) {
+            ct = c8 + t * E;
+            sc = (const float*)scales + t * (E / 64);
+        } else {
+            int bits = scheme == ORC_INT4_ASYM ? 4 : 8;
+            ct = c8 + t * (E * bits / 8);
+            sc = (const uint16_t*)scales + t * (E / 128);
+            zt = (const uint16_t*)zeros + t * (E / 128);
+        }
+        const float* st = state ? state + 2 * t : 0;
+        for (int64_t b = 0; b < E / B; ++b) {
+            for (int i = 0; i < B; ++i) v[i] = dequant(scheme, B, ct, sc, zt, st, b * B + i);
+            if (scheme == ORC_TACO_FP8) {
+                orc_fwht(v, B);
+                for (int i = 0; i < B; ++i) v[i] = v[i] * (1.0f / (float)B);
+            }
+            for (int i = 0; i < B; ++i) store_elem(y, out_dtype, t * E + b * B + i, v[i]);
+        }
+    }
+    free(v);
+    return 0;
+}
+
+/* Dequantize-reduce ([EQuARX] What carries the argument: every received
+ * shard is dequantized to FP32 before it is added, partial sums stay FP32;
+ * [FLASH] What carries the argument: local FP32 sum after the All2All).
+ * R9: per element, v_r = dequant(shard r) in FP32, then acc = v_0 + v_1 +
+ * ... + v_{N-1} left to right in rank order.  TACO sums in the Hadamard
+ * domain and applies the inverse transform once to the sum (then 1/B). */
+int orc_reduce(int scheme, int B, int n_ranks, const void* const* codes,
+               const void* const* scales, const void* const* zeros,
+               const float* const* states, int64_t rows, int64_t cols,
+               int64_t row_begin, int64_t row_end, float* sum_out)
+{
+    if (check_shape(scheme, B, 1, rows, cols)) return -1;
+    if (n_ranks < 1 || row_begin < 0 || row_end < row_begin || row_end > rows) return -1;
+    int64_t e0 = row_begin * cols, e1 = row_end * cols;
+    for (int64_t b0 = e0; b0 < e1; b0 += B) {
+        for (int i = 0; i < B; ++i) {
+            float acc = 0.0f;
+            for (int r = 0; r < n_ranks; ++r) {
+                float v = dequant(scheme, B, codes[r], scales[r], zeros ? zeros[r] : 0,
+                                  states ? states[r] : 0, b0 + i);
+                acc = (r == 0) ? v : acc + v;
+            }
+            sum_out[b0 - e0 + i] = acc;
+        }
+        if (scheme == ORC_TACO_FP8) {
+            orc_fwht(sum_out + (b0 - e0), B);
+            for (int i = 0; i < B; ++i) sum_out[b0 - e0 + i] = sum_out[b0 - e0 + i] * (1.0f / (float)B);
+        }
+    }
+    return 0;
+}
