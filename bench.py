@@ -1,0 +1,400 @@
+"""Benchmark of the codec's hot path on one GB300 (or N independent replicas).
+
+One step = one pass of the whole path over one batch of synthetic input:
+  K1 taco_compress   all simulated TP ranks (one launch, DELAYED dual-scale)
+     taco_update_scale
+  K2 qar_reduce      dequantize the N code planes to FP32 and sum (all rows)
+  K3 qar_requant     requantize the FP32 sum for the gather stage
+     taco_update_scale
+  K4 taco_decompress the gathered codes back to the 16-bit dtype
+Metric: GB/s of 16-bit input processed (2 bytes x elements x ranks / step
+time), with the fraction of the measured HBM bandwidth reached by the
+dominant kernel (K1) reported in "roofline".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl qta|reference]
+
+--impl reference times the CPU oracle (the plain single-threaded reference
+implementation of the same path) on a bounded row sample of the workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "fused compress + dequant-reduce GB/s of bf16 input; % of GB300 HBM peak"
+FALLBACK_HBM_GBS = 6800.0
+
+# Per-launch DRAM traffic (bytes read + written) of the dominant kernel from
+# one ncu capture, keyed by (kernel, workload) together with the digest of
+# the CUDA sources it was measured on; a changed source makes it stale (null).
+NCU_TRAFFIC = {}
+
+
+def _src_digest() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "quantized_tensor_activation_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    return ws, rank
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="qta_clocks_", suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _cpu_oracle_path(w: workloads.Workload, rows: int, seed: int = 0):
+    """The oracle's full path over a row sample of every rank; returns
+    (seconds, 16-bit input bytes processed, threads used)."""
+    import numpy as np
+    import torch
+
+    import oracle as orc
+    torch.set_num_threads(1)
+    x = workloads.make_rank_inputs(w, rows=rows, seed=seed)
+    xb = x.view(torch.int16).numpy().view(np.uint16).reshape(-1)
+    sch = {"taco_fp8": orc.TACO_FP8, "int8_sym": orc.INT8_SYM, "int4_asym": orc.INT4_ASYM,
+           "int8_asym": orc.INT8_ASYM}
+    s1, s2 = sch[w.scheme], sch[w.gather_scheme]
+    N, C, B, gB = w.ranks, w.cols, w.block, w.gather_block
+    dt = orc.BF16 if w.dtype == "bf16" else orc.FP16
+    E = rows * C
+    t0 = time.perf_counter()
+    st = np.zeros(2 * N, dtype=np.float32) if s1 == orc.TACO_FP8 else None
+    c, s, z = orc.compress(s1, B, xb, dt, N, rows, C, st, orc.CURRENT)
+    cb = E // 2 if s1 == orc.INT4_ASYM else E
+    nb = E // B
+    shards = [(c[r * cb:(r + 1) * cb], s[r * nb:(r + 1) * nb], None if z is None else z[r * nb:(r + 1) * nb],
+               None if st is None else st[2 * r:2 * r + 2]) for r in range(N)]
+    ssum = orc.reduce(s1, B, shards, rows, C)
+    gr = max(1, rows // N)
+    st2 = np.zeros(2 * N, dtype=np.float32) if s2 == orc.TACO_FP8 else None
+    c2, sc2, z2 = orc.compress(s2, gB, ssum[: N * gr * C], orc.FP32, N, gr, C, st2, orc.CURRENT)
+    orc.decompress(s2, gB, c2, sc2, z2, st2, N, gr, C, dt)
+    dt_s = time.perf_counter() - t0
+    return dt_s, 2 * E * N, 1
+
+
+def run_reference(args, w):
+    ws, rank = _dist()
+    if rank != 0:
+        return
+    rows = args.ref_rows
+    _cpu_oracle_path(w, 8)  # build / warm the oracle
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt_s, nbytes, threads = _cpu_oracle_path(w, rows, seed=i)
+        if i >= args.warmup:
+            times.append(dt_s)
+    t = sum(times) / len(times)
+    val = nbytes / t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": _config(w),
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows} of {w.rows} rows of each of the {w.ranks} ranks per step "
+                                   f"({w.ranks * rows * w.cols} elements), full path"},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(w):
+    return {"workload": f"{w.name}: {w.description}", "ranks": w.ranks, "rows": w.rows, "cols": w.cols,
+            "input_dtype": w.dtype, "scheme": w.scheme, "block": w.block, "gather_scheme": w.gather_scheme,
+            "gather_block": w.gather_block,
+            "l2": "inputs larger than L2 (%.0f MB of 16-bit input per step)" % (2 * w.elems_per_rank * w.ranks / 1e6)}
+
+
+def algorithmic_bytes(w):
+    """Bytes each kernel must move once per step (inputs read once, outputs
+    written once)."""
+    E, N = w.elems_per_rank, w.ranks
+
+    def codes(s):
+        return 0.5 if s == "int4_asym" else 1.0
+
+    def meta(s, b):
+        return {"taco_fp8": 1.0, "int8_sym": 4.0, "int4_asym": 4.0, "int8_asym": 4.0}[s] / b
+
+    k1 = N * E * (2 + codes(w.scheme) + meta(w.scheme, w.block))
+    k2 = N * E * (codes(w.scheme) + meta(w.scheme, w.block)) + E * 4
+    k3 = E * (4 + codes(w.gather_scheme) + meta(w.gather_scheme, w.gather_block))
+    k4 = E * (codes(w.gather_scheme) + meta(w.gather_scheme, w.gather_block) + 2)
+    return {"K1": k1, "K2": k2, "K3": k3, "K4": k4}
+
+
+def run_qta(args, w):
+    import torch
+
+    import quantized_tensor_activation_gb300 as qta
+
+    ws, rank = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    qta.build()
+    sch = qta.SCHEMES
+    N, R, C = w.ranks, w.rows, w.cols
+    in_dt = qta.BF16 if w.dtype == "bf16" else qta.FP16
+    tdt = w.torch_dtype
+    x = workloads.make_rank_inputs(w, device=dev, seed=args.seed)            # [N, R, C] resident in HBM
+    d_in = qta.desc(sch[w.scheme], w.block, R, C, batch=N)
+    d_sh = qta.desc(sch[w.scheme], w.block, R, C)
+    d_g = qta.desc(sch[w.gather_scheme], w.gather_block, R // N, C, batch=N)
+    q = qta.alloc_qtensor(d_in, dev)
+    g = qta.alloc_qtensor(d_g, dev)
+    shards = [q.shard(r) for r in range(N)]
+    ssum = torch.empty((R, C), dtype=torch.float32, device=dev)
+    y = torch.empty((R, C), dtype=tdt, device=dev)
+    stream = torch.cuda.current_stream()
+    taco1 = w.scheme == "taco_fp8"
+    taco2 = w.gather_scheme == "taco_fp8"
+
+    launches = [0]
+
+    def step(first=False, ev=None):
+        mode = qta.SCALE_CURRENT if first else qta.SCALE_DELAYED
+        if ev:
+            ev[0].record(stream)
+        qta.taco_compress(d_in, x, in_dt, q, mode)
+        if ev:
+            ev[1].record(stream)
+        if taco1:
+            qta.taco_update_scale(q.state, N)
+        if ev:
+            ev[2].record(stream)
+        qta.qar_reduce(d_sh, shards, 0, R, ssum)
+        if ev:
+            ev[3].record(stream)
+        qta.qar_requant(d_g, ssum, g, mode)
+        if ev:
+            ev[4].record(stream)
+        if taco2:
+            qta.taco_update_scale(g.state, N)
+        if ev:
+            ev[5].record(stream)
+        qta.taco_decompress(d_g, g, y, in_dt)
+        if ev:
+            ev[6].record(stream)
+        launches[0] += 4 + int(taco1) + int(taco2)
+
+    # warm-up (first step in CURRENT mode, the rest as timed)
+    step(first=True)
+    for _ in range(max(args.warmup, 3) - 1):
+        step()
+    torch.cuda.synchronize()
+    assert qta.qta_device_error() == 0
+
+    # ---- timed region: inputs resident in HBM
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    launches[0] = 0
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(ev=evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    n_launch = launches[0]
+    total_ms = t_start.elapsed_time(t_end)
+    per = {k: [] for k in ("K1", "U1", "K2", "K3", "U2", "K4")}
+    for e in evs:
+        for j, k in enumerate(per):
+            per[k].append(e[j].elapsed_time(e[j + 1]))
+    ms_step = total_ms / args.steps
+    if ws > 1:
+        t = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    assert qta.qta_device_error() == 0
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        xh = x.cpu().pin_memory()
+        yh = torch.empty((R, C), dtype=tdt).pin_memory()
+        xd = torch.empty_like(x)
+        torch.cuda.synchronize()
+
+        def e2e_step():
+            xd.copy_(xh, non_blocking=True)
+            qta.taco_compress(d_in, xd, in_dt, q, qta.SCALE_DELAYED)
+            if taco1:
+                qta.taco_update_scale(q.state, N)
+            qta.qar_reduce(d_sh, shards, 0, R, ssum)
+            qta.qar_requant(d_g, ssum, g, qta.SCALE_DELAYED)
+            if taco2:
+                qta.taco_update_scale(g.state, N)
+            qta.taco_decompress(d_g, g, y, in_dt)
+            yh.copy_(y, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k = max(3, args.steps // 2)
+        a.record(stream)
+        for _ in range(k):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / k
+        e2e = {"value": 2 * N * R * C / (e2e_ms * 1e-3) / 1e9 * ws, "unit": "GB/s",
+               "h2d_bytes_per_step": x.numel() * x.element_size(),
+               "d2h_bytes_per_step": y.numel() * y.element_size(), "ms_per_step": e2e_ms}
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    in_bytes = 2 * N * R * C
+    value = in_bytes / (ms_step * 1e-3) / 1e9 * ws
+    peak, peak_kind = _peaks()
+    alg = algorithmic_bytes(w)
+    kern = {}
+    for k, name in (("K1", "K1"), ("K2", "K2"), ("K3", "K3"), ("K4", "K4")):
+        ms = statistics.mean(per[k])
+        kern[name] = {"ms": ms, "gb_s": alg[name] / (ms * 1e-3) / 1e9,
+                      "frac_of_hbm": alg[name] / (ms * 1e-3) / 1e9 / peak,
+                      "input_gb_s": (in_bytes / (ms * 1e-3) / 1e9) if name == "K1" else None}
+    k1_ms = statistics.mean(per["K1"])
+    achieved = alg["K1"] / (k1_ms * 1e-3) / 1e9
+    tr = NCU_TRAFFIC.get(("taco_compress", w.name))
+    traffic = tr["bytes"] if tr and tr.get("src") == _src_digest() else None
+
+    cpu = None
+    if not args.no_cpu_baseline and ws == 1:
+        rows = args.cpu_rows
+        dt_s, nbytes, threads = _cpu_oracle_path(w, rows, seed=args.seed)
+        cpu = {"value": nbytes / dt_s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"{rows} of {w.rows} rows of each of the {w.ranks} ranks "
+                         f"({w.ranks * rows * w.cols} elements), full path, {dt_s:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": _config(w),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "kernel": "K1 taco_compress",
+                     "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes": alg["K1"]},
+        "kernels": kern,
+        "step_frac_of_hbm": sum(alg.values()) / (ms_step * 1e-3) / 1e9 / peak,
+        "cpu_baseline": cpu,
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": n_launch,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="gpt_tp", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="qta", choices=["qta", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-rows", type=int, default=4096)
+    ap.add_argument("--ref-rows", type=int, default=256)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_qta(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,466 @@
+// qta_api.cu -- the C ABI (include/qta.h): argument checks, TMA tensor maps,
+// grid sizing and launches; plus the per-tensor state kernel, the copy
+// kernel and the device error flags.
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/qta.h"
+#include "qta_launch.h"
+
+namespace qta {
+
+// Flags recorded by kernels whose bounded waits gave up.
+__device__ unsigned int g_error_flags;
+
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+
+struct DeviceInfo {
+    std::atomic<int> sms{0};
+    std::atomic<int> smem_per_sm{0};
+    std::atomic<unsigned int*> err{nullptr};
+};
+DeviceInfo g_dev[MAX_DEVICES];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+cudaError_t device_info(int* sms, int* smem_per_sm, unsigned int** err)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
+    DeviceInfo& d = g_dev[dev];
+    if (d.sms.load() == 0) {
+        int a = 0, b = 0;
+        if ((e = cudaDeviceGetAttribute(&a, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&b, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess)
+            return e;
+        void* p = nullptr;
+        if ((e = cudaGetSymbolAddress(&p, g_error_flags)) != cudaSuccess) return e;
+        d.smem_per_sm.store(b);
+        d.err.store(static_cast<unsigned int*>(p));
+        d.sms.store(a);
+    }
+    *sms = d.sms.load();
+    *smem_per_sm = d.smem_per_sm.load();
+    *err = d.err.load();
+    return cudaSuccess;
+}
+
+bool encoder_ready()
+{
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+// 2D map over rows of `inner` elements (row stride = inner * elem bytes),
+// box = {inner, 32 rows}.
+bool map_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t inner,
+            uint64_t rows, CUtensorMapSwizzle sw)
+{
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * elem_bytes};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(inner), 32};
+    cuuint32_t es[2] = {1, 1};
+    return g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Segments of fp32 (256 B) as two 128-B halves: dims {32, 2, M}, box {32,1,32}.
+bool map_f32(CUtensorMap* m, const void* base, uint64_t segs)
+{
+    cuuint64_t dims[3] = {32, 2, segs};
+    cuuint64_t strides[2] = {128, 256};
+    cuuint32_t box[3] = {32, 1, 32};
+    cuuint32_t es[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Map of a segment array of the given dtype (input of compress, output of
+// decompress).
+bool map_values(CUtensorMap* m, int dtype, const void* base, uint64_t segs)
+{
+    if (dtype == QTA_FP32) return map_f32(m, base, segs);
+    return map_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, 64, segs, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Map of the codes of a segment array (8-bit: 64 B per segment; 4-bit: 32 B).
+bool map_codes(CUtensorMap* m, int scheme, const void* base, uint64_t segs)
+{
+    if (scheme == QTA_INT4_ASYM_G128)
+        return map_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, 32, segs, CU_TENSOR_MAP_SWIZZLE_32B);
+    return map_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, 64, segs, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+FastDiv make_fastdiv(uint32_t d)
+{
+    FastDiv f;
+    f.d = d;
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    f.l = l;
+    f.m = static_cast<uint32_t>(((1ull << 32) * ((1ull << l) - d)) / d + 1);
+    return f;
+}
+
+int log2i(int v)
+{
+    int l = 0;
+    while ((1 << l) < v) ++l;
+    return l;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Scheme checks shared by every call: scheme / block combination and shape.
+qta_status check_desc(const qta_desc* d)
+{
+    if (!d) return QTA_ERR_INVALID_ARG;
+    switch (d->scheme) {
+    case QTA_TACO_FP8:
+        if (d->block != 64 && d->block != 128 && d->block != 256) return QTA_ERR_UNSUPPORTED;
+        break;
+    case QTA_INT8_SYM_B64:
+        if (d->block != 64) return QTA_ERR_UNSUPPORTED;
+        break;
+    case QTA_INT4_ASYM_G128:
+    case QTA_INT8_ASYM_G128:
+        if (d->block != 128) return QTA_ERR_UNSUPPORTED;
+        break;
+    default: return QTA_ERR_UNSUPPORTED;
+    }
+    if (d->batch < 0 || d->rows < 0 || d->cols < 0) return QTA_ERR_INVALID_ARG;
+    if (d->cols % d->block) return QTA_ERR_INVALID_ARG;
+    // element count must leave fewer than 2^31 segments
+    const long double n = (long double)d->batch * (long double)d->rows * (long double)d->cols;
+    if (n / 64.0L >= 2147483648.0L) return QTA_ERR_UNSUPPORTED;
+    return QTA_OK;
+}
+
+int64_t n_elems(const qta_desc* d) { return d->batch * d->rows * d->cols; }
+
+int lanes_of(const qta_desc* d)
+{
+    if (d->scheme == QTA_TACO_FP8) return d->block / 64;
+    if (d->scheme == QTA_INT8_SYM_B64) return 1;
+    return 2;
+}
+
+// Checks of one quantized tensor's buffers for a descriptor.
+qta_status check_qtensor(const qta_desc* d, const qta_qtensor* q)
+{
+    if (!q || !q->codes || !q->scales) return QTA_ERR_INVALID_ARG;
+    if (!aligned(q->codes, 16)) return QTA_ERR_ALIGNMENT;
+    if (d->scheme == QTA_INT8_SYM_B64 && !aligned(q->scales, 4)) return QTA_ERR_ALIGNMENT;
+    if (d->scheme == QTA_INT4_ASYM_G128 || d->scheme == QTA_INT8_ASYM_G128) {
+        if (!q->zeros) return QTA_ERR_INVALID_ARG;
+        if (!aligned(q->scales, 2) || !aligned(q->zeros, 2)) return QTA_ERR_ALIGNMENT;
+    }
+    if (d->scheme == QTA_TACO_FP8) {
+        if (!q->state) return QTA_ERR_INVALID_ARG;
+        if (!aligned(q->state, 4)) return QTA_ERR_ALIGNMENT;
+    }
+    return QTA_OK;
+}
+
+int grid_for(int n_warp_tiles, int warps, int smem, int sms, int smem_per_sm)
+{
+    int per_sm = smem_per_sm / (smem + 1024);
+    if (per_sm < 1) per_sm = 1;
+    const int ctas = (n_warp_tiles + warps - 1) / warps;
+    const int cap = sms * per_sm;
+    return ctas < cap ? ctas : cap;
+}
+
+qta_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QTA_OK : QTA_ERR_CUDA; }
+
+}  // namespace
+
+cudaError_t ensure_smem_attr(const void* func, int smem, std::atomic<unsigned>* done_mask)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned bit = dev < 32 ? (1u << dev) : 0u;
+    if (bit && (done_mask->load() & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess && bit) done_mask->fetch_or(bit);
+    return e;
+}
+
+__global__ void state_kernel(float* state, long long n, int op)
+{
+    const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    if (t >= n) return;
+    if (op == STATE_UPDATE) {
+        state[2 * t] = scale_from_amax(state[2 * t + 1]);
+        state[2 * t + 1] = 0.0f;
+    } else if (op == STATE_RESET_AMAX) {
+        state[2 * t + 1] = 0.0f;
+    } else {
+        state[2 * t] = scale_from_amax(state[2 * t + 1]);
+    }
+}
+
+// Grid-stride 16-byte copy; each thread keeps four loads in flight.
+__global__ void __launch_bounds__(512) copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                   long long n16)
+{
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n16; i += 4 * stride) {
+        const uint4 a = __ldcs(src + i), b = __ldcs(src + i + stride);
+        const uint4 c = __ldcs(src + i + 2 * stride), d = __ldcs(src + i + 3 * stride);
+        __stcs(dst + i, a);
+        __stcs(dst + i + stride, b);
+        __stcs(dst + i + 2 * stride, c);
+        __stcs(dst + i + 3 * stride, d);
+    }
+    for (; i < n16; i += stride) __stcs(dst + i, __ldcs(src + i));
+}
+
+cudaError_t launch_state(float* state, long long n, int op, cudaStream_t stream)
+{
+    if (n <= 0) return cudaSuccess;
+    const int threads = 128;
+    const long long blocks = (n + threads - 1) / threads;
+    state_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(state, n, op);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy(const void* src, void* dst, size_t bytes, int grid, cudaStream_t stream)
+{
+    copy_kernel<<<grid, 512, 0, stream>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst),
+                                          static_cast<long long>(bytes / 16));
+    return cudaGetLastError();
+}
+
+}  // namespace qta
+
+using namespace qta;
+
+extern "C" {
+
+size_t qta_codes_bytes(const qta_desc* d)
+{
+    if (check_desc(d) != QTA_OK) return 0;
+    const size_t n = static_cast<size_t>(n_elems(d));
+    return d->scheme == QTA_INT4_ASYM_G128 ? n / 2 : n;
+}
+
+size_t qta_scales_bytes(const qta_desc* d)
+{
+    if (check_desc(d) != QTA_OK) return 0;
+    const size_t nb = static_cast<size_t>(n_elems(d)) / d->block;
+    if (d->scheme == QTA_TACO_FP8) return nb;
+    if (d->scheme == QTA_INT8_SYM_B64) return nb * 4;
+    return nb * 2;
+}
+
+size_t qta_zeros_bytes(const qta_desc* d)
+{
+    if (check_desc(d) != QTA_OK) return 0;
+    if (d->scheme != QTA_INT4_ASYM_G128 && d->scheme != QTA_INT8_ASYM_G128) return 0;
+    return static_cast<size_t>(n_elems(d)) / d->block * 2;
+}
+
+size_t qta_state_bytes(const qta_desc* d)
+{
+    if (check_desc(d) != QTA_OK) return 0;
+    return d->scheme == QTA_TACO_FP8 ? static_cast<size_t>(d->batch) * 2 * sizeof(float) : 0;
+}
+
+static qta_status compress_impl(const qta_desc* d, const void* x, int32_t x_dtype, const qta_qtensor* out,
+                                int32_t mode, qta_stream_t stream)
+{
+    qta_status st = check_desc(d);
+    if (st != QTA_OK) return st;
+    if (x_dtype != QTA_BF16 && x_dtype != QTA_FP16 && x_dtype != QTA_FP32) return QTA_ERR_UNSUPPORTED;
+    if (d->scheme == QTA_TACO_FP8 && mode != QTA_SCALE_DELAYED && mode != QTA_SCALE_CURRENT)
+        return QTA_ERR_INVALID_ARG;
+    if (n_elems(d) == 0) return QTA_OK;
+    if (!x) return QTA_ERR_INVALID_ARG;
+    if (!aligned(x, 16)) return QTA_ERR_ALIGNMENT;
+    if ((st = check_qtensor(d, out)) != QTA_OK) return st;
+    if (!encoder_ready()) return QTA_ERR_CUDA;
+    int sms = 0, smem_sm = 0;
+    unsigned int* err = nullptr;
+    if (device_info(&sms, &smem_sm, &err) != cudaSuccess) return QTA_ERR_CUDA;
+
+    const int64_t segs = n_elems(d) / 64;
+    CompressParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (!map_values(&p.in_map, x_dtype, x, segs)) return QTA_ERR_CUDA;
+    if (!map_codes(&p.out_map, d->scheme, out->codes, segs)) return QTA_ERR_CUDA;
+    p.scales = out->scales;
+    p.zeros = out->zeros;
+    p.state = out->state;
+    p.err = err;
+    p.M = static_cast<int>(segs);
+    p.n_warp_tiles = static_cast<int>((segs + 31) / 32);
+    p.lanes_per_block = lanes_of(d);
+    p.lanes_log2 = log2i(p.lanes_per_block);
+    p.seg_per_tensor = make_fastdiv(static_cast<uint32_t>(d->rows * d->cols / 64));
+    const int sch = d->scheme;  // qta_scheme values equal the kernel scheme kinds
+    const int grid = grid_for(p.n_warp_tiles, compress_warps(), compress_smem(x_dtype, sch), sms, smem_sm);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (d->scheme == QTA_TACO_FP8 && mode == QTA_SCALE_CURRENT) {
+        cudaError_t e = launch_state(out->state, d->batch, STATE_RESET_AMAX, s);
+        if (e == cudaSuccess) e = launch_compress(x_dtype, sch, true, p, grid, s);
+        if (e == cudaSuccess) e = launch_state(out->state, d->batch, STATE_SET_SCALE, s);
+        if (e != cudaSuccess) return QTA_ERR_CUDA;
+    }
+    return cuda_status(launch_compress(x_dtype, sch, false, p, grid, s));
+}
+
+qta_status taco_compress(const qta_desc* d, const void* x, int32_t x_dtype, const qta_qtensor* out, int32_t mode,
+                         qta_stream_t stream)
+{
+    return compress_impl(d, x, x_dtype, out, mode, stream);
+}
+
+qta_status qar_requant(const qta_desc* d, const float* sum, const qta_qtensor* out, int32_t mode,
+                       qta_stream_t stream)
+{
+    return compress_impl(d, sum, QTA_FP32, out, mode, stream);
+}
+
+qta_status taco_decompress(const qta_desc* d, const qta_qtensor* in, void* y, int32_t y_dtype, qta_stream_t stream)
+{
+    qta_status st = check_desc(d);
+    if (st != QTA_OK) return st;
+    if (y_dtype != QTA_BF16 && y_dtype != QTA_FP16 && y_dtype != QTA_FP32) return QTA_ERR_UNSUPPORTED;
+    if (n_elems(d) == 0) return QTA_OK;
+    if (!y) return QTA_ERR_INVALID_ARG;
+    if (!aligned(y, 16)) return QTA_ERR_ALIGNMENT;
+    if ((st = check_qtensor(d, in)) != QTA_OK) return st;
+    if (!encoder_ready()) return QTA_ERR_CUDA;
+    int sms = 0, smem_sm = 0;
+    unsigned int* err = nullptr;
+    if (device_info(&sms, &smem_sm, &err) != cudaSuccess) return QTA_ERR_CUDA;
+
+    const int64_t segs = n_elems(d) / 64;
+    DecompressParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (!map_codes(&p.in_map, d->scheme, in->codes, segs)) return QTA_ERR_CUDA;
+    if (!map_values(&p.out_map, y_dtype, y, segs)) return QTA_ERR_CUDA;
+    p.scales = in->scales;
+    p.zeros = in->zeros;
+    p.state = in->state;
+    p.err = err;
+    p.M = static_cast<int>(segs);
+    p.n_warp_tiles = static_cast<int>((segs + 31) / 32);
+    p.lanes_per_block = lanes_of(d);
+    p.lanes_log2 = log2i(p.lanes_per_block);
+    p.inv_block = 1.0f / static_cast<float>(d->block);
+    p.seg_per_tensor = make_fastdiv(static_cast<uint32_t>(d->rows * d->cols / 64));
+    const int grid = grid_for(p.n_warp_tiles, decompress_warps(), decompress_smem(d->scheme, y_dtype), sms, smem_sm);
+    return cuda_status(launch_decompress(d->scheme, y_dtype, p, grid, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+qta_status qar_reduce(const qta_desc* d, const qta_qtensor* shards, int32_t n_ranks, int64_t row_begin,
+                      int64_t row_end, float* sum_out, qta_stream_t stream)
+{
+    qta_status st = check_desc(d);
+    if (st != QTA_OK) return st;
+    if (d->batch != 1) return QTA_ERR_INVALID_ARG;
+    if (n_ranks < 1) return QTA_ERR_INVALID_ARG;
+    if (n_ranks > MAX_RANKS) return QTA_ERR_UNSUPPORTED;
+    if (row_begin < 0 || row_end < row_begin || row_end > d->rows) return QTA_ERR_INVALID_ARG;
+    if (!shards) return QTA_ERR_INVALID_ARG;
+    if (row_end == row_begin || d->cols == 0) return QTA_OK;
+    if (!sum_out) return QTA_ERR_INVALID_ARG;
+    if (!aligned(sum_out, 16)) return QTA_ERR_ALIGNMENT;
+    for (int r = 0; r < n_ranks; ++r)
+        if ((st = check_qtensor(d, &shards[r])) != QTA_OK) return st;
+    if (!encoder_ready()) return QTA_ERR_CUDA;
+    int sms = 0, smem_sm = 0;
+    unsigned int* err = nullptr;
+    if (device_info(&sms, &smem_sm, &err) != cudaSuccess) return QTA_ERR_CUDA;
+
+    const int64_t segs = n_elems(d) / 64;
+    const int64_t per_row = d->cols / 64;
+    ReduceParams p;
+    std::memset(&p, 0, sizeof(p));
+    for (int r = 0; r < n_ranks; ++r) {
+        if (!map_codes(&p.in_map[r], d->scheme, shards[r].codes, segs)) return QTA_ERR_CUDA;
+        p.scales[r] = shards[r].scales;
+        p.zeros[r] = shards[r].zeros;
+        p.state[r] = shards[r].state;
+    }
+    const int64_t m_out = (row_end - row_begin) * per_row;
+    if (!map_f32(&p.out_map, sum_out, m_out)) return QTA_ERR_CUDA;
+    p.err = err;
+    p.n_ranks = n_ranks;
+    p.seg_begin = static_cast<int>(row_begin * per_row);
+    p.M_out = static_cast<int>(m_out);
+    p.n_warp_tiles = static_cast<int>((m_out + 31) / 32);
+    p.lanes_per_block = lanes_of(d);
+    p.lanes_log2 = log2i(p.lanes_per_block);
+    p.inv_block = 1.0f / static_cast<float>(d->block);
+    const int grid = grid_for(p.n_warp_tiles, reduce_warps(), reduce_smem(d->scheme), sms, smem_sm);
+    return cuda_status(launch_reduce(d->scheme, p, grid, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+qta_status taco_update_scale(float* state, int64_t n_tensors, qta_stream_t stream)
+{
+    if (n_tensors < 0) return QTA_ERR_INVALID_ARG;
+    if (n_tensors == 0) return QTA_OK;
+    if (!state) return QTA_ERR_INVALID_ARG;
+    if (!aligned(state, 4)) return QTA_ERR_ALIGNMENT;
+    return cuda_status(launch_state(state, n_tensors, STATE_UPDATE, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+qta_status qta_copy(const void* src, void* dst, size_t bytes, qta_stream_t stream)
+{
+    if (bytes == 0) return QTA_OK;
+    if (!src || !dst) return QTA_ERR_INVALID_ARG;
+    if (!aligned(src, 16) || !aligned(dst, 16) || (bytes & 15)) return QTA_ERR_ALIGNMENT;
+    int sms = 0, smem_sm = 0;
+    unsigned int* err = nullptr;
+    if (device_info(&sms, &smem_sm, &err) != cudaSuccess) return QTA_ERR_CUDA;
+    return cuda_status(launch_copy(src, dst, bytes, sms * 4, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+qta_status qta_device_error(uint32_t* flags, int32_t clear)
+{
+    if (!flags) return QTA_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return QTA_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_error_flags, sizeof(v)) != cudaSuccess) return QTA_ERR_CUDA;
+    *flags = v;
+    if (clear && v) {
+        const unsigned int z = 0;
+        if (cudaMemcpyToSymbol(g_error_flags, &z, sizeof(z)) != cudaSuccess) return QTA_ERR_CUDA;
+    }
+    return QTA_OK;
+}
+
+const char* qta_status_string(qta_status s)
+{
+    switch (s) {
+    case QTA_OK: return "QTA_OK";
+    case QTA_ERR_INVALID_ARG: return "QTA_ERR_INVALID_ARG";
+    case QTA_ERR_ALIGNMENT: return "QTA_ERR_ALIGNMENT";
+    case QTA_ERR_UNSUPPORTED: return "QTA_ERR_UNSUPPORTED";
+    case QTA_ERR_CUDA: return "QTA_ERR_CUDA";
+    default: return "QTA_ERR_UNKNOWN";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,53 @@
+// qta_compress.cu -- instantiations and launcher of the compress kernels
+// (taco_compress, qar_requant and the CURRENT-mode amax pre-pass).
+#include "qta_launch.h"
+
+namespace qta {
+
+int compress_warps() { return CompressCfg<IN_BF16, S_TACO>::WARPS; }
+
+int compress_smem(int in_kind, int scheme)
+{
+    const bool f32 = in_kind == IN_FP32;
+    const bool a4 = scheme == S_ASYM4;
+    if (f32) return a4 ? CompressCfg<IN_FP32, S_ASYM4>::SMEM : CompressCfg<IN_FP32, S_TACO>::SMEM;
+    return a4 ? CompressCfg<IN_BF16, S_ASYM4>::SMEM : CompressCfg<IN_BF16, S_TACO>::SMEM;
+}
+
+template <int IN, int SCH, bool AMAX>
+static cudaError_t launch_one(const CompressParams& p, int grid, cudaStream_t stream)
+{
+    using C = CompressCfg<IN, SCH>;
+    static std::atomic<unsigned> done{0};
+    auto fn = compress_kernel<IN, SCH, AMAX>;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(fn), C::SMEM, &done);
+    if (e != cudaSuccess) return e;
+    fn<<<grid, C::WARPS * 32, C::SMEM, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <int IN>
+static cudaError_t launch_in(int scheme, bool amax_only, const CompressParams& p, int grid, cudaStream_t s)
+{
+    switch (scheme) {
+    case S_TACO:
+        return amax_only ? launch_one<IN, S_TACO, true>(p, grid, s) : launch_one<IN, S_TACO, false>(p, grid, s);
+    case S_INT8SYM: return launch_one<IN, S_INT8SYM, false>(p, grid, s);
+    case S_ASYM4: return launch_one<IN, S_ASYM4, false>(p, grid, s);
+    case S_ASYM8: return launch_one<IN, S_ASYM8, false>(p, grid, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_compress(int in_kind, int scheme, bool amax_only, const CompressParams& p, int grid,
+                            cudaStream_t stream)
+{
+    switch (in_kind) {
+    case IN_BF16: return launch_in<IN_BF16>(scheme, amax_only, p, grid, stream);
+    case IN_FP16: return launch_in<IN_FP16>(scheme, amax_only, p, grid, stream);
+    case IN_FP32: return launch_in<IN_FP32>(scheme, amax_only, p, grid, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace qta

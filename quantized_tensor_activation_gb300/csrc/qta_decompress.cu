@@ -1,0 +1,77 @@
+// qta_decompress.cu -- instantiations and launchers of the decompress and
+// dequantize-reduce kernels.
+#include "qta_launch.h"
+
+namespace qta {
+
+int decompress_warps() { return DecompressCfg<S_TACO, IN_BF16>::WARPS; }
+int reduce_warps() { return ReduceCfg<S_TACO>::WARPS; }
+
+int decompress_smem(int scheme, int out_kind)
+{
+    const bool f32 = out_kind == IN_FP32;
+    const bool a4 = scheme == S_ASYM4;
+    if (f32) return a4 ? DecompressCfg<S_ASYM4, IN_FP32>::SMEM : DecompressCfg<S_TACO, IN_FP32>::SMEM;
+    return a4 ? DecompressCfg<S_ASYM4, IN_BF16>::SMEM : DecompressCfg<S_TACO, IN_BF16>::SMEM;
+}
+
+int reduce_smem(int scheme) { return scheme == S_ASYM4 ? ReduceCfg<S_ASYM4>::SMEM : ReduceCfg<S_TACO>::SMEM; }
+
+template <int SCH, int OUT>
+static cudaError_t launch_d(const DecompressParams& p, int grid, cudaStream_t stream)
+{
+    using C = DecompressCfg<SCH, OUT>;
+    static std::atomic<unsigned> done{0};
+    auto fn = decompress_kernel<SCH, OUT>;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(fn), C::SMEM, &done);
+    if (e != cudaSuccess) return e;
+    fn<<<grid, C::WARPS * 32, C::SMEM, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <int SCH>
+static cudaError_t launch_d_out(int out_kind, const DecompressParams& p, int grid, cudaStream_t s)
+{
+    switch (out_kind) {
+    case IN_BF16: return launch_d<SCH, IN_BF16>(p, grid, s);
+    case IN_FP16: return launch_d<SCH, IN_FP16>(p, grid, s);
+    case IN_FP32: return launch_d<SCH, IN_FP32>(p, grid, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_decompress(int scheme, int out_kind, const DecompressParams& p, int grid, cudaStream_t stream)
+{
+    switch (scheme) {
+    case S_TACO: return launch_d_out<S_TACO>(out_kind, p, grid, stream);
+    case S_INT8SYM: return launch_d_out<S_INT8SYM>(out_kind, p, grid, stream);
+    case S_ASYM4: return launch_d_out<S_ASYM4>(out_kind, p, grid, stream);
+    case S_ASYM8: return launch_d_out<S_ASYM8>(out_kind, p, grid, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int SCH>
+static cudaError_t launch_r(const ReduceParams& p, int grid, cudaStream_t stream)
+{
+    using C = ReduceCfg<SCH>;
+    static std::atomic<unsigned> done{0};
+    auto fn = reduce_kernel<SCH>;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(fn), C::SMEM, &done);
+    if (e != cudaSuccess) return e;
+    fn<<<grid, C::WARPS * 32, C::SMEM, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_reduce(int scheme, const ReduceParams& p, int grid, cudaStream_t stream)
+{
+    switch (scheme) {
+    case S_TACO: return launch_r<S_TACO>(p, grid, stream);
+    case S_INT8SYM: return launch_r<S_INT8SYM>(p, grid, stream);
+    case S_ASYM4: return launch_r<S_ASYM4>(p, grid, stream);
+    case S_ASYM8: return launch_r<S_ASYM8>(p, grid, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace qta

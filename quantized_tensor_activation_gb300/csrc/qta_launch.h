@@ -1,0 +1,31 @@
+// qta_launch.h -- host-side launchers of the codec kernels (internal).
+#pragma once
+
+#include <atomic>
+
+#include "qta_kernels.cuh"
+
+namespace qta {
+
+// Dynamic shared memory a kernel needs (bytes).
+int compress_smem(int in_kind, int scheme);
+int decompress_smem(int scheme, int out_kind);
+int reduce_smem(int scheme);
+
+// Warps per CTA of each kernel family.
+int compress_warps();
+int decompress_warps();
+int reduce_warps();
+
+cudaError_t launch_compress(int in_kind, int scheme, bool amax_only, const CompressParams& p, int grid,
+                            cudaStream_t stream);
+cudaError_t launch_decompress(int scheme, int out_kind, const DecompressParams& p, int grid,
+                              cudaStream_t stream);
+cudaError_t launch_reduce(int scheme, const ReduceParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_state(float* state, long long n, int op, cudaStream_t stream);
+cudaError_t launch_copy(const void* src, void* dst, size_t bytes, int grid, cudaStream_t stream);
+
+// Per-device one-time setting of the dynamic shared-memory limit of a kernel.
+cudaError_t ensure_smem_attr(const void* func, int smem, std::atomic<unsigned>* done_mask);
+
+}  // namespace qta

@@ -1,0 +1,109 @@
+"""The C ABI library builds, loads and exports every call the header
+declares; host-side argument checks return their status codes without a GPU
+(no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import quantized_tensor_activation_gb300 as qta
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    qta.build()
+    return qta.lib()
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z_0-9]*\s*\*?\s+\**([a-z_][a-z_0-9]*)\s*\(",
+                             text, flags=re.M):
+            names.append(m.group(1))
+    return names
+
+
+def test_exports_every_declared_call(L):
+    names = _declared_functions()
+    for must in ("taco_compress", "taco_decompress", "qar_reduce", "qar_requant", "taco_update_scale",
+                 "qta_copy", "qta_device_error", "qta_status_string", "qta_codes_bytes"):
+        assert must in names
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_sizes(L):
+    d = qta.desc("taco_fp8", 128, 256, 1024, batch=4)
+    assert (qta.codes_bytes(d), qta.scales_bytes(d), qta.zeros_bytes(d), qta.state_bytes(d)) == \
+        (1048576, 8192, 0, 32)
+    d = qta.desc("int8_sym", 64, 16, 512)
+    assert (qta.codes_bytes(d), qta.scales_bytes(d), qta.zeros_bytes(d), qta.state_bytes(d)) == \
+        (8192, 512, 0, 0)
+    d = qta.desc("int4_asym", 128, 8, 256, batch=2)
+    assert (qta.codes_bytes(d), qta.scales_bytes(d), qta.zeros_bytes(d)) == (2048, 64, 64)
+    assert qta.codes_bytes(qta.desc("taco_fp8", 100, 1, 200)) == 0   # invalid block
+
+
+def _c(L, name, *args):
+    return getattr(L, name)(*args)
+
+
+def test_argument_checks(L):
+    D = lambda *a: ctypes.byref(qta.desc(*a))
+    Q = lambda c=16, s=16, z=16, st=16: ctypes.byref(qta.QTensorC(c, s, z, st))
+    OK, INV, ALN, UNS = qta.QTA_OK, qta.QTA_ERR_INVALID_ARG, qta.QTA_ERR_ALIGNMENT, qta.QTA_ERR_UNSUPPORTED
+    # descriptor problems
+    assert L.taco_compress(None, 16, 0, Q(), 0, None) == INV
+    assert L.taco_compress(D(9, 128, 4, 128), 16, 0, Q(), 0, None) == UNS
+    assert L.taco_compress(D(0, 96, 4, 192), 16, 0, Q(), 0, None) == UNS
+    assert L.taco_compress(D(1, 128, 4, 128), 16, 0, Q(), 0, None) == UNS
+    assert L.taco_compress(D(0, 128, 4, 192), 16, 0, Q(), 0, None) == INV      # cols % block
+    assert L.taco_compress(D(0, 128, -1, 128), 16, 0, Q(), 0, None) == INV
+    assert L.taco_compress(D(0, 128, 4, 128), 16, 7, Q(), 0, None) == UNS      # dtype
+    assert L.taco_compress(D(0, 128, 4, 128), 16, 0, Q(), 5, None) == INV      # mode
+    # pointer problems
+    assert L.taco_compress(D(0, 128, 4, 128), None, 0, Q(), 0, None) == INV
+    assert L.taco_compress(D(0, 128, 4, 128), 24, 0, Q(), 0, None) == ALN
+    assert L.taco_compress(D(0, 128, 4, 128), 16, 0, Q(c=40), 0, None) == ALN
+    assert L.taco_compress(D(0, 128, 4, 128), 16, 0, Q(st=None), 0, None) == INV
+    assert L.taco_compress(D(0, 128, 4, 128), 16, 0, Q(st=18), 0, None) == ALN
+    assert L.taco_compress(D(2, 128, 4, 128), 16, 1, Q(z=None), 0, None) == INV
+    assert L.taco_compress(D(2, 128, 4, 128), 16, 1, Q(s=17), 0, None) == ALN
+    assert L.taco_compress(D(1, 64, 4, 128), 16, 1, Q(s=18), 0, None) == ALN
+    # too many segments for 32-bit tile coordinates
+    assert L.taco_compress(D(0, 128, 1 << 20, 1 << 17), 16, 0, Q(), 0, None) == UNS
+    # empty tensors are a no-op
+    assert L.taco_compress(D(0, 128, 0, 128), None, 0, None, 0, None) == OK
+    assert L.taco_decompress(D(0, 128, 4, 0), None, None, 0, None) == OK
+    # decompress / reduce / requant / update / copy checks
+    assert L.taco_decompress(D(0, 128, 4, 128), Q(), 24, 0, None) == ALN
+    assert L.taco_decompress(D(0, 128, 4, 128), Q(), 16, 3, None) == UNS
+    arr = (qta.QTensorC * 2)(qta.QTensorC(16, 16, 16, 16), qta.QTensorC(16, 16, 16, 16))
+    assert L.qar_reduce(D(0, 128, 4, 128, 2), arr, 2, 0, 4, 16, None) == INV   # batch must be 1
+    assert L.qar_reduce(D(0, 128, 4, 128), arr, 0, 0, 4, 16, None) == INV
+    assert L.qar_reduce(D(0, 128, 4, 128), arr, 17, 0, 4, 16, None) == UNS
+    assert L.qar_reduce(D(0, 128, 4, 128), arr, 2, 3, 2, 16, None) == INV
+    assert L.qar_reduce(D(0, 128, 4, 128), arr, 2, 0, 5, 16, None) == INV
+    assert L.qar_reduce(D(0, 128, 4, 128), arr, 2, 2, 2, 16, None) == OK      # empty range
+    assert L.qar_reduce(D(0, 128, 4, 128), arr, 2, 0, 4, 24, None) == ALN
+    assert L.qar_reduce(D(0, 128, 4, 128), None, 2, 0, 4, 16, None) == INV
+    bad = (qta.QTensorC * 2)(qta.QTensorC(16, 16, 16, 16), qta.QTensorC(8, 16, 16, 16))
+    assert L.qar_reduce(D(0, 128, 4, 128), bad, 2, 0, 4, 16, None) == ALN
+    assert L.qar_requant(D(0, 128, 4, 128), 20, Q(), 0, None) == ALN
+    assert L.taco_update_scale(None, 3, None) == INV
+    assert L.taco_update_scale(18, 3, None) == ALN
+    assert L.taco_update_scale(None, 0, None) == OK
+    assert L.taco_update_scale(16, -1, None) == INV
+    assert L.qta_copy(16, 32, 24, None) == ALN
+    assert L.qta_copy(None, 32, 32, None) == INV
+    assert L.qta_copy(16, 32, 0, None) == OK
+    assert L.qta_device_error(None, 0) == INV
+    assert L.qta_status_string(qta.QTA_ERR_ALIGNMENT) == b"QTA_ERR_ALIGNMENT"

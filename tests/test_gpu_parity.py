@@ -1,0 +1,266 @@
+"""GPU parity: every kernel through the C ABI against the CPU oracle on the
+same seeded inputs, element by element.  Codes, scales, zeros and per-tensor
+state must be bit-exact; FP32 sums and decompressed values are expected
+bit-exact and must be within max relative error 1e-5.
+
+Shapes cover one block, one row, ragged tails (segment counts that are not a
+multiple of the 32-segment warp tile), tensor boundaries inside a warp tile,
+several tiles per warp (the stage ring wraps), every block size, every input
+and output dtype, both scale modes, and 1..16 ranks."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+import quantized_tensor_activation_gb300 as qta
+from gpu_util import (BLOCK_OF, ORC_DT, ORC_SCH, assert_close_f32, assert_same, compare_qtensor, device,
+                      gpu_compress, oracle_bits_in, oracle_compress, random_values, to_dtype_cpu)
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = [qta.BF16, qta.FP16, qta.FP32]
+# (batch, rows, cols): one block, one row, ragged tiles with tensor boundaries
+# inside warp tiles, many CTAs, and enough warp tiles to wrap the stage ring.
+SHAPES = [(1, 1, 256), (3, 5, 512), (2, 37, 768), (4, 640, 1024), (4, 1024, 4096)]
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return device()
+
+
+def _x(rng, batch, rows, cols, dtype, kind="mixed", scale=1.0):
+    return to_dtype_cpu(random_values(rng, (batch, rows, cols), kind, scale), dtype)
+
+
+@pytest.mark.parametrize("B", [64, 128, 256])
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", SHAPES)
+def test_taco_compress_current(dev, B, dtype, shape):
+    batch, rows, cols = shape
+    rng = np.random.default_rng(hash((B, dtype, shape)) % 2 ** 32)
+    xt = _x(rng, batch, rows, cols, dtype)
+    _, q = gpu_compress(qta.TACO_FP8, B, xt, dtype, batch, rows, cols, qta.SCALE_CURRENT, dev=dev)
+    ref = oracle_compress(qta.TACO_FP8, B, xt, dtype, batch, rows, cols, orc.CURRENT)
+    torch.cuda.synchronize()
+    compare_qtensor("taco", q, ref)
+
+
+@pytest.mark.parametrize("B", [128, 256])
+@pytest.mark.parametrize("dtype", [qta.BF16, qta.FP32])
+def test_taco_compress_delayed_stale_scale(dev, B, dtype):
+    # a previous-step scale far too small and one far too large: exercises
+    # block-scale saturation (ratio > 448), codes saturating at 448, and the
+    # r_b -> 2^-9 floor; amax accumulates onto the incoming value.
+    batch, rows, cols = 3, 40, 1024
+    rng = np.random.default_rng(B + dtype)
+    xt = _x(rng, batch, rows, cols, dtype)
+    state = np.array([1e-6, 0.5, 1e3, 0.0, 0.01, 7.0], dtype=np.float32)
+    _, q = gpu_compress(qta.TACO_FP8, B, xt, dtype, batch, rows, cols, qta.SCALE_DELAYED, state=state, dev=dev)
+    ref = oracle_compress(qta.TACO_FP8, B, xt, dtype, batch, rows, cols, orc.DELAYED, state=state)
+    torch.cuda.synchronize()
+    compare_qtensor("taco delayed", q, ref)
+    assert (q.scales.cpu().numpy() == 0x7E).any()          # saturated block scales occurred
+
+
+@pytest.mark.parametrize("scheme", [qta.INT8_SYM_B64, qta.INT4_ASYM_G128, qta.INT8_ASYM_G128])
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", SHAPES)
+def test_int_compress(dev, scheme, dtype, shape):
+    batch, rows, cols = shape
+    B = BLOCK_OF[scheme]
+    rng = np.random.default_rng(hash((scheme, dtype, shape)) % 2 ** 32)
+    xt = _x(rng, batch, rows, cols, dtype, kind="t")
+    _, q = gpu_compress(scheme, B, xt, dtype, batch, rows, cols, dev=dev)
+    ref = oracle_compress(scheme, B, xt, dtype, batch, rows, cols)
+    torch.cuda.synchronize()
+    compare_qtensor(f"scheme {scheme}", q, ref)
+
+
+def test_asym_fp32_extreme_range(dev):
+    # fp32 sums beyond the fp16 range: the scale clamps at 65504 and the zero-
+    # point at -65504; constant groups give s = 0.
+    rng = np.random.default_rng(7)
+    x = (rng.standard_normal((2, 8, 512)) * 1e5).astype(np.float32)
+    x[0, 3] = 2.5
+    xt = torch.from_numpy(x)
+    for scheme in (qta.INT4_ASYM_G128, qta.INT8_ASYM_G128):
+        _, q = gpu_compress(scheme, 128, xt, qta.FP32, 2, 8, 512, dev=dev)
+        ref = oracle_compress(scheme, 128, xt, qta.FP32, 2, 8, 512)
+        torch.cuda.synchronize()
+        compare_qtensor("asym extreme", q, ref)
+
+
+def test_zero_and_constant_tensors(dev):
+    for scheme, B in ((qta.TACO_FP8, 128), (qta.INT8_SYM_B64, 64), (qta.INT4_ASYM_G128, 128)):
+        for val in (0.0, -3.0):
+            xt = torch.full((2, 3, 256), val, dtype=torch.bfloat16)
+            _, q = gpu_compress(scheme, B, xt, qta.BF16, 2, 3, 256, dev=dev)
+            ref = oracle_compress(scheme, B, xt, qta.BF16, 2, 3, 256)
+            torch.cuda.synchronize()
+            compare_qtensor(f"const {val}", q, ref)
+
+
+@pytest.mark.parametrize("scheme,B", [(qta.TACO_FP8, 64), (qta.TACO_FP8, 128), (qta.TACO_FP8, 256),
+                                      (qta.INT8_SYM_B64, 64), (qta.INT4_ASYM_G128, 128),
+                                      (qta.INT8_ASYM_G128, 128)])
+@pytest.mark.parametrize("out_dtype", DTYPES)
+@pytest.mark.parametrize("shape", [(1, 1, 256), (3, 5, 512), (4, 640, 1024), (2, 2048, 4096)])
+def test_decompress(dev, scheme, B, out_dtype, shape):
+    batch, rows, cols = shape
+    rng = np.random.default_rng(hash((scheme, B, out_dtype, shape)) % 2 ** 32)
+    xt = _x(rng, batch, rows, cols, qta.FP32, kind="mixed")
+    # the oracle's codes are the decompressor's input on both sides
+    c, s, z, st = oracle_compress(scheme, B, xt, qta.FP32, batch, rows, cols)
+    d = qta.desc(scheme, B, rows, cols, batch=batch)
+    q = qta.QTensor(d, torch.from_numpy(c.view(np.uint8)).to(dev), torch.from_numpy(s.view(np.uint8)).to(dev),
+                    None if z is None else torch.from_numpy(z.view(np.uint8)).to(dev),
+                    None if st is None else torch.from_numpy(st).to(dev))
+    y = torch.empty((batch, rows, cols), dtype={0: torch.bfloat16, 1: torch.float16, 2: torch.float32}[out_dtype],
+                    device=dev)
+    qta.taco_decompress(d, q, y, out_dtype)
+    ref = orc.decompress(ORC_SCH[scheme], B, c, s, z, st, batch, rows, cols, ORC_DT[out_dtype])
+    torch.cuda.synchronize()
+    assert_same("decompress", y, ref)
+    if out_dtype == qta.FP32:
+        assert_close_f32("decompress fp32", y, ref)
+
+
+def _oracle_shards(scheme, B, n, rows, cols, rng, dtype=qta.BF16):
+    shards, dev_shards = [], []
+    for r in range(n):
+        xt = to_dtype_cpu(random_values(rng, (rows, cols), "mixed", scale=1.0 + r), dtype)
+        c, s, z, st = oracle_compress(scheme, B, xt, dtype, 1, rows, cols)
+        shards.append((c, s, z, st))
+    return shards
+
+
+def _to_dev(scheme, B, rows, cols, shards, dev):
+    d = qta.desc(scheme, B, rows, cols)
+    out = []
+    for c, s, z, st in shards:
+        out.append(qta.QTensor(d, torch.from_numpy(c.view(np.uint8).copy()).to(dev),
+                               torch.from_numpy(s.view(np.uint8).copy()).to(dev),
+                               None if z is None else torch.from_numpy(z.view(np.uint8).copy()).to(dev),
+                               None if st is None else torch.from_numpy(st.copy()).to(dev)))
+    return d, out
+
+
+@pytest.mark.parametrize("scheme,B", [(qta.TACO_FP8, 64), (qta.TACO_FP8, 128), (qta.TACO_FP8, 256),
+                                      (qta.INT8_SYM_B64, 64), (qta.INT4_ASYM_G128, 128),
+                                      (qta.INT8_ASYM_G128, 128)])
+@pytest.mark.parametrize("n", [1, 2, 3, 8, 16])
+def test_reduce(dev, scheme, B, n):
+    rows, cols = 96, 1024
+    rng = np.random.default_rng(hash((scheme, B, n)) % 2 ** 32)
+    shards = _oracle_shards(scheme, B, n, rows, cols, rng)
+    d, ds = _to_dev(scheme, B, rows, cols, shards, dev)
+    for rb, re_ in ((0, rows), (7, 61), (95, 96)):
+        out = torch.full((re_ - rb, cols), float("nan"), dtype=torch.float32, device=dev)
+        qta.qar_reduce(d, ds, rb, re_, out)
+        ref = orc.reduce(ORC_SCH[scheme], B, shards, rows, cols, rb, re_)
+        torch.cuda.synchronize()
+        assert_same(f"reduce rows {rb}:{re_}", out, ref)
+        assert_close_f32("reduce", out, ref)
+
+
+def test_reduce_many_tiles(dev):
+    # enough output segments that every warp of the persistent grid loops over
+    # several tiles and its (tile, rank) stage ring wraps many times
+    scheme, B, n, rows, cols = qta.TACO_FP8, 128, 8, 2048, 4096
+    rng = np.random.default_rng(11)
+    shards = _oracle_shards(scheme, B, n, rows, cols, rng)
+    d, ds = _to_dev(scheme, B, rows, cols, shards, dev)
+    out = torch.empty((rows, cols), dtype=torch.float32, device=dev)
+    qta.qar_reduce(d, ds, 0, rows, out)
+    ref = orc.reduce(orc.TACO_FP8, B, shards, rows, cols)
+    torch.cuda.synchronize()
+    assert_same("reduce many tiles", out, ref)
+
+
+def test_taco_steps_with_drift(dev):
+    # successive steps with a per-step magnitude drift: step 0 CURRENT, later
+    # steps DELAYED with the scale left by taco_update_scale of the previous
+    # step, on both sides.
+    batch, rows, cols, B = 2, 64, 1024, 256
+    rng = np.random.default_rng(3)
+    base = random_values(rng, (batch, rows, cols), "normal", 1e-4)
+    d = qta.desc(qta.TACO_FP8, B, rows, cols, batch=batch)
+    q = qta.alloc_qtensor(d, dev)
+    st = np.zeros(2 * batch, dtype=np.float32)
+    for step in range(8):
+        f = float(np.exp(rng.uniform(np.log(0.25), np.log(4.0))))
+        xt = to_dtype_cpu((base * np.float32(f)).astype(np.float32), qta.BF16)
+        mode = qta.SCALE_CURRENT if step == 0 else qta.SCALE_DELAYED
+        qta.taco_compress(d, xt.to(dev), qta.BF16, q, mode)
+        c, s, _ = orc.compress(orc.TACO_FP8, B, oracle_bits_in(xt), orc.BF16, batch, rows, cols, st,
+                               orc.CURRENT if step == 0 else orc.DELAYED)
+        torch.cuda.synchronize()
+        assert_same(f"step {step} codes", q.codes, c)
+        assert_same(f"step {step} scales", q.scales, s)
+        assert_same(f"step {step} state", q.state, st)
+        qta.taco_update_scale(q.state, batch)
+        orc.taco_update_scale(st)
+        torch.cuda.synchronize()
+        assert_same(f"step {step} updated state", q.state, st)
+
+
+def test_requant_full_chain(dev):
+    # compress -> reduce -> requant -> decompress for each workload's scheme
+    # pair, at a reduced size, bit-exact at every stage
+    cases = [(qta.TACO_FP8, 128, qta.TACO_FP8, 128, qta.BF16, 4),
+             (qta.INT8_SYM_B64, 64, qta.INT8_SYM_B64, 64, qta.BF16, 8),
+             (qta.INT4_ASYM_G128, 128, qta.INT8_ASYM_G128, 128, qta.FP16, 8)]
+    for sch, B, gsch, gB, dtype, N in cases:
+        R, C = 128, 1024
+        rng = np.random.default_rng(sch)
+        xt = to_dtype_cpu(random_values(rng, (N, R, C), "t"), dtype)
+        d, q = gpu_compress(sch, B, xt, dtype, N, R, C, dev=dev)
+        ref = oracle_compress(sch, B, xt, dtype, N, R, C)
+        d1 = qta.desc(sch, B, R, C)
+        ssum = torch.empty((R, C), dtype=torch.float32, device=dev)
+        qta.qar_reduce(d1, [q.shard(r) for r in range(N)], 0, R, ssum)
+        E = R * C
+        nb = E // B
+        cb = E // 2 if sch == qta.INT4_ASYM_G128 else E
+        shards = [(ref[0][r * cb:(r + 1) * cb], ref[1][r * nb:(r + 1) * nb],
+                   None if ref[2] is None else ref[2][r * nb:(r + 1) * nb],
+                   None if ref[3] is None else ref[3][2 * r:2 * r + 2]) for r in range(N)]
+        osum = orc.reduce(ORC_SCH[sch], B, shards, R, C)
+        dg = qta.desc(gsch, gB, R // N, C, batch=N)
+        g = qta.alloc_qtensor(dg, dev)
+        qta.qar_requant(dg, ssum, g, qta.SCALE_CURRENT)
+        gref = oracle_compress(gsch, gB, torch.from_numpy(osum.reshape(R, C)), qta.FP32, N, R // N, C)
+        y = torch.empty((R, C), dtype=torch.bfloat16 if dtype == qta.BF16 else torch.float16, device=dev)
+        qta.taco_decompress(dg, g, y, dtype)
+        yref = orc.decompress(ORC_SCH[gsch], gB, *gref, N, R // N, C, ORC_DT[dtype])
+        torch.cuda.synchronize()
+        compare_qtensor("stage-1", q, ref)
+        assert_same("sum", ssum, osum)
+        compare_qtensor("requant", g, gref)
+        assert_same("output", y, yref)
+
+
+def test_error_status_leaves_outputs_untouched(dev):
+    d = qta.desc(qta.TACO_FP8, 128, 4, 256)
+    q = qta.alloc_qtensor(d, dev)
+    q.codes.fill_(0xA5)
+    x = torch.randn(4 * 256 + 8, dtype=torch.bfloat16, device=dev)
+    with pytest.raises(qta.QtaError) as e:
+        qta.taco_compress(d, x.data_ptr() + 2, qta.BF16, q)      # misaligned input
+    assert e.value.status == qta.QTA_ERR_ALIGNMENT
+    with pytest.raises(qta.QtaError) as e:
+        qta.qar_reduce(d, [q.shard(0)] * 17, 0, 4, torch.empty(4, 256, device=dev))
+    assert e.value.status == qta.QTA_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert (q.codes == 0xA5).all()
+    assert qta.qta_device_error() == 0
+
+
+def test_copy_kernel(dev):
+    n = (1 << 24) + 48
+    src = torch.randint(0, 255, (n,), dtype=torch.uint8, device=dev)
+    dst = torch.zeros_like(src)
+    qta.qta_copy(src, dst, n)
+    torch.cuda.synchronize()
+    assert torch.equal(src, dst)
