@@ -85,7 +85,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.STDOUT)
         except Exception:
             self.proc = None
 
@@ -100,19 +100,33 @@ class ClockSampler:
         self.f.close()
         rows = []
         with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
+            raw = f.read()
+        for line in raw.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
         os.unlink(self.path)
         if not rows:
-            return None
+            return {"error": "no nvidia-smi samples", "gpu": str(self.idx), "output": raw[:200]}
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]})
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
                 "reasons": reasons, "samples": len(rows)}
+
+
+def _smi_gpu_id(torch, local: int) -> str:
+    """The identifier nvidia-smi needs for the device this process uses."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        tok = vis.split(",")[local].strip()
+        if tok:
+            return tok
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        return str(local)
 
 
 def _cpu_oracle_path(w: workloads.Workload, rows: int, seed: int = 0):
@@ -263,13 +277,29 @@ def run_qta(args, w):
     torch.cuda.synchronize()
     assert qta.qta_device_error() == 0
 
+    # calibrate a load window of about 0.6 s on each side of the timed region,
+    # so that nvidia-smi samples the clocks under the same continuous load
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(3):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    pad = max(1, int(600.0 / max(a.elapsed_time(b) / 3, 1e-3)))
+
     # ---- timed region: inputs resident in HBM
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
-    clocks = ClockSampler(torch.cuda.current_device())
+    clocks = ClockSampler(_smi_gpu_id(torch, local))
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
+    time.sleep(0.3)
+    for _ in range(pad):
+        step()
+    if ws > 1:
+        torch.cuda.synchronize()
+        torch.distributed.barrier()
     launches[0] = 0
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
@@ -277,11 +307,15 @@ def run_qta(args, w):
     for i in range(args.steps):
         step(ev=evs[i])
     t_end.record(stream)
+    n_launch = launches[0]
+    for _ in range(pad):
+        step()
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    n_launch = launches[0]
+    if clk is not None:
+        clk["window"] = f"sampled every 100 ms over {2 * pad + args.steps} back-to-back steps around and including the timed ones"
     total_ms = t_start.elapsed_time(t_end)
     per = {k: [] for k in ("K1", "U1", "K2", "K3", "U2", "K4")}
     for e in evs:
@@ -351,7 +385,7 @@ def run_qta(args, w):
 
     cpu = None
     if not args.no_cpu_baseline and ws == 1:
-        rows = args.cpu_rows
+        rows = args.cpu_rows or w.rows
         dt_s, nbytes, threads = _cpu_oracle_path(w, rows, seed=args.seed)
         cpu = {"value": nbytes / dt_s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"{rows} of {w.rows} rows of each of the {w.ranks} ranks "
@@ -384,7 +418,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="gpt_tp", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="qta", choices=["qta", "reference"])
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--cpu-rows", type=int, default=4096)
+    ap.add_argument("--cpu-rows", type=int, default=0, help="oracle row sample per rank (0: all rows)")
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
