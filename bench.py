@@ -79,6 +79,8 @@ class ClockSampler:
         self.path = None
 
     def start(self):
+        if self.idx is None:
+            return
         try:
             fd, self.path = tempfile.mkstemp(prefix="qta_clocks_", suffix=".csv")
             os.close(fd)
@@ -285,16 +287,17 @@ def run_qta(args, w):
         step()
     b.record(stream)
     torch.cuda.synchronize()
-    pad = max(1, int(600.0 / max(a.elapsed_time(b) / 3, 1e-3)))
+    pad = 0 if args.no_clocks else max(1, int(600.0 / max(a.elapsed_time(b) / 3, 1e-3)))
 
     # ---- timed region: inputs resident in HBM
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
-    clocks = ClockSampler(_smi_gpu_id(torch, local))
+    clocks = ClockSampler(None if args.no_clocks else _smi_gpu_id(torch, local))
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    time.sleep(0.3)
+    if not args.no_clocks:
+        time.sleep(0.3)
     for _ in range(pad):
         step()
     if ws > 1:
@@ -422,6 +425,7 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true", help="skip the nvidia-smi clock window (profiling runs)")
     args = ap.parse_args(argv)
     w = workloads.WORKLOADS[args.workload]
     if args.impl == "reference":
