@@ -270,9 +270,11 @@ static void asym_compress_tensor(const void* x, int dtype, int64_t off, int64_t 
             mn = fminf(mn, v);
             mx = fmaxf(mx, v);
         }
-        float sf = (mx - mn) / Q;
+        /* "+ 0.0f" stores a zero scale / zero-point as +0, so that which of
+         * -0 and +0 a min / max picks (an order detail) cannot show. */
+        float sf = (mx - mn) / Q + 0.0f;
         if (sf > 65504.0f) sf = 65504.0f;
-        float zc = mn;
+        float zc = mn + 0.0f;
         if (zc > 65504.0f) zc = 65504.0f;
         if (zc < -65504.0f) zc = -65504.0f;
         uint16_t s16 = orc_f32_to_f16(sf), z16 = orc_f32_to_f16(zc);
