@@ -242,6 +242,7 @@ static void int8sym_compress_tensor(const void* x, int dtype, int64_t off, int64
         for (int i = 0; i < 64; ++i) a = fmaxf(a, fabsf(load_elem(x, dtype, off + b * 64 + i)));
         float s = a / 127.0f;
         float inv = (a > 0.0f) ? 127.0f / a : 0.0f;
+        if (inv > FLT_MAX) inv = 0.0f; /* a < 127/FLT_MAX: the block is stored as zeros */
         for (int i = 0; i < 64; ++i) {
             float q = rintf(load_elem(x, dtype, off + b * 64 + i) * inv);
             if (q > 127.0f) q = 127.0f;
