@@ -49,7 +49,9 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         return LIB
     nvcc = _nvcc()
     os.makedirs(OUT_DIR, exist_ok=True)
-    common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
+    # --fmad=false: no multiply-add contraction anywhere; the kernels spell out
+    # every fused multiply-add they want, so the rounding is the written one.
+    common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "--fmad=false", "-Xcompiler", "-fPIC", "-I", INCLUDE,
                      "--expt-relaxed-constexpr", "-Xcompiler", "-Wall"]
     if ptxas_info:
         common += ["-Xptxas", "-v"]

@@ -164,10 +164,73 @@ __device__ __forceinline__ void sts128(uint8_t* base, uint32_t off, uint4 v)
     *reinterpret_cast<uint4*>(base + off) = v;
 }
 
+// ---------------------------------------------------------------- packed FP32
+// Values travel as pairs of binary32 in one 64-bit register: pair j of a
+// segment holds elements (2j, 2j+1).  add/sub/mul/fma .f32x2 round each lane
+// to nearest-even exactly like the scalar instructions, at one instruction
+// per pair.
+using u64 = unsigned long long;
+
+__device__ __forceinline__ u64 pk2(float lo, float hi)
+{
+    u64 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ float2 up2(u64 v)
+{
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+
+__device__ __forceinline__ u64 add2(u64 a, u64 b)
+{
+    u64 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ u64 sub2(u64 a, u64 b)
+{
+    u64 d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ u64 mul2(u64 a, u64 b)
+{
+    u64 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c)
+{
+    u64 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ float max3f(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ float min3f(float a, float b, float c)
+{
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // ---------------------------------------------------------------- formats
 // FP8 E4M3 pair encode, round-to-nearest-even with saturation to +-448
 // (cvt .satfinite); lo goes to the low byte.
-__device__ __forceinline__ uint32_t e4m3x2_encode(float lo, float hi)
+__device__ __forceinline__ uint16_t e4m3x2_encode(float lo, float hi)
 {
     uint16_t r;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
@@ -176,46 +239,114 @@ __device__ __forceinline__ uint32_t e4m3x2_encode(float lo, float hi)
 
 __device__ __forceinline__ uint32_t e4m3_encode(float v) { return e4m3x2_encode(v, 0.0f) & 0xffu; }
 
-// FP8 E4M3 pair decode (exact): the low byte gives .x.
-__device__ __forceinline__ float2 e4m3x2_decode(uint32_t two_codes)
+__device__ __forceinline__ uint32_t join16(uint16_t lo, uint16_t hi)
+{
+    uint32_t r;
+    asm("mov.b32 %0, {%1, %2};" : "=r"(r) : "h"(lo), "h"(hi));
+    return r;
+}
+
+// FP8 E4M3 pair decode (exact) to a float pair: the low byte gives .x.
+__device__ __forceinline__ u64 e4m3x2_decode(uint16_t two_codes)
 {
     uint32_t h2;
-    uint16_t in = static_cast<uint16_t>(two_codes);
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
-    __half2 h = *reinterpret_cast<__half2*>(&h2);
-    return __half22float2(h);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two_codes));
+    const float2 f = __half22float2(*reinterpret_cast<__half2*>(&h2));
+    return pk2(f.x, f.y);
 }
 
-__device__ __forceinline__ float e4m3_decode(uint32_t code) { return e4m3x2_decode(code & 0xffu).x; }
-
-__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-__device__ __forceinline__ float2 f16x2_to_f32(uint32_t w)
+__device__ __forceinline__ float e4m3_decode(uint32_t code)
 {
-    __half2 h = *reinterpret_cast<__half2*>(&w);
-    return __half22float2(h);
+    return up2(e4m3x2_decode(static_cast<uint16_t>(code & 0xffu))).x;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+__device__ __forceinline__ uint16_t lo16(uint32_t w) { return static_cast<uint16_t>(w & 0xffffu); }
+__device__ __forceinline__ uint16_t hi16(uint32_t w) { return static_cast<uint16_t>(w >> 16); }
+
+__device__ __forceinline__ u64 bf16x2_to_pair(uint32_t w) { return pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)); }
+
+__device__ __forceinline__ u64 f16x2_to_pair(uint32_t w)
 {
+    const float2 f = __half22float2(*reinterpret_cast<__half2*>(&w));
+    return pk2(f.x, f.y);
+}
+
+__device__ __forceinline__ uint32_t pair_to_bf16x2(u64 v)
+{
+    const float2 f = up2(v);
     uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(f.y), "f"(f.x));
     return r;
 }
 
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+__device__ __forceinline__ uint32_t pair_to_f16x2(u64 v)
 {
+    const float2 f = up2(v);
     uint32_t r;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(f.y), "f"(f.x));
     return r;
 }
 
-// Exact small-integer to float without the conversion pipe: the bits
-// 0x4B000000 | u are the float 2^23 + u for u < 2^23.
-__device__ __forceinline__ float u8_to_float(uint32_t u) { return __fsub_rn(__uint_as_float(0x4B000000u | u), 8388608.0f); }
-// Signed int8 held in the low byte of b (two's complement).
-__device__ __forceinline__ float s8_to_float(uint32_t b) { return __fsub_rn(__uint_as_float(0x4B000000u | ((b & 0xffu) ^ 0x80u)), 8388736.0f); }
+// Small integers to float without the conversion pipe: the bits
+// 0x4B000000 | u are the float 2^23 + u for u < 2^23.  Byte k of `w` (k = 0..3)
+// goes to the low byte via PRMT.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// Four unsigned bytes of w as two float pairs (exact): (b0, b1), (b2, b3).
+__device__ __forceinline__ void u8x4_to_pairs(uint32_t w, u64& p01, u64& p23)
+{
+    const uint32_t magic = 0x4B000000u;
+    const u64 off = pk2(8388608.0f, 8388608.0f);
+    // prmt selectors: byte 0..3 of w into the low byte, bytes 1..3 from magic (b = magic: bytes 4..7)
+    p01 = sub2(pk2(__uint_as_float(prmt(w, magic, 0x7650u)), __uint_as_float(prmt(w, magic, 0x7651u))), off);
+    p23 = sub2(pk2(__uint_as_float(prmt(w, magic, 0x7652u)), __uint_as_float(prmt(w, magic, 0x7653u))), off);
+}
+
+// Four signed (two's complement) bytes of w as two float pairs (exact).
+__device__ __forceinline__ void s8x4_to_pairs(uint32_t w, u64& p01, u64& p23)
+{
+    const u64 off = pk2(8388736.0f, 8388736.0f);  // 2^23 + 128
+    const uint32_t wb = w ^ 0x80808080u;           // b + 128 for each signed byte
+    const uint32_t magic = 0x4B000000u;
+    p01 = sub2(pk2(__uint_as_float(prmt(wb, magic, 0x7650u)), __uint_as_float(prmt(wb, magic, 0x7651u))), off);
+    p23 = sub2(pk2(__uint_as_float(prmt(wb, magic, 0x7652u)), __uint_as_float(prmt(wb, magic, 0x7653u))), off);
+}
+
+// Eight nibbles of w (element 2k low nibble of byte k, 2k+1 high nibble) as
+// four float pairs (exact).
+__device__ __forceinline__ void u4x8_to_pairs(uint32_t w, u64 (&p)[4])
+{
+    const uint32_t even = w & 0x0F0F0F0Fu;          // elements 0,2,4,6 in bytes 0..3
+    const uint32_t odd = (w >> 4) & 0x0F0F0F0Fu;    // elements 1,3,5,7
+    const uint32_t magic = 0x4B000000u;
+    const u64 off = pk2(8388608.0f, 8388608.0f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        p[k] = sub2(pk2(__uint_as_float(prmt(even, magic, 0x7650u + k)), __uint_as_float(prmt(odd, magic, 0x7650u + k))),
+                    off);
+}
+
+// Round-to-nearest-even to an integer through the FP32 adder: for |y| < 2^22
+// the bits of y + 1.5*2^23 are 0x4B400000 + rint(y); the low byte of those
+// bits is rint(y) mod 256.
+__device__ __forceinline__ u64 rint_bits2(u64 y)
+{
+    return add2(y, pk2(12582912.0f, 12582912.0f));
+}
+
+// Low bytes of four words into one word: (a, b, c, d) -> bytes [a b c d].
+__device__ __forceinline__ uint32_t bytes4(uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    return prmt(prmt(a, b, 0x7740u), prmt(c, d, 0x7740u), 0x5410u);
+}
+
+__device__ __forceinline__ uint32_t lo32(u64 v) { return static_cast<uint32_t>(v); }
+__device__ __forceinline__ uint32_t hi32(u64 v) { return static_cast<uint32_t>(v >> 32); }
 
 // Per-tensor scale rule: S = amax/448, or 1 when that is zero, non-finite or
 // below the smallest normal float.
@@ -227,35 +358,44 @@ __device__ __forceinline__ float scale_from_amax(float amax)
 }
 
 // ---------------------------------------------------------------- Hadamard
-// Butterfly stages with strides 1..32 inside one thread's 64 values, in
-// ascending order; each pair (j, j+h) -> (a+b, a-b) in binary32.
-__device__ __forceinline__ void fwht64_local(float (&v)[SEG])
+// Butterfly stages with strides 1, 2, 4, ..., 32 inside one lane's 64 values
+// (32 pairs), ascending; each (j, j+h) -> (a+b, a-b) in binary32.  Stride 1
+// pairs the two halves of a register pair (scalar); strides 2..32 pair whole
+// register pairs (packed).
+__device__ __forceinline__ void fwht64_local(u64 (&v)[32])
 {
 #pragma unroll
-    for (int h = 1; h < SEG; h <<= 1) {
+    for (int j = 0; j < 32; ++j) {
+        const float2 t = up2(v[j]);
+        v[j] = pk2(__fadd_rn(t.x, t.y), __fsub_rn(t.x, t.y));
+    }
 #pragma unroll
-        for (int i = 0; i < SEG; i += 2 * h) {
+    for (int hp = 1; hp < 32; hp <<= 1) {
 #pragma unroll
-            for (int j = i; j < i + h; ++j) {
-                const float a = v[j], b = v[j + h];
-                v[j] = __fadd_rn(a, b);
-                v[j + h] = __fsub_rn(a, b);
+        for (int i = 0; i < 32; i += 2 * hp) {
+#pragma unroll
+            for (int j = i; j < i + hp; ++j) {
+                const u64 a = v[j], b = v[j + hp];
+                v[j] = add2(a, b);
+                v[j + hp] = sub2(a, b);
             }
         }
     }
 }
 
 // Remaining stages (strides 64, 128) across the 2 or 4 lanes that hold one
-// block: the lower lane of a pair keeps a+b, the upper keeps a-b, where a is
-// the lower lane's value.
-__device__ __forceinline__ void fwht_cross(float (&v)[SEG], int lanes_per_block, int lane)
+// block.  With a = the lower lane's value and b = the upper lane's, the lower
+// lane keeps fma(a, +1, b) = a+b and the upper fma(b, -1, a) = a-b: one
+// rounding each, identical to the add / subtract.
+__device__ __forceinline__ void fwht_cross(u64 (&v)[32], int lanes_per_block, int lane)
 {
     for (int d = 1; d < lanes_per_block; d <<= 1) {
-        const bool upper = (lane & d) != 0;
+        const float sgn = (lane & d) ? -1.0f : 1.0f;
+        const u64 s2 = pk2(sgn, sgn);
 #pragma unroll
-        for (int i = 0; i < SEG; ++i) {
-            const float o = __shfl_xor_sync(0xffffffffu, v[i], d);
-            v[i] = upper ? __fsub_rn(o, v[i]) : __fadd_rn(v[i], o);
+        for (int j = 0; j < 32; ++j) {
+            const u64 o = __shfl_xor_sync(0xffffffffu, v[j], d);
+            v[j] = fma2(v[j], s2, o);
         }
     }
 }
@@ -269,6 +409,18 @@ __device__ __forceinline__ float group_max(float m, int lanes_per_block)
 __device__ __forceinline__ float group_min(float m, int lanes_per_block)
 {
     for (int d = 1; d < lanes_per_block; d <<= 1) m = fminf(m, __shfl_xor_sync(0xffffffffu, m, d));
+    return m;
+}
+
+// max |v| over the 64 values of a lane.
+__device__ __forceinline__ float absmax64(const u64 (&v)[32])
+{
+    float m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const float2 t = up2(v[j]);
+        m = max3f(m, fabsf(t.x), fabsf(t.y));
+    }
     return m;
 }
 

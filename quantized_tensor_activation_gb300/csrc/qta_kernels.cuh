@@ -119,9 +119,10 @@ __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw)
 }
 
 // ------------------------------------------------------------ segment I/O
-// Read this lane's 64-element input segment (row `lane` of a stage).
+// Read this lane's 64-element input segment (row `lane` of a stage) as 32
+// float pairs.
 template <int IN>
-__device__ __forceinline__ void load_segment(const uint8_t* st, int lane, float (&v)[SEG])
+__device__ __forceinline__ void load_segment(const uint8_t* st, int lane, u64 (&v)[32])
 {
     if constexpr (IN == IN_FP32) {
 #pragma unroll
@@ -129,56 +130,42 @@ __device__ __forceinline__ void load_segment(const uint8_t* st, int lane, float 
             const uint8_t* box = st + h * 4096;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                uint4 w = lds128(box, sw128(lane, c));
-                v[h * 32 + c * 4 + 0] = __uint_as_float(w.x);
-                v[h * 32 + c * 4 + 1] = __uint_as_float(w.y);
-                v[h * 32 + c * 4 + 2] = __uint_as_float(w.z);
-                v[h * 32 + c * 4 + 3] = __uint_as_float(w.w);
+                const uint4 w = lds128(box, sw128(lane, c));
+                v[h * 16 + c * 2 + 0] = pk2(__uint_as_float(w.x), __uint_as_float(w.y));
+                v[h * 16 + c * 2 + 1] = pk2(__uint_as_float(w.z), __uint_as_float(w.w));
             }
         }
     } else {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-            uint4 w = lds128(st, sw128(lane, c));
-            uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            const uint4 w = lds128(st, sw128(lane, c));
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                if constexpr (IN == IN_BF16) {
-                    v[c * 8 + 2 * k] = bf16lo(ws[k]);
-                    v[c * 8 + 2 * k + 1] = bf16hi(ws[k]);
-                } else {
-                    float2 f = f16x2_to_f32(ws[k]);
-                    v[c * 8 + 2 * k] = f.x;
-                    v[c * 8 + 2 * k + 1] = f.y;
-                }
-            }
+            for (int k = 0; k < 4; ++k)
+                v[c * 4 + k] = (IN == IN_BF16) ? bf16x2_to_pair(ws[k]) : f16x2_to_pair(ws[k]);
         }
     }
 }
 
 // Write this lane's 64-element output row into a staging buffer.
 template <int OUT>
-__device__ __forceinline__ void store_segment(uint8_t* ob, int lane, const float (&v)[SEG])
+__device__ __forceinline__ void store_segment(uint8_t* ob, int lane, const u64 (&v)[32])
 {
     if constexpr (OUT == IN_FP32) {
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                const int e = h * 32 + c * 4;
-                sts128(ob + h * 4096, sw128(lane, c),
-                       make_uint4(__float_as_uint(v[e]), __float_as_uint(v[e + 1]),
-                                  __float_as_uint(v[e + 2]), __float_as_uint(v[e + 3])));
+                const u64 a = v[h * 16 + c * 2], b = v[h * 16 + c * 2 + 1];
+                sts128(ob + h * 4096, sw128(lane, c), make_uint4(lo32(a), hi32(a), lo32(b), hi32(b)));
             }
     } else {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
             uint32_t w[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float lo = v[c * 8 + 2 * k], hi = v[c * 8 + 2 * k + 1];
-                w[k] = (OUT == IN_BF16) ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
-            }
+            for (int k = 0; k < 4; ++k)
+                w[k] = (OUT == IN_BF16) ? pair_to_bf16x2(v[c * 4 + k]) : pair_to_f16x2(v[c * 4 + k]);
             sts128(ob, sw128(lane, c), make_uint4(w[0], w[1], w[2], w[3]));
         }
     }
@@ -189,7 +176,7 @@ __device__ __forceinline__ void load_codes8(const uint8_t* st, int lane, uint32_
 {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        uint4 w = lds128(st, sw64(lane, c));
+        const uint4 w = lds128(st, sw64(lane, c));
         q[c * 4 + 0] = w.x;
         q[c * 4 + 1] = w.y;
         q[c * 4 + 2] = w.z;
@@ -202,11 +189,54 @@ __device__ __forceinline__ void load_codes4(const uint8_t* st, int lane, uint32_
 {
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-        uint4 w = lds128(st, sw32(lane, c));
+        const uint4 w = lds128(st, sw32(lane, c));
         q[c * 4 + 0] = w.x;
         q[c * 4 + 1] = w.y;
         q[c * 4 + 2] = w.z;
         q[c * 4 + 3] = w.w;
+    }
+}
+
+// Dequantized FP32 pairs of one segment's codes (before any transform):
+// TACO  E4M3(q) * s          (s = S * r_b)
+// INT8  q * s
+// ASYM  fmaf(q, s, z)
+template <int SCH>
+__device__ __forceinline__ void dequant_segment(const uint8_t* st, int lane, float s, float z, u64 (&v)[32])
+{
+    const u64 s2 = pk2(s, s);
+    if constexpr (SCH == S_ASYM4) {
+        uint32_t q[8];
+        load_codes4(st, lane, q);
+        const u64 z2 = pk2(z, z);
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            u64 p[4];
+            u4x8_to_pairs(q[w], p);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) v[w * 4 + k] = fma2(p[k], s2, z2);
+        }
+    } else {
+        uint32_t q[16];
+        load_codes8(st, lane, q);
+#pragma unroll
+        for (int w = 0; w < 16; ++w) {
+            if constexpr (SCH == S_TACO) {
+                v[2 * w] = mul2(e4m3x2_decode(lo16(q[w])), s2);
+                v[2 * w + 1] = mul2(e4m3x2_decode(hi16(q[w])), s2);
+            } else if constexpr (SCH == S_INT8SYM) {
+                u64 a, b;
+                s8x4_to_pairs(q[w], a, b);
+                v[2 * w] = mul2(a, s2);
+                v[2 * w + 1] = mul2(b, s2);
+            } else {
+                u64 a, b;
+                u8x4_to_pairs(q[w], a, b);
+                const u64 z2 = pk2(z, z);
+                v[2 * w] = fma2(a, s2, z2);
+                v[2 * w + 1] = fma2(b, s2, z2);
+            }
+        }
     }
 }
 
@@ -251,6 +281,19 @@ struct AmaxTracker {
     }
 };
 
+// Drain path after a timed-out wait: let every load this warp issued land
+// before the CTA may exit (each wait is bounded as well).
+__device__ __forceinline__ void drain_ring(uint64_t* bars, int stages, int stage, uint32_t phase, unsigned int* err)
+{
+    for (int i = 0; i < stages; ++i) {
+        mbar_wait(&bars[stage], phase, err);
+        if (++stage == stages) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+}
+
 // ------------------------------------------------------------ compress
 // taco_compress / qar_requant / CURRENT-mode amax pre-pass (AMAX_ONLY).
 template <int IN, int SCH, bool AMAX_ONLY>
@@ -270,16 +313,13 @@ compress_kernel(const __grid_constant__ CompressParams p)
     if (lane == 0) {
         for (int s = 0; s < C::STAGES; ++s) mbar_init(&bars[s], 1);
         fence_barrier_init();
-    }
-    __syncwarp();
-    // prologue: fill the ring
-    if (lane == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             const int wt = first + s * W;
             if (wt >= p.n_warp_tiles) break;
             issue_in16or32<IN>(&p.in_map, wb + s * C::IN_BYTES, wt * 32, &bars[s]);
         }
     }
+    __syncwarp();
 
     AmaxTracker amax;
     int cached_tensor = -1;
@@ -296,17 +336,14 @@ compress_kernel(const __grid_constant__ CompressParams p)
             aborted = true;
             break;
         }
-        float v[SEG];
+        u64 v[32];
         load_segment<IN>(wb + stage * C::IN_BYTES, lane, v);
         __syncwarp();
-        // refill this stage with the tile STAGES ahead
-        {
+        {   // refill this stage with the tile STAGES ahead
             const int nwt = wt + C::STAGES * W;
-            if (nwt < p.n_warp_tiles) {
-                if (lane == 0) {
-                    fence_proxy_async_smem();
-                    issue_in16or32<IN>(&p.in_map, wb + stage * C::IN_BYTES, nwt * 32, &bars[stage]);
-                }
+            if (nwt < p.n_warp_tiles && lane == 0) {
+                fence_proxy_async_smem();
+                issue_in16or32<IN>(&p.in_map, wb + stage * C::IN_BYTES, nwt * 32, &bars[stage]);
             }
         }
         if (++stage == C::STAGES) {
@@ -317,9 +354,8 @@ compress_kernel(const __grid_constant__ CompressParams p)
         const int g = wt * 32 + lane;     // global segment of this lane
         const bool valid = g < p.M;
 
-        uint32_t out_words[16];
+        uint32_t ow[16];                  // output code words of this lane
         if constexpr (SCH == S_TACO) {
-            // per-tensor state of this warp tile
             const int g_last = min(wt * 32 + 31, p.M - 1);
             const int t_first = (int)fdiv((uint32_t)(wt * 32), p.seg_per_tensor);
             const int t_last = (int)fdiv((uint32_t)g_last, p.seg_per_tensor);
@@ -327,9 +363,7 @@ compress_kernel(const __grid_constant__ CompressParams p)
             const int tens = uniform ? t_first : (int)fdiv((uint32_t)min(g, p.M - 1), p.seg_per_tensor);
             fwht64_local(v);
             fwht_cross(v, L, lane);
-            float a = 0.0f;
-#pragma unroll
-            for (int i = 0; i < SEG; ++i) a = fmaxf(a, fabsf(v[i]));
+            const float a = absmax64(v);
             if (uniform) {
                 if (tens != amax.tensor) {
                     amax.flush(p.state, lane);
@@ -352,73 +386,67 @@ compress_kernel(const __grid_constant__ CompressParams p)
                 if (r == 0u && ab > 0.0f) r = 1u;
                 const float sb = __fmul_rn(S, e4m3_decode(r));
                 const float inv = (sb > 0.0f) ? __frcp_rn(sb) : 0.0f;
+                const u64 inv2 = pk2(inv, inv);
 #pragma unroll
                 for (int w = 0; w < 16; ++w) {
-                    const uint32_t lo = e4m3x2_encode(__fmul_rn(v[4 * w], inv), __fmul_rn(v[4 * w + 1], inv));
-                    const uint32_t hi = e4m3x2_encode(__fmul_rn(v[4 * w + 2], inv), __fmul_rn(v[4 * w + 3], inv));
-                    out_words[w] = lo | (hi << 16);
+                    const float2 q0 = up2(mul2(v[2 * w], inv2));
+                    const float2 q1 = up2(mul2(v[2 * w + 1], inv2));
+                    ow[w] = join16(e4m3x2_encode(q0.x, q0.y), e4m3x2_encode(q1.x, q1.y));
                 }
                 if (valid && (lane & (L - 1)) == 0)
                     static_cast<uint8_t*>(p.scales)[g >> p.lanes_log2] = static_cast<uint8_t>(r);
             }
         } else if constexpr (SCH == S_INT8SYM) {
-            float a = 0.0f;
-#pragma unroll
-            for (int i = 0; i < SEG; ++i) a = fmaxf(a, fabsf(v[i]));
+            const float a = absmax64(v);
             const float s = __fdiv_rn(a, 127.0f);
-            const float inv = (a > 0.0f) ? __fdiv_rn(127.0f, a) : 0.0f;
+            float inv = (a > 0.0f) ? __fdiv_rn(127.0f, a) : 0.0f;
+            if (inv > 3.40282347e+38f) inv = 0.0f;   // absmax below 127/FLT_MAX: zero codes
+            const u64 inv2 = pk2(inv, inv);
+            // |x * inv| <= 127.00002 < 127.5 here, so no clamp is needed
 #pragma unroll
             for (int w = 0; w < 16; ++w) {
-                uint32_t word = 0;
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    int q = __float2int_rn(__fmul_rn(v[4 * w + b], inv));
-                    q = max(-127, min(127, q));
-                    word |= (static_cast<uint32_t>(q) & 0xffu) << (8 * b);
-                }
-                out_words[w] = word;
+                const u64 r0 = rint_bits2(mul2(v[2 * w], inv2));
+                const u64 r1 = rint_bits2(mul2(v[2 * w + 1], inv2));
+                ow[w] = bytes4(lo32(r0), hi32(r0), lo32(r1), hi32(r1));
             }
             if (valid) static_cast<float*>(p.scales)[g] = s;
         } else {
-            constexpr int Q = (SCH == S_ASYM4) ? 15 : 255;
-            float mn = v[0], mx = v[0];
+            constexpr float Q = (SCH == S_ASYM4) ? 15.0f : 255.0f;
+            float mn = up2(v[0]).x, mx = mn;
 #pragma unroll
-            for (int i = 1; i < SEG; ++i) {
-                mn = fminf(mn, v[i]);
-                mx = fmaxf(mx, v[i]);
+            for (int j = 0; j < 32; ++j) {
+                const float2 t = up2(v[j]);
+                mn = min3f(mn, t.x, t.y);
+                mx = max3f(mx, t.x, t.y);
             }
             mn = group_min(mn, 2);
             mx = group_max(mx, 2);
-            float sf = __fdiv_rn(__fsub_rn(mx, mn), (float)Q);
+            float sf = __fadd_rn(__fdiv_rn(__fsub_rn(mx, mn), Q), 0.0f);
             sf = fminf(sf, 65504.0f);
+            const float zc = fminf(fmaxf(__fadd_rn(mn, 0.0f), -65504.0f), 65504.0f);
             const __half s16 = __float2half_rn(sf);
-            const __half z16 = __float2half_rn(fminf(fmaxf(mn, -65504.0f), 65504.0f));
+            const __half z16 = __float2half_rn(zc);
             const float s = __half2float(s16), z = __half2float(z16);
             const float inv = (s > 0.0f) ? __frcp_rn(s) : 0.0f;
+            const u64 inv2 = pk2(inv, inv), z2 = pk2(z, z);
+            uint32_t rb[64];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float2 y = up2(mul2(sub2(v[j], z2), inv2));
+                const u64 r = rint_bits2(pk2(fminf(fmaxf(y.x, 0.0f), Q), fminf(fmaxf(y.y, 0.0f), Q)));
+                rb[2 * j] = lo32(r);
+                rb[2 * j + 1] = hi32(r);
+            }
             if constexpr (SCH == S_ASYM4) {
 #pragma unroll
                 for (int w = 0; w < 8; ++w) {
-                    uint32_t word = 0;
-#pragma unroll
-                    for (int b = 0; b < 8; ++b) {
-                        int q = __float2int_rn(__fmul_rn(__fsub_rn(v[8 * w + b], z), inv));
-                        q = max(0, min(Q, q));
-                        word |= static_cast<uint32_t>(q) << (4 * b);
-                    }
-                    out_words[w] = word;
+                    const uint32_t ev = bytes4(rb[8 * w + 0], rb[8 * w + 2], rb[8 * w + 4], rb[8 * w + 6]);
+                    const uint32_t od = bytes4(rb[8 * w + 1], rb[8 * w + 3], rb[8 * w + 5], rb[8 * w + 7]);
+                    ow[w] = ev | (od << 4);
                 }
             } else {
 #pragma unroll
-                for (int w = 0; w < 16; ++w) {
-                    uint32_t word = 0;
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        int q = __float2int_rn(__fmul_rn(__fsub_rn(v[4 * w + b], z), inv));
-                        q = max(0, min(Q, q));
-                        word |= static_cast<uint32_t>(q) << (8 * b);
-                    }
-                    out_words[w] = word;
-                }
+                for (int w = 0; w < 16; ++w) ow[w] = bytes4(rb[4 * w], rb[4 * w + 1], rb[4 * w + 2], rb[4 * w + 3]);
             }
             if (valid && (lane & 1) == 0) {
                 static_cast<__half*>(p.scales)[g >> 1] = s16;
@@ -434,13 +462,11 @@ compress_kernel(const __grid_constant__ CompressParams p)
             if constexpr (SCH == S_ASYM4) {
 #pragma unroll
                 for (int c = 0; c < 2; ++c)
-                    sts128(ob, sw32(lane, c),
-                           make_uint4(out_words[4 * c], out_words[4 * c + 1], out_words[4 * c + 2], out_words[4 * c + 3]));
+                    sts128(ob, sw32(lane, c), make_uint4(ow[4 * c], ow[4 * c + 1], ow[4 * c + 2], ow[4 * c + 3]));
             } else {
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    sts128(ob, sw64(lane, c),
-                           make_uint4(out_words[4 * c], out_words[4 * c + 1], out_words[4 * c + 2], out_words[4 * c + 3]));
+                    sts128(ob, sw64(lane, c), make_uint4(ow[4 * c], ow[4 * c + 1], ow[4 * c + 2], ow[4 * c + 3]));
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -453,22 +479,47 @@ compress_kernel(const __grid_constant__ CompressParams p)
     if constexpr (SCH == S_TACO) amax.flush(p.state, lane);
     if (lane == 0) {
         bulk_wait_all();
-        if (aborted) {
-            // let every load this warp issued land before the CTA can exit
-            int s = stage;
-            uint32_t ph = phase;
-            for (int i = 0; i < C::STAGES; ++i) {
-                mbar_wait(&bars[s], ph, p.err);
-                if (++s == C::STAGES) {
-                    s = 0;
-                    ph ^= 1u;
-                }
-            }
-        }
+        if (aborted) drain_ring(bars, C::STAGES, stage, phase, p.err);
     }
 }
 
 // ------------------------------------------------------------ decompress
+// Metadata of one segment: the dequantization scale and zero-point.
+template <int SCH>
+struct SegMeta {
+    uint32_t raw = 0;   // TACO: scale byte; INT8: f32 bits; ASYM: s16 | z16 << 16
+    float S = 0.0f;     // TACO per-tensor scale
+
+    __device__ __forceinline__ void load(const void* scales, const void* zeros, const float* state, int g,
+                                         int lanes_log2, const FastDiv& spt)
+    {
+        if constexpr (SCH == S_TACO) {
+            raw = __ldg(static_cast<const uint8_t*>(scales) + (g >> lanes_log2));
+            S = __ldg(state + 2 * (int)fdiv((uint32_t)g, spt));
+        } else if constexpr (SCH == S_INT8SYM) {
+            raw = __float_as_uint(__ldg(static_cast<const float*>(scales) + g));
+        } else {
+            const uint32_t s = __ldg(static_cast<const unsigned short*>(scales) + (g >> 1));
+            const uint32_t z = __ldg(static_cast<const unsigned short*>(zeros) + (g >> 1));
+            raw = s | (z << 16);
+        }
+    }
+
+    __device__ __forceinline__ void decode(float& s, float& z) const
+    {
+        if constexpr (SCH == S_TACO) {
+            s = __fmul_rn(S, e4m3_decode(raw));
+            z = 0.0f;
+        } else if constexpr (SCH == S_INT8SYM) {
+            s = __uint_as_float(raw);
+            z = 0.0f;
+        } else {
+            s = __half2float(__ushort_as_half(static_cast<unsigned short>(raw & 0xffffu)));
+            z = __half2float(__ushort_as_half(static_cast<unsigned short>(raw >> 16)));
+        }
+    }
+};
+
 template <int SCH, int OUT>
 __global__ void __launch_bounds__(DecompressCfg<SCH, OUT>::WARPS * 32, 1)
 decompress_kernel(const __grid_constant__ DecompressParams p)
@@ -498,61 +549,27 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
     uint32_t phase = 0;
     int k = 0;
     bool aborted = false;
+    // metadata of the next warp tile is fetched one tile ahead
+    SegMeta<SCH> meta;
+    if (first < p.n_warp_tiles && first * 32 + lane < p.M)
+        meta.load(p.scales, p.zeros, p.state, first * 32 + lane, p.lanes_log2, p.seg_per_tensor);
     for (int wt = first; wt < p.n_warp_tiles; wt += W, ++k) {
-        const int g = wt * 32 + lane;
-        const bool valid = g < p.M;
-        // metadata of this lane's segment
-        float sb = 0.0f, z = 0.0f;
-        if (valid) {
-            if constexpr (SCH == S_TACO) {
-                const int tens = (int)fdiv((uint32_t)g, p.seg_per_tensor);
-                const uint32_t r = __ldg(static_cast<const uint8_t*>(p.scales) + (g >> p.lanes_log2));
-                sb = __fmul_rn(__ldg(p.state + 2 * tens), e4m3_decode(r));
-            } else if constexpr (SCH == S_INT8SYM) {
-                sb = __ldg(static_cast<const float*>(p.scales) + g);
-            } else {
-                sb = __half2float(__ldg(static_cast<const __half*>(p.scales) + (g >> 1)));
-                z = __half2float(__ldg(static_cast<const __half*>(p.zeros) + (g >> 1)));
-            }
+        SegMeta<SCH> cur = meta;
+        {
+            const int gn = (wt + W) * 32 + lane;
+            if (wt + W < p.n_warp_tiles && gn < p.M)
+                meta.load(p.scales, p.zeros, p.state, gn, p.lanes_log2, p.seg_per_tensor);
         }
         const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[stage], phase, p.err));
         if (!ok) {
             aborted = true;
             break;
         }
-        float v[SEG];
-        if constexpr (SCH == S_ASYM4) {
-            uint32_t q[8];
-            load_codes4(wb + stage * C::IN_BYTES, lane, q);
-            __syncwarp();
-#pragma unroll
-            for (int w = 0; w < 8; ++w)
-#pragma unroll
-                for (int b = 0; b < 8; ++b)
-                    v[8 * w + b] = __fmaf_rn(u8_to_float((q[w] >> (4 * b)) & 15u), sb, z);
-        } else {
-            uint32_t q[16];
-            load_codes8(wb + stage * C::IN_BYTES, lane, q);
-            __syncwarp();
-#pragma unroll
-            for (int w = 0; w < 16; ++w) {
-                if constexpr (SCH == S_TACO) {
-                    const float2 lo = e4m3x2_decode(q[w] & 0xffffu);
-                    const float2 hi = e4m3x2_decode(q[w] >> 16);
-                    v[4 * w + 0] = __fmul_rn(lo.x, sb);
-                    v[4 * w + 1] = __fmul_rn(lo.y, sb);
-                    v[4 * w + 2] = __fmul_rn(hi.x, sb);
-                    v[4 * w + 3] = __fmul_rn(hi.y, sb);
-                } else if constexpr (SCH == S_INT8SYM) {
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) v[4 * w + b] = __fmul_rn(s8_to_float(q[w] >> (8 * b)), sb);
-                } else {
-#pragma unroll
-                    for (int b = 0; b < 4; ++b)
-                        v[4 * w + b] = __fmaf_rn(u8_to_float((q[w] >> (8 * b)) & 0xffu), sb, z);
-                }
-            }
-        }
+        float s, z;
+        cur.decode(s, z);
+        u64 v[32];
+        dequant_segment<SCH>(wb + stage * C::IN_BYTES, lane, s, z, v);
+        __syncwarp();
         {
             const int nwt = wt + C::STAGES * W;
             if (nwt < p.n_warp_tiles && lane == 0) {
@@ -568,8 +585,9 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
         if constexpr (SCH == S_TACO) {
             fwht64_local(v);
             fwht_cross(v, L, lane);
+            const u64 ib = pk2(p.inv_block, p.inv_block);
 #pragma unroll
-            for (int i = 0; i < SEG; ++i) v[i] = __fmul_rn(v[i], p.inv_block);
+            for (int j = 0; j < 32; ++j) v[j] = mul2(v[j], ib);
         }
         uint8_t* ob = outb + (k & 1) * C::OUT_BYTES;
         if (lane == 0) bulk_wait_read<1>();
@@ -584,17 +602,7 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
     }
     if (lane == 0) {
         bulk_wait_all();
-        if (aborted) {
-            int s = stage;
-            uint32_t ph = phase;
-            for (int i = 0; i < C::STAGES; ++i) {
-                mbar_wait(&bars[s], ph, p.err);
-                if (++s == C::STAGES) {
-                    s = 0;
-                    ph ^= 1u;
-                }
-            }
-        }
+        if (aborted) drain_ring(bars, C::STAGES, stage, phase, p.err);
     }
 }
 
@@ -609,6 +617,38 @@ __device__ __forceinline__ void reduce_issue(const ReduceParams& p, uint8_t* wb,
     const int wt = first + t * W;
     mbar_arrive_expect_tx(&bars[stage], C::IN_BYTES);
     tma_load_2d(wb + stage * C::IN_BYTES, &p.in_map[r], 0, p.seg_begin + wt * 32, &bars[stage]);
+}
+
+// Ranks are processed in chunks of RANK_CHUNK; the scale metadata of the next
+// chunk is fetched while the current one is accumulated.
+constexpr int RANK_CHUNK = 4;
+
+template <int SCH>
+__device__ __forceinline__ void reduce_meta_load(const ReduceParams& p, int t, int c, int first, int W, int lane,
+                                                 SegMeta<SCH> (&m)[RANK_CHUNK])
+{
+    const int o = (first + t * W) * 32 + lane;
+    const int g = p.seg_begin + o;
+    const bool valid = o < p.M_out;
+#pragma unroll
+    for (int k = 0; k < RANK_CHUNK; ++k) {
+        const int r = c * RANK_CHUNK + k;
+        if (valid && r < p.n_ranks) {
+            if constexpr (SCH == S_TACO) {
+                m[k].raw = __ldg(static_cast<const uint8_t*>(p.scales[r]) + (g >> p.lanes_log2));
+                m[k].S = __ldg(p.state[r]);
+            } else if constexpr (SCH == S_INT8SYM) {
+                m[k].raw = __float_as_uint(__ldg(static_cast<const float*>(p.scales[r]) + g));
+            } else {
+                const uint32_t s = __ldg(static_cast<const unsigned short*>(p.scales[r]) + (g >> 1));
+                const uint32_t z = __ldg(static_cast<const unsigned short*>(p.zeros[r]) + (g >> 1));
+                m[k].raw = s | (z << 16);
+            }
+        } else {
+            m[k].raw = 0u;
+            m[k].S = 0.0f;
+        }
+    }
 }
 
 template <int SCH>
@@ -633,104 +673,64 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
         for (int u = 0; u < C::STAGES && u < total_units; ++u) reduce_issue<SCH>(p, wb, bars, u, u, first, W);
     }
     __syncwarp();
-    float Sr[MAX_RANKS];
-    if constexpr (SCH == S_TACO) {
-#pragma unroll
-        for (int r = 0; r < MAX_RANKS; ++r) Sr[r] = (r < n) ? __ldg(p.state[r]) : 0.0f;
-    }
     const int L = p.lanes_per_block;
+    const int n_chunks = (n + RANK_CHUNK - 1) / RANK_CHUNK;
     int stage = 0;
     uint32_t phase = 0;
     int unit = 0;
     bool aborted = false;
+    SegMeta<SCH> nxt[RANK_CHUNK];
+    if (my_tiles > 0) reduce_meta_load<SCH>(p, 0, 0, first, W, lane, nxt);
     for (int t = 0; t < my_tiles && !aborted; ++t) {
         const int wt = first + t * W;
-        const int o = wt * 32 + lane;          // output segment
-        const bool valid = o < p.M_out;
-        const int g = p.seg_begin + o;         // input segment
-        float sc[MAX_RANKS], zz[MAX_RANKS];
+        u64 acc[32];
+        for (int c = 0; c < n_chunks && !aborted; ++c) {
+            SegMeta<SCH> cur[RANK_CHUNK];
 #pragma unroll
-        for (int r = 0; r < MAX_RANKS; ++r) {
-            sc[r] = 0.0f;
-            zz[r] = 0.0f;
-            if (r < n && valid) {
-                if constexpr (SCH == S_TACO) {
-                    const uint32_t b = __ldg(static_cast<const uint8_t*>(p.scales[r]) + (g >> p.lanes_log2));
-                    sc[r] = __fmul_rn(Sr[r], e4m3_decode(b));
-                } else if constexpr (SCH == S_INT8SYM) {
-                    sc[r] = __ldg(static_cast<const float*>(p.scales[r]) + g);
+            for (int kk = 0; kk < RANK_CHUNK; ++kk) cur[kk] = nxt[kk];
+            if (c + 1 < n_chunks)
+                reduce_meta_load<SCH>(p, t, c + 1, first, W, lane, nxt);
+            else if (t + 1 < my_tiles)
+                reduce_meta_load<SCH>(p, t + 1, 0, first, W, lane, nxt);
+#pragma unroll
+            for (int kk = 0; kk < RANK_CHUNK; ++kk) {
+                const int r = c * RANK_CHUNK + kk;
+                if (r >= n) break;
+                const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[stage], phase, p.err));
+                if (!ok) {
+                    aborted = true;
+                    break;
+                }
+                float s, z;
+                cur[kk].decode(s, z);
+                u64 v[32];
+                dequant_segment<SCH>(wb + stage * C::IN_BYTES, lane, s, z, v);
+                __syncwarp();
+                if (lane == 0 && unit + C::STAGES < total_units) {
+                    fence_proxy_async_smem();
+                    reduce_issue<SCH>(p, wb, bars, stage, unit + C::STAGES, first, W);
+                }
+                ++unit;
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                if (r == 0) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) acc[j] = v[j];
                 } else {
-                    sc[r] = __half2float(__ldg(static_cast<const __half*>(p.scales[r]) + (g >> 1)));
-                    zz[r] = __half2float(__ldg(static_cast<const __half*>(p.zeros[r]) + (g >> 1)));
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) acc[j] = add2(acc[j], v[j]);
                 }
-            }
-        }
-        float acc[SEG];
-#pragma unroll
-        for (int r = 0; r < MAX_RANKS; ++r) {
-            if (r >= n) break;
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[stage], phase, p.err));
-            if (!ok) {
-                aborted = true;
-                break;
-            }
-            float v[SEG];
-            if constexpr (SCH == S_ASYM4) {
-                uint32_t q[8];
-                load_codes4(wb + stage * C::IN_BYTES, lane, q);
-                __syncwarp();
-#pragma unroll
-                for (int w = 0; w < 8; ++w)
-#pragma unroll
-                    for (int b = 0; b < 8; ++b)
-                        v[8 * w + b] = __fmaf_rn(u8_to_float((q[w] >> (4 * b)) & 15u), sc[r], zz[r]);
-            } else {
-                uint32_t q[16];
-                load_codes8(wb + stage * C::IN_BYTES, lane, q);
-                __syncwarp();
-#pragma unroll
-                for (int w = 0; w < 16; ++w) {
-                    if constexpr (SCH == S_TACO) {
-                        const float2 lo = e4m3x2_decode(q[w] & 0xffffu);
-                        const float2 hi = e4m3x2_decode(q[w] >> 16);
-                        v[4 * w + 0] = __fmul_rn(lo.x, sc[r]);
-                        v[4 * w + 1] = __fmul_rn(lo.y, sc[r]);
-                        v[4 * w + 2] = __fmul_rn(hi.x, sc[r]);
-                        v[4 * w + 3] = __fmul_rn(hi.y, sc[r]);
-                    } else if constexpr (SCH == S_INT8SYM) {
-#pragma unroll
-                        for (int b = 0; b < 4; ++b) v[4 * w + b] = __fmul_rn(s8_to_float(q[w] >> (8 * b)), sc[r]);
-                    } else {
-#pragma unroll
-                        for (int b = 0; b < 4; ++b)
-                            v[4 * w + b] = __fmaf_rn(u8_to_float((q[w] >> (8 * b)) & 0xffu), sc[r], zz[r]);
-                    }
-                }
-            }
-            // refill this stage
-            if (lane == 0 && unit + C::STAGES < total_units) {
-                fence_proxy_async_smem();
-                reduce_issue<SCH>(p, wb, bars, stage, unit + C::STAGES, first, W);
-            }
-            ++unit;
-            if (++stage == C::STAGES) {
-                stage = 0;
-                phase ^= 1u;
-            }
-            if (r == 0) {
-#pragma unroll
-                for (int i = 0; i < SEG; ++i) acc[i] = v[i];
-            } else {
-#pragma unroll
-                for (int i = 0; i < SEG; ++i) acc[i] = __fadd_rn(acc[i], v[i]);
             }
         }
         if (aborted) break;
         if constexpr (SCH == S_TACO) {
             fwht64_local(acc);
             fwht_cross(acc, L, lane);
+            const u64 ib = pk2(p.inv_block, p.inv_block);
 #pragma unroll
-            for (int i = 0; i < SEG; ++i) acc[i] = __fmul_rn(acc[i], p.inv_block);
+            for (int j = 0; j < 32; ++j) acc[j] = mul2(acc[j], ib);
         }
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
@@ -744,17 +744,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
     }
     if (lane == 0) {
         bulk_wait_all();
-        if (aborted) {
-            int s = stage;
-            uint32_t ph = phase;
-            for (int i = 0; i < C::STAGES; ++i) {
-                mbar_wait(&bars[s], ph, p.err);
-                if (++s == C::STAGES) {
-                    s = 0;
-                    ph ^= 1u;
-                }
-            }
-        }
+        if (aborted) drain_ring(bars, C::STAGES, stage, phase, p.err);
     }
 }
 
