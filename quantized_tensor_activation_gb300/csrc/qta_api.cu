@@ -317,7 +317,7 @@ static qta_status compress_impl(const qta_desc* d, const void* x, int32_t x_dtyp
     p.lanes_log2 = log2i(p.lanes_per_block);
     p.seg_per_tensor = make_fastdiv(static_cast<uint32_t>(d->rows * d->cols / 64));
     const int sch = d->scheme;  // qta_scheme values equal the kernel scheme kinds
-    const int grid = grid_for(p.n_warp_tiles, compress_warps(), compress_smem(x_dtype, sch), sms, smem_sm);
+    const int grid = grid_for(p.n_warp_tiles, compress_warps(x_dtype), compress_smem(x_dtype, sch), sms, smem_sm);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (d->scheme == QTA_TACO_FP8 && mode == QTA_SCALE_CURRENT) {
         cudaError_t e = launch_state(out->state, d->batch, STATE_RESET_AMAX, s);
@@ -369,7 +369,7 @@ qta_status taco_decompress(const qta_desc* d, const qta_qtensor* in, void* y, in
     p.lanes_log2 = log2i(p.lanes_per_block);
     p.inv_block = 1.0f / static_cast<float>(d->block);
     p.seg_per_tensor = make_fastdiv(static_cast<uint32_t>(d->rows * d->cols / 64));
-    const int grid = grid_for(p.n_warp_tiles, decompress_warps(), decompress_smem(d->scheme, y_dtype), sms, smem_sm);
+    const int grid = grid_for(p.n_warp_tiles, decompress_warps(y_dtype), decompress_smem(d->scheme, y_dtype), sms, smem_sm);
     return cuda_status(launch_decompress(d->scheme, y_dtype, p, grid, reinterpret_cast<cudaStream_t>(stream)));
 }
 

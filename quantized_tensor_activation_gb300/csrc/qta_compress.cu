@@ -4,7 +4,10 @@
 
 namespace qta {
 
-int compress_warps() { return CompressCfg<IN_BF16, S_TACO>::WARPS; }
+int compress_warps(int in_kind)
+{
+    return in_kind == IN_FP32 ? CompressCfg<IN_FP32, S_TACO>::WARPS : CompressCfg<IN_BF16, S_TACO>::WARPS;
+}
 
 int compress_smem(int in_kind, int scheme)
 {

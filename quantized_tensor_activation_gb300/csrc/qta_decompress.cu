@@ -4,7 +4,10 @@
 
 namespace qta {
 
-int decompress_warps() { return DecompressCfg<S_TACO, IN_BF16>::WARPS; }
+int decompress_warps(int out_kind)
+{
+    return out_kind == IN_FP32 ? DecompressCfg<S_TACO, IN_FP32>::WARPS : DecompressCfg<S_TACO, IN_BF16>::WARPS;
+}
 int reduce_warps() { return ReduceCfg<S_TACO>::WARPS; }
 
 int decompress_smem(int scheme, int out_kind)

@@ -74,38 +74,41 @@ struct ReduceParams {
 };
 
 // ------------------------------------------------------------ configuration
+// Per kernel family: warps per CTA (one CTA per SM; __launch_bounds__ caps
+// the registers at 64K / threads), stages of the per-warp TMA ring, and
+// output staging buffers per warp.  Shared memory per CTA stays below 227 KB.
 template <int IN, int SCH>
 struct CompressCfg {
-    static constexpr int WARPS = 8;
+    static constexpr int WARPS = (IN == IN_FP32) ? 12 : 16;
     static constexpr int IN_SEG = (IN == IN_FP32) ? 256 : 128;
     static constexpr int OUT_SEG = (SCH == S_ASYM4) ? 32 : 64;
-    static constexpr int STAGES = (IN == IN_FP32) ? 2 : 4;
+    static constexpr int STAGES = 2;
     static constexpr int IN_BYTES = 32 * IN_SEG;
     static constexpr int OUT_BYTES = 32 * OUT_SEG;
-    static constexpr int OUT_BUFS = 2;
+    static constexpr int OUT_BUFS = (IN == IN_FP32) ? 1 : 2;
     static constexpr int WARP_SMEM = STAGES * IN_BYTES + OUT_BUFS * OUT_BYTES;
     static constexpr int SMEM = WARPS * WARP_SMEM + WARPS * STAGES * 8 + 1024;
 };
 
 template <int SCH, int OUT>
 struct DecompressCfg {
-    static constexpr int WARPS = 8;
+    static constexpr int WARPS = (OUT == IN_FP32) ? 12 : 16;
     static constexpr int IN_SEG = (SCH == S_ASYM4) ? 32 : 64;
     static constexpr int OUT_SEG = (OUT == IN_FP32) ? 256 : 128;
-    static constexpr int STAGES = 6;
+    static constexpr int STAGES = 4;
     static constexpr int IN_BYTES = 32 * IN_SEG;
     static constexpr int OUT_BYTES = 32 * OUT_SEG;
-    static constexpr int OUT_BUFS = 2;
+    static constexpr int OUT_BUFS = 1;
     static constexpr int WARP_SMEM = STAGES * IN_BYTES + OUT_BUFS * OUT_BYTES;
     static constexpr int SMEM = WARPS * WARP_SMEM + WARPS * STAGES * 8 + 1024;
 };
 
 template <int SCH>
 struct ReduceCfg {
-    static constexpr int WARPS = 8;
+    static constexpr int WARPS = 12;
     static constexpr int IN_SEG = (SCH == S_ASYM4) ? 32 : 64;
     static constexpr int OUT_SEG = 256;
-    static constexpr int STAGES = (SCH == S_ASYM4) ? 12 : 8;
+    static constexpr int STAGES = (SCH == S_ASYM4) ? 8 : 4;
     static constexpr int IN_BYTES = 32 * IN_SEG;
     static constexpr int OUT_BYTES = 32 * OUT_SEG;
     static constexpr int OUT_BUFS = 1;
@@ -201,20 +204,23 @@ __device__ __forceinline__ void load_codes4(const uint8_t* st, int lane, uint32_
 // TACO  E4M3(q) * s          (s = S * r_b)
 // INT8  q * s
 // ASYM  fmaf(q, s, z)
-template <int SCH>
+// MODE 0 writes v = dequant, MODE 1 accumulates v += dequant (the product is
+// rounded to FP32 first, then added).
+template <int SCH, int MODE>
 __device__ __forceinline__ void dequant_segment(const uint8_t* st, int lane, float s, float z, u64 (&v)[32])
 {
     const u64 s2 = pk2(s, s);
+    const u64 z2 = pk2(z, z);
+    auto put = [&](int j, u64 d) { v[j] = (MODE == 0) ? d : add2(v[j], d); };
     if constexpr (SCH == S_ASYM4) {
         uint32_t q[8];
         load_codes4(st, lane, q);
-        const u64 z2 = pk2(z, z);
 #pragma unroll
         for (int w = 0; w < 8; ++w) {
             u64 p[4];
             u4x8_to_pairs(q[w], p);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) v[w * 4 + k] = fma2(p[k], s2, z2);
+            for (int k = 0; k < 4; ++k) put(w * 4 + k, fma2(p[k], s2, z2));
         }
     } else {
         uint32_t q[16];
@@ -222,19 +228,18 @@ __device__ __forceinline__ void dequant_segment(const uint8_t* st, int lane, flo
 #pragma unroll
         for (int w = 0; w < 16; ++w) {
             if constexpr (SCH == S_TACO) {
-                v[2 * w] = mul2(e4m3x2_decode(lo16(q[w])), s2);
-                v[2 * w + 1] = mul2(e4m3x2_decode(hi16(q[w])), s2);
+                put(2 * w, mul2(e4m3x2_decode(lo16(q[w])), s2));
+                put(2 * w + 1, mul2(e4m3x2_decode(hi16(q[w])), s2));
             } else if constexpr (SCH == S_INT8SYM) {
                 u64 a, b;
                 s8x4_to_pairs(q[w], a, b);
-                v[2 * w] = mul2(a, s2);
-                v[2 * w + 1] = mul2(b, s2);
+                put(2 * w, mul2(a, s2));
+                put(2 * w + 1, mul2(b, s2));
             } else {
                 u64 a, b;
                 u8x4_to_pairs(q[w], a, b);
-                const u64 z2 = pk2(z, z);
-                v[2 * w] = fma2(a, s2, z2);
-                v[2 * w + 1] = fma2(b, s2, z2);
+                put(2 * w, fma2(a, s2, z2));
+                put(2 * w + 1, fma2(b, s2, z2));
             }
         }
     }
@@ -402,11 +407,15 @@ compress_kernel(const __grid_constant__ CompressParams p)
             float inv = (a > 0.0f) ? __fdiv_rn(127.0f, a) : 0.0f;
             if (inv > 3.40282347e+38f) inv = 0.0f;   // absmax below 127/FLT_MAX: zero codes
             const u64 inv2 = pk2(inv, inv);
-            // |x * inv| <= 127.00002 < 127.5 here, so no clamp is needed
+            // |x * inv| <= 127.00002 < 127.5, so clamping from below at -127
+            // changes no code; it also keeps the product rounded to FP32 on its
+            // own before the rounding add (a fused multiply-add would round once).
 #pragma unroll
             for (int w = 0; w < 16; ++w) {
-                const u64 r0 = rint_bits2(mul2(v[2 * w], inv2));
-                const u64 r1 = rint_bits2(mul2(v[2 * w + 1], inv2));
+                const float2 y0 = up2(mul2(v[2 * w], inv2));
+                const float2 y1 = up2(mul2(v[2 * w + 1], inv2));
+                const u64 r0 = rint_bits2(pk2(fmaxf(y0.x, -127.0f), fmaxf(y0.y, -127.0f)));
+                const u64 r1 = rint_bits2(pk2(fmaxf(y1.x, -127.0f), fmaxf(y1.y, -127.0f)));
                 ow[w] = bytes4(lo32(r0), hi32(r0), lo32(r1), hi32(r1));
             }
             if (valid) static_cast<float*>(p.scales)[g] = s;
@@ -456,8 +465,13 @@ compress_kernel(const __grid_constant__ CompressParams p)
 
         if constexpr (!AMAX_ONLY) {
             // stage the codes and store them with one TMA per warp tile
-            uint8_t* ob = outb + (k & 1) * C::OUT_BYTES;
-            if (lane == 0) bulk_wait_read<1>();
+            uint8_t* ob = outb + (k % C::OUT_BUFS) * C::OUT_BYTES;
+            if (lane == 0) {
+                if constexpr (C::OUT_BUFS == 1)
+                    bulk_wait_read<0>();
+                else
+                    bulk_wait_read<1>();
+            }
             __syncwarp();
             if constexpr (SCH == S_ASYM4) {
 #pragma unroll
@@ -568,7 +582,7 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
         float s, z;
         cur.decode(s, z);
         u64 v[32];
-        dequant_segment<SCH>(wb + stage * C::IN_BYTES, lane, s, z, v);
+        dequant_segment<SCH, 0>(wb + stage * C::IN_BYTES, lane, s, z, v);
         __syncwarp();
         {
             const int nwt = wt + C::STAGES * W;
@@ -589,8 +603,13 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = mul2(v[j], ib);
         }
-        uint8_t* ob = outb + (k & 1) * C::OUT_BYTES;
-        if (lane == 0) bulk_wait_read<1>();
+        uint8_t* ob = outb + (k % C::OUT_BUFS) * C::OUT_BYTES;
+        if (lane == 0) {
+            if constexpr (C::OUT_BUFS == 1)
+                bulk_wait_read<0>();
+            else
+                bulk_wait_read<1>();
+        }
         __syncwarp();
         store_segment<OUT>(ob, lane, v);
         fence_proxy_async_smem();
@@ -703,8 +722,10 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                 }
                 float s, z;
                 cur[kk].decode(s, z);
-                u64 v[32];
-                dequant_segment<SCH>(wb + stage * C::IN_BYTES, lane, s, z, v);
+                if (r == 0)
+                    dequant_segment<SCH, 0>(wb + stage * C::IN_BYTES, lane, s, z, acc);
+                else
+                    dequant_segment<SCH, 1>(wb + stage * C::IN_BYTES, lane, s, z, acc);
                 __syncwarp();
                 if (lane == 0 && unit + C::STAGES < total_units) {
                     fence_proxy_async_smem();
@@ -714,13 +735,6 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                 if (++stage == C::STAGES) {
                     stage = 0;
                     phase ^= 1u;
-                }
-                if (r == 0) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) acc[j] = v[j];
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) acc[j] = add2(acc[j], v[j]);
                 }
             }
         }

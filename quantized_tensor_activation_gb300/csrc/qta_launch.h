@@ -13,8 +13,8 @@ int decompress_smem(int scheme, int out_kind);
 int reduce_smem(int scheme);
 
 // Warps per CTA of each kernel family.
-int compress_warps();
-int decompress_warps();
+int compress_warps(int in_kind);
+int decompress_warps(int out_kind);
 int reduce_warps();
 
 cudaError_t launch_compress(int in_kind, int scheme, bool amax_only, const CompressParams& p, int grid,

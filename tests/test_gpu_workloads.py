@@ -1,0 +1,114 @@
+"""Full-size parity: every workload at its full size, through the same calls
+and launch configuration the benchmark times, checked against the oracle on
+sampled rows (the oracle computes those rows from the inputs alone) and on
+per-tensor quantities the oracle computes over whole tensors.
+
+Step checked: compress all ranks (CURRENT mode for TACO, so the per-tensor
+scale is a function of the data) -> dequantize-reduce all rows -> requantize
+the sum for the gather stage (DELAYED, with a per-shard scale fixed by the
+test) -> decompress."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+import quantized_tensor_activation_gb300 as qta
+import workloads
+from gpu_util import ORC_SCH, assert_close_f32, assert_same, bits, device
+
+pytestmark = pytest.mark.gpu
+
+N_SAMPLE_ROWS = 12
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return device()
+
+
+def _rows_of(buf: torch.Tensor, rows_idx, per_row: int) -> np.ndarray:
+    """Bytes of the given rows of a flat byte buffer with per_row bytes/row."""
+    b = buf.view(-1, per_row)[torch.as_tensor(rows_idx, device=buf.device)]
+    return bits(b)
+
+
+@pytest.mark.parametrize("name", ["taco_tiny", "gpt_tp", "qwen_grad", "equarx_int8", "flash_int4"])
+def test_workload_full_size(dev, name):
+    w = workloads.WORKLOADS[name]
+    N, R, C, B, gB = w.ranks, w.rows, w.cols, w.block, w.gather_block
+    s1, s2 = qta.SCHEMES[w.scheme], qta.SCHEMES[w.gather_scheme]
+    in_dt = qta.BF16 if w.dtype == "bf16" else qta.FP16
+    o_dt = orc.BF16 if w.dtype == "bf16" else orc.FP16
+    x = workloads.make_rank_inputs(w, device=dev, seed=7)
+
+    # ---- the benchmark's calls
+    d_in = qta.desc(s1, B, R, C, batch=N)
+    q = qta.alloc_qtensor(d_in, dev)
+    mode = qta.SCALE_CURRENT if s1 == qta.TACO_FP8 else qta.SCALE_DELAYED
+    qta.taco_compress(d_in, x, in_dt, q, mode)
+    d1 = qta.desc(s1, B, R, C)
+    ssum = torch.empty((R, C), dtype=torch.float32, device=dev)
+    qta.qar_reduce(d1, [q.shard(r) for r in range(N)], 0, R, ssum)
+    gr = R // N
+    d_g = qta.desc(s2, gB, gr, C, batch=N)
+    g = qta.alloc_qtensor(d_g, dev)
+    S2 = np.array([0.0, 0.0] * N, dtype=np.float32)
+    S2[0::2] = [2.0 ** -7 * (1 + 0.25 * j) for j in range(N)]   # fixed gather-stage scales
+    if g.state is not None:
+        g.state.copy_(torch.from_numpy(S2))
+    qta.qar_requant(d_g, ssum, g, qta.SCALE_DELAYED)
+    y = torch.empty((R, C), dtype=w.torch_dtype, device=dev)
+    qta.taco_decompress(d_g, g, y, in_dt)
+    torch.cuda.synchronize()
+    assert qta.qta_device_error() == 0
+
+    # ---- per-tensor scale (TACO, CURRENT mode): oracle over whole tensors
+    st = None
+    if s1 == qta.TACO_FP8:
+        st = np.zeros(2 * N, dtype=np.float32)
+        for r in range(N):
+            xr = x[r].float().cpu().numpy().reshape(-1)
+            amax = np.float32(np.abs(orc.fwht(xr, B)).max())
+            st[2 * r] = orc.scale_from_amax(amax)
+            st[2 * r + 1] = amax
+        assert_same("per-tensor state", q.state, st)
+
+    # ---- sampled rows
+    rng = np.random.default_rng(hash(name) % 2 ** 32)
+    rows = np.unique(np.concatenate([[0, R - 1, gr - 1, gr], rng.choice(R, N_SAMPLE_ROWS, replace=False)]))
+    k = len(rows)
+    xs = x[:, torch.as_tensor(rows, device=dev)].contiguous().cpu()              # [N, k, C]
+    xb = bits(xs)
+    cpr = C // 2 if s1 == qta.INT4_ASYM_G128 else C                              # code bytes per row
+    ref = []
+    for r in range(N):
+        st_r = None if st is None else st[2 * r:2 * r + 2].copy()
+        c, s, z = orc.compress(ORC_SCH[s1], B, xb[r * k * C:(r + 1) * k * C], o_dt, 1, k, C, st_r, orc.DELAYED)
+        ref.append((c, s, z, st_r))
+        # the GPU's codes / scales of those rows of rank r
+        sh = q.shard(r)
+        assert_same(f"rank {r} codes", _rows_of(sh.codes, rows, cpr), c)
+        sbytes = {qta.TACO_FP8: 1, qta.INT8_SYM_B64: 4}.get(s1, 2) * (C // B)
+        assert_same(f"rank {r} scales", _rows_of(sh.scales, rows, sbytes), s)
+        if z is not None:
+            assert_same(f"rank {r} zeros", _rows_of(sh.zeros, rows, sbytes), z)
+    osum = orc.reduce(ORC_SCH[s1], B, ref, k, C)
+    gsum = ssum[torch.as_tensor(rows, device=dev)]
+    assert_same("sum rows", gsum, osum)
+    assert_close_f32("sum rows", gsum, osum)
+
+    # requant of the sampled rows: each row belongs to shard row // gr
+    gcodes = []
+    for i, row in enumerate(rows):
+        j = row // gr
+        stj = None if g.state is None else S2[2 * j:2 * j + 2].copy()
+        c, s, z = orc.compress(ORC_SCH[s2], gB, osum[i * C:(i + 1) * C], orc.FP32, 1, 1, C, stj, orc.DELAYED)
+        gcodes.append((c, s, z, stj))
+    gcpr = C // 2 if s2 == qta.INT4_ASYM_G128 else C
+    gsb = {qta.TACO_FP8: 1, qta.INT8_SYM_B64: 4}.get(s2, 2) * (C // gB)
+    assert_same("requant codes", _rows_of(g.codes, rows, gcpr), np.concatenate([c[0] for c in gcodes]))
+    assert_same("requant scales", _rows_of(g.scales, rows, gsb), np.concatenate([c[1] for c in gcodes]))
+    if gcodes[0][2] is not None:
+        assert_same("requant zeros", _rows_of(g.zeros, rows, gsb), np.concatenate([c[2] for c in gcodes]))
+    yo = np.concatenate([orc.decompress(ORC_SCH[s2], gB, c, s, z, stj, 1, 1, C, o_dt) for c, s, z, stj in gcodes])
+    assert_same("output rows", y[torch.as_tensor(rows, device=dev)], yo)
