@@ -343,6 +343,20 @@ int orc_compress(int scheme, int B, const void* x, int in_dtype, int64_t batch,
     return 0;
 }
 
+/* The decoded code (exact) and the FP32 dequantization scale of element e
+ * for the symmetric schemes: TACO E4M3(q) and s_b = S * r_b; INT8 q and s. */
+static void code_and_scale(int scheme, int B, const void* codes, const void* scales, const float* st,
+                           int64_t e, float* code, float* sc)
+{
+    if (scheme == ORC_TACO_FP8) {
+        *sc = st[0] * orc_e4m3_decode(((const uint8_t*)scales)[e / B]);
+        *code = orc_e4m3_decode(((const uint8_t*)codes)[e]);
+    } else {
+        *sc = ((const float*)scales)[e / 64];
+        *code = (float)((const int8_t*)codes)[e];
+    }
+}
+
 /* Dequantized value of element e (flat index within one tensor) in FP32.
  * TACO: E4M3 code times s_b = S * r_b, before the inverse transform.
  * INT8: q * s.  ASYM: fmaf(q, s, z) (one rounding, R7). */
@@ -409,9 +423,14 @@ int orc_decompress(int scheme, int B, const void* codes, const void* scales,
 /* Dequantize-reduce ([EQuARX] What carries the argument: every received
  * shard is dequantized to FP32 before it is added, partial sums stay FP32;
  * [FLASH] What carries the argument: local FP32 sum after the All2All).
- * R9: per element, v_r = dequant(shard r) in FP32, then acc = v_0 + v_1 +
- * ... + v_{N-1} left to right in rank order.  TACO sums in the Hadamard
- * domain and applies the inverse transform once to the sum (then 1/B). */
+ * R9: per element, in rank order r = 0 .. N-1, with the dequantized term in
+ * FP32 arithmetic entering the FP32 partial sum:
+ *   TACO, INT8:  acc = code_0 * s_0;  acc = fmaf(code_r, s_r, acc)
+ *                (the product code * scale is exact inside the fused
+ *                multiply-add; one FP32 rounding per rank)
+ *   ASYM:        acc = fmaf(q_0, s_0, z_0);  acc = acc + fmaf(q_r, s_r, z_r)
+ * TACO sums in the Hadamard domain and applies the inverse transform once to
+ * the sum (then 1/B). */
 int orc_reduce(int scheme, int B, int n_ranks, const void* const* codes,
                const void* const* scales, const void* const* zeros,
                const float* const* states, int64_t rows, int64_t cols,
@@ -424,9 +443,17 @@ int orc_reduce(int scheme, int B, int n_ranks, const void* const* codes,
         for (int i = 0; i < B; ++i) {
             float acc = 0.0f;
             for (int r = 0; r < n_ranks; ++r) {
-                float v = dequant(scheme, B, codes[r], scales[r], zeros ? zeros[r] : 0,
-                                  states ? states[r] : 0, b0 + i);
-                acc = (r == 0) ? v : acc + v;
+                const void* z = zeros ? zeros[r] : 0;
+                const float* st = states ? states[r] : 0;
+                if (r == 0) {
+                    acc = dequant(scheme, B, codes[r], scales[r], z, st, b0 + i);
+                } else if (scheme == ORC_TACO_FP8 || scheme == ORC_INT8_SYM) {
+                    float code, sc;
+                    code_and_scale(scheme, B, codes[r], scales[r], st, b0 + i, &code, &sc);
+                    acc = fmaf(code, sc, acc);
+                } else {
+                    acc = acc + dequant(scheme, B, codes[r], scales[r], z, st, b0 + i);
+                }
             }
             sum_out[b0 - e0 + i] = acc;
         }

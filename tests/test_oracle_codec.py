@@ -261,3 +261,52 @@ def test_reduce_matches_float64_sum(orc, scheme, B):
     # a row range gives the same rows as the full reduction
     part = orc.reduce(scheme, B, shards, rows, cols, 3, 7)
     assert np.array_equal(part, out[3 * cols:7 * cols])
+
+
+def _round_f32(x):
+    """Exact rational -> nearest binary32 (ties to even), by integer arithmetic."""
+    from fractions import Fraction
+    if x == 0:
+        return 0.0
+    sign = -1 if x < 0 else 1
+    a = abs(Fraction(x))
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    e = max(e, -126) - 23                     # grid step 2^e (subnormals: 2^-149)
+    q = a / Fraction(2) ** e
+    n = q.numerator // q.denominator
+    rem = q - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return sign * float(n * Fraction(2) ** e)
+
+
+@pytest.mark.parametrize("scheme,B", [(0, 128), (1, 64)])
+def test_reduce_accumulates_with_one_rounding_per_rank(orc, scheme, B):
+    # R9: acc = RN(c0*s0), then acc = RN(c1*s1 + acc) with the product exact
+    # (a fused multiply-add); emulated here with exact rationals.
+    from fractions import Fraction
+    rows, cols = 2, 256
+    shards, _ = _make_shards(orc, scheme, B, 3, rows, cols, seed=9)
+    out = orc.reduce(scheme, B, shards, rows, cols)
+    table = _e4m3_pos()
+    E = rows * cols
+    acc = np.zeros(E, dtype=np.float64)
+    for e in range(E):
+        a = None
+        for r, (c, s, z, st) in enumerate(shards):
+            if scheme == orc.TACO_FP8:
+                code = Fraction(float(table[c[e]]))
+                sc = Fraction(float(np.float32(st[0]) * table[s[e // B]]))
+            else:
+                code = Fraction(int(c[e]))
+                sc = Fraction(float(s[e // 64]))
+            a = _round_f32(code * sc) if r == 0 else _round_f32(code * sc + Fraction(a))
+        acc[e] = a
+    ref = acc.astype(np.float32)
+    if scheme == orc.TACO_FP8:
+        ref = (orc.fwht(ref, B) * np.float32(1.0 / B)).astype(np.float32)
+    assert np.array_equal(out.view(np.uint32), ref.view(np.uint32))
