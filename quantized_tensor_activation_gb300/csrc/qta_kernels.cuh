@@ -200,18 +200,33 @@ __device__ __forceinline__ void load_codes4(const uint8_t* st, int lane, uint32_
     }
 }
 
-// Dequantized FP32 pairs of one segment's codes (before any transform):
-// TACO  E4M3(q) * s          (s = S * r_b)
-// INT8  q * s
-// ASYM  fmaf(q, s, z)
-// MODE 0 writes v = dequant, MODE 1 accumulates v += dequant (the product is
-// rounded to FP32 first, then added).
+// Dequantization of one segment's codes (before any transform).
+// MODE 0 (assign):     TACO E4M3(q)*s, INT8 q*s   -- scalar mul.rn
+//                      ASYM fmaf(q, s, z)
+// MODE 1 (accumulate): TACO/INT8 v = fmaf(code, s, v)
+//                      ASYM      v = v + fmaf(q, s, z)
+// The assigning multiply is scalar because ptxas contracts a packed
+// multiply into a packed add that consumes it in the same basic block;
+// scalar mul.rn is never contracted, so the product is rounded on its own
+// exactly as defined.
 template <int SCH, int MODE>
 __device__ __forceinline__ void dequant_segment(const uint8_t* st, int lane, float s, float z, u64 (&v)[32])
 {
     const u64 s2 = pk2(s, s);
     const u64 z2 = pk2(z, z);
-    auto put = [&](int j, u64 d) { v[j] = (MODE == 0) ? d : add2(v[j], d); };
+    // code pair c (exact) -> v[j]
+    auto sym = [&](int j, u64 c) {
+        if constexpr (MODE == 0) {
+            const float2 t = up2(c);
+            v[j] = pk2(__fmul_rn(t.x, s), __fmul_rn(t.y, s));
+        } else {
+            v[j] = fma2(c, s2, v[j]);
+        }
+    };
+    auto asym = [&](int j, u64 c) {
+        const u64 d = fma2(c, s2, z2);
+        v[j] = (MODE == 0) ? d : add2(v[j], d);
+    };
     if constexpr (SCH == S_ASYM4) {
         uint32_t q[8];
         load_codes4(st, lane, q);
@@ -220,7 +235,7 @@ __device__ __forceinline__ void dequant_segment(const uint8_t* st, int lane, flo
             u64 p[4];
             u4x8_to_pairs(q[w], p);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) put(w * 4 + k, fma2(p[k], s2, z2));
+            for (int k = 0; k < 4; ++k) asym(w * 4 + k, p[k]);
         }
     } else {
         uint32_t q[16];
@@ -228,18 +243,18 @@ __device__ __forceinline__ void dequant_segment(const uint8_t* st, int lane, flo
 #pragma unroll
         for (int w = 0; w < 16; ++w) {
             if constexpr (SCH == S_TACO) {
-                put(2 * w, mul2(e4m3x2_decode(lo16(q[w])), s2));
-                put(2 * w + 1, mul2(e4m3x2_decode(hi16(q[w])), s2));
+                sym(2 * w, e4m3x2_decode(lo16(q[w])));
+                sym(2 * w + 1, e4m3x2_decode(hi16(q[w])));
             } else if constexpr (SCH == S_INT8SYM) {
                 u64 a, b;
                 s8x4_to_pairs(q[w], a, b);
-                put(2 * w, mul2(a, s2));
-                put(2 * w + 1, mul2(b, s2));
+                sym(2 * w, a);
+                sym(2 * w + 1, b);
             } else {
                 u64 a, b;
                 u8x4_to_pairs(q[w], a, b);
-                put(2 * w, fma2(a, s2, z2));
-                put(2 * w + 1, fma2(b, s2, z2));
+                asym(2 * w, a);
+                asym(2 * w + 1, b);
             }
         }
     }
