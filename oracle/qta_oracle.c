@@ -52,7 +52,7 @@ float orc_e4m3_decode(uint8_t c)
 }
 
 /* Encode with round-to-nearest-even onto the E4M3 grid; magnitudes that
- * round above 448 saturate to 448 ("saturation at 448"), +-Inf -> +-448,
+ * round above 448 saturate to 448, +-Inf -> +-448,
  * NaN -> 0x7F.  The sign of zero is kept. */
 uint8_t orc_e4m3_encode(float v)
 {
@@ -420,8 +420,8 @@ int orc_decompress(int scheme, int B, const void* codes, const void* scales,
     return 0;
 }
 
-/* Dequantize-reduce ([EQuARX] What carries the argument: every received
- * shard is dequantized to FP32 before it is added, partial sums stay FP32;
+/* Dequantize-reduce ([EQuARX] What carries the argument: each received shard
+ * is converted to FP32 first and the partial sums are kept in FP32;
  * [FLASH] What carries the argument: local FP32 sum after the All2All).
  * R9: per element, in rank order r = 0 .. N-1, with the dequantized term in
  * FP32 arithmetic entering the FP32 partial sum:
