@@ -209,8 +209,9 @@ def algorithmic_bytes(w):
     k1 = N * E * (2 + codes(w.scheme) + meta(w.scheme, w.block))
     k2 = N * E * (codes(w.scheme) + meta(w.scheme, w.block)) + E * 4
     k3 = E * (4 + codes(w.gather_scheme) + meta(w.gather_scheme, w.gather_block))
+    k23 = k2 - E * 4 + k3 - E * 4
     k4 = E * (codes(w.gather_scheme) + meta(w.gather_scheme, w.gather_block) + 2)
-    return {"K1": k1, "K2": k2, "K3": k3, "K4": k4}
+    return {"K1": k1, "K2": k2, "K3": k3, "K23": k23, "K4": k4}
 
 
 def run_qta(args, w):
@@ -234,6 +235,8 @@ def run_qta(args, w):
     d_in = qta.desc(sch[w.scheme], w.block, R, C, batch=N)
     d_sh = qta.desc(sch[w.scheme], w.block, R, C)
     d_g = qta.desc(sch[w.gather_scheme], w.gather_block, R // N, C, batch=N)
+    taco1 = w.scheme == "taco_fp8"
+    taco2 = w.gather_scheme == "taco_fp8"
     q = qta.alloc_qtensor(d_in, dev)
     g = qta.alloc_qtensor(d_g, dev)
     # both stages' per-tensor states live in one buffer so that one
@@ -251,12 +254,10 @@ def run_qta(args, w):
     ssum = torch.empty((R, C), dtype=torch.float32, device=dev)
     y = torch.empty((R, C), dtype=tdt, device=dev)
     stream = torch.cuda.current_stream()
-    taco1 = w.scheme == "taco_fp8"
-    taco2 = w.gather_scheme == "taco_fp8"
 
     launches = [0]
 
-    def step(first=False, ev=None):
+    def step(first=False, ev=None, fused=True):
         # each compress uses the per-tensor scale left by the previous step and
         # accumulates this step's amax; the receiving side dequantizes with the
         # same scale, so the states are updated once, at the end of the step
@@ -266,12 +267,18 @@ def run_qta(args, w):
         qta.taco_compress(d_in, x, in_dt, q, mode)
         if ev:
             ev[1].record(stream)
-        qta.qar_reduce(d_sh, shards, 0, R, ssum)
-        if ev:
-            ev[2].record(stream)
-        qta.qar_requant(d_g, ssum, g, mode)
-        if ev:
-            ev[3].record(stream)
+        if fused:
+            qta.qar_reduce_requant(d_sh, shards, 0, R, d_g, g, mode)
+            if ev:
+                ev[2].record(stream)
+                ev[3].record(stream)
+        else:
+            qta.qar_reduce(d_sh, shards, 0, R, ssum)
+            if ev:
+                ev[2].record(stream)
+            qta.qar_requant(d_g, ssum, g, mode)
+            if ev:
+                ev[3].record(stream)
         qta.taco_decompress(d_g, g, y, in_dt)
         if ev:
             ev[4].record(stream)
@@ -279,12 +286,14 @@ def run_qta(args, w):
             qta.taco_update_scale(states, n_state)
         if ev:
             ev[5].record(stream)
-        launches[0] += 4 + int(n_state > 0)
+        launches[0] += (3 if fused else 4) + int(n_state > 0)
 
-    # warm-up (first step in CURRENT mode, the rest as timed)
-    step(first=True)
+    fused = args.path == "fused"
+    # warm-up (first step in CURRENT mode, the rest as timed), both paths
+    step(first=True, fused=fused)
     for _ in range(max(args.warmup, 3) - 1):
-        step()
+        step(fused=fused)
+        step(fused=not fused)
     torch.cuda.synchronize()
     assert qta.qta_device_error() == 0
 
@@ -293,13 +302,23 @@ def run_qta(args, w):
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
     for _ in range(3):
-        step()
+        step(fused=fused)
     b.record(stream)
     torch.cuda.synchronize()
     pad = 0 if args.no_clocks else max(1, int(600.0 / max(a.elapsed_time(b) / 3, 1e-3)))
 
+    def timed(fused_path):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        launches[0] = 0
+        t0.record(stream)
+        for i in range(args.steps):
+            step(ev=evs[i], fused=fused_path)
+        t1.record(stream)
+        return evs, t0, t1, launches[0]
+
     # ---- timed region: inputs resident in HBM
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     clocks = ClockSampler(None if args.no_clocks else _smi_gpu_id(torch, local))
     if ws > 1:
         torch.distributed.barrier()
@@ -308,20 +327,13 @@ def run_qta(args, w):
     if not args.no_clocks:
         time.sleep(0.3)
     for _ in range(pad):
-        step()
+        step(fused=fused)
     if ws > 1:
         torch.cuda.synchronize()
         torch.distributed.barrier()
-    launches[0] = 0
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        step(ev=evs[i])
-    t_end.record(stream)
-    n_launch = launches[0]
+    evs, t_start, t_end, n_launch = timed(fused)
     for _ in range(pad):
-        step()
+        step(fused=fused)
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
@@ -338,6 +350,10 @@ def run_qta(args, w):
         t = torch.tensor([ms_step], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms_step = float(t.item())
+    # the other path (two calls, FP32 sum through HBM), for comparison
+    evs2, s2a, s2b, _ = timed(not fused)
+    torch.cuda.synchronize()
+    other_ms = s2a.elapsed_time(s2b) / args.steps
     assert qta.qta_device_error() == 0
 
     # ---- end to end through the public API with host buffers
@@ -351,8 +367,11 @@ def run_qta(args, w):
         def e2e_step():
             xd.copy_(xh, non_blocking=True)
             qta.taco_compress(d_in, xd, in_dt, q, qta.SCALE_DELAYED)
-            qta.qar_reduce(d_sh, shards, 0, R, ssum)
-            qta.qar_requant(d_g, ssum, g, qta.SCALE_DELAYED)
+            if fused:
+                qta.qar_reduce_requant(d_sh, shards, 0, R, d_g, g, qta.SCALE_DELAYED)
+            else:
+                qta.qar_reduce(d_sh, shards, 0, R, ssum)
+                qta.qar_requant(d_g, ssum, g, qta.SCALE_DELAYED)
             qta.taco_decompress(d_g, g, y, in_dt)
             if n_state:
                 qta.taco_update_scale(states, n_state)
@@ -382,12 +401,18 @@ def run_qta(args, w):
     value = in_bytes / (ms_step * 1e-3) / 1e9 * ws
     peak, peak_kind = _peaks()
     alg = algorithmic_bytes(w)
+    names = {"K1": "taco_compress", "K2": "qar_reduce_requant" if fused else "qar_reduce",
+             "K3": None if fused else "qar_requant", "K4": "taco_decompress"}
     kern = {}
-    for k, name in (("K1", "K1"), ("K2", "K2"), ("K3", "K3"), ("K4", "K4")):
+    for k in ("K1", "K2", "K3", "K4"):
+        if names[k] is None:
+            continue
         ms = statistics.mean(per[k])
-        kern[name] = {"ms": ms, "gb_s": alg[name] / (ms * 1e-3) / 1e9,
-                      "frac_of_hbm": alg[name] / (ms * 1e-3) / 1e9 / peak,
-                      "input_gb_s": (in_bytes / (ms * 1e-3) / 1e9) if name == "K1" else None}
+        nbytes = alg["K23"] if (k == "K2" and fused) else alg[k]
+        kern[k] = {"call": names[k], "ms": ms, "gb_s": nbytes / (ms * 1e-3) / 1e9,
+                   "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / peak, "algorithmic_bytes": nbytes}
+    kern["U"] = {"call": "taco_update_scale", "ms": statistics.mean(per["U"])}
+    step_bytes = alg["K1"] + alg["K4"] + (alg["K23"] if fused else alg["K2"] + alg["K3"])
     k1_ms = statistics.mean(per["K1"])
     achieved = alg["K1"] / (k1_ms * 1e-3) / 1e9
     tr = NCU_TRAFFIC.get(("taco_compress", w.name))
@@ -408,8 +433,11 @@ def run_qta(args, w):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "kernel": "K1 taco_compress",
                      "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes": alg["K1"]},
+        "path": "fused reduce+requant (qar_reduce_requant)" if fused else "qar_reduce + qar_requant",
         "kernels": kern,
-        "step_frac_of_hbm": sum(alg.values()) / (ms_step * 1e-3) / 1e9 / peak,
+        "step_frac_of_hbm": step_bytes / (ms_step * 1e-3) / 1e9 / peak,
+        "other_path": {"path": "qar_reduce + qar_requant" if fused else "qar_reduce_requant",
+                       "ms_per_step": other_ms, "value": in_bytes / (other_ms * 1e-3) / 1e9 * ws},
         "cpu_baseline": cpu,
         "clocks": clk,
         "e2e": e2e,
@@ -433,6 +461,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="skip the nvidia-smi clock window (profiling runs)")
+    ap.add_argument("--path", default="fused", choices=["fused", "split"],
+                    help="fused: qar_reduce_requant; split: qar_reduce then qar_requant (FP32 sum in HBM)")
     args = ap.parse_args(argv)
     w = workloads.WORKLOADS[args.workload]
     if args.impl == "reference":

@@ -14,8 +14,8 @@
  *   [EQuARX] "EQuARX: Efficient Quantized AllReduce in XLA for Distributed
  *            Machine Learning Acceleration" -- What carries the argument:
  *            block-wise dynamic int8 with one FP32 scale per 64 entries,
- *            Qp1 (metadata) / Qp2 (scale data), receivers dequantize every
- *            shard to FP32 before adding; reduce-scatter + all-gather.
+ *            Qp1 (metadata) / Qp2 (scale data), shards converted to FP32
+ *            on receipt and summed in FP32; reduce-scatter + all-gather.
  *   [FLASH]  "Flash Communication: Reducing Tensor Parallelization
  *            Bottleneck for Fast Large Language Model Inference" -- What
  *            carries the argument: asymmetric group-128 quantization, two-
@@ -148,17 +148,37 @@ qta_status taco_decompress(const qta_desc* d, const qta_qtensor* in, void* y,
                            int32_t y_dtype, qta_stream_t stream);
 
 /* qar_reduce -- dequantize-reduce of a quantized reduce-scatter [EQuARX:
- * every received shard is dequantized to FP32 before it is added; FLASH:
- * local FP32 sum after the All2All].  `shards` is a HOST array of n_ranks
- * quantized tensors (device buffers), each described by `d` (batch must be
- * 1), 1 <= n_ranks <= 16.  For every element of rows [row_begin, row_end):
- * v_r = dequantized value of shard r in FP32, sum = v_0 + v_1 + ... in rank
- * order; for QTA_TACO_FP8 the sum is formed in the Hadamard domain and the
- * inverse transform (butterfly, then 1/B) is applied once to it.
+ * received shards are converted to FP32 and the partial sums kept in FP32;
+ * FLASH: local FP32 sum after the All2All].  `shards` is a HOST array of
+ * n_ranks quantized tensors (device buffers), each described by `d` (batch
+ * must be 1), 1 <= n_ranks <= 16.  For every element of rows
+ * [row_begin, row_end), in rank order: TACO / INT8 sym acc = code_0 * s_0,
+ * then acc = fmaf(code_r, s_r, acc) (one FP32 rounding per rank); asym
+ * acc = fmaf(q_0, s_0, z_0), then acc += fmaf(q_r, s_r, z_r).  For
+ * QTA_TACO_FP8 the sum is formed in the Hadamard domain and the inverse
+ * transform (butterfly, then 1/B) is applied once to it.
  * sum_out: device f32 [row_end-row_begin, cols], 16-byte aligned. */
 qta_status qar_reduce(const qta_desc* d, const qta_qtensor* shards, int32_t n_ranks,
                       int64_t row_begin, int64_t row_end, float* sum_out,
                       qta_stream_t stream);
+
+/* qar_reduce_requant -- qar_reduce followed by qar_requant in one kernel: the
+ * FP32 sum of rows [row_begin, row_end) is formed exactly as qar_reduce forms
+ * it and quantized exactly as qar_requant quantizes an FP32 input, without
+ * writing the sum to memory; codes, scales, zeros and state are bit-identical
+ * to the two calls.  This is the receiving side of one step of the two-step
+ * all-reduce [FLASH: local FP32 sum, then INT8 requantization before the
+ * All-Gather; TACO Fig. 9: one fused operator instead of several kernels].
+ * `d` and `shards` as for qar_reduce; `out_desc` describes the requantized
+ * rows as out_desc->batch shards of out_desc->rows rows each
+ * (batch * rows == row_end - row_begin, same cols), `out` its buffers, `mode`
+ * its scale mode (QTA_TACO_FP8 output).  Supported scheme pairs (shards ->
+ * output): TACO_FP8 -> TACO_FP8, INT8_SYM_B64 -> INT8_SYM_B64,
+ * INT4_ASYM_G128 -> INT8_ASYM_G128, INT8_ASYM_G128 -> INT8_ASYM_G128; other
+ * pairs return QTA_ERR_UNSUPPORTED (use the two calls). */
+qta_status qar_reduce_requant(const qta_desc* d, const qta_qtensor* shards, int32_t n_ranks,
+                              int64_t row_begin, int64_t row_end, const qta_desc* out_desc,
+                              const qta_qtensor* out, int32_t mode, qta_stream_t stream);
 
 /* qar_requant -- requantization of the FP32 partial sums for the gather
  * stage [FLASH: INT8 requantization before the All-Gather; EQuARX: quantized

@@ -2,7 +2,7 @@
 
 A thin ctypes layer over ``libqta.so`` (C ABI in ``include/qta.h``) with the
 same call names: ``taco_compress``, ``taco_decompress``, ``qar_reduce``,
-``qar_requant``, ``taco_update_scale``, ``qta_copy``.  It only marshals
+``qar_requant``, ``qar_reduce_requant``, ``taco_update_scale``, ``qta_copy``.  It only marshals
 arguments (device pointers, sizes, the current CUDA stream); every step of
 the codec runs in the library's CUDA kernels.  There is no CPU fallback: if
 the library is missing or a call fails, an exception is raised.
@@ -74,11 +74,12 @@ def lib():
         L.taco_decompress.argtypes = [PD, PQ, vp, i32, vp]
         L.qar_reduce.argtypes = [PD, PQ, i32, i64, i64, vp, vp]
         L.qar_requant.argtypes = [PD, vp, PQ, i32, vp]
+        L.qar_reduce_requant.argtypes = [PD, PQ, i32, i64, i64, PD, PQ, i32, vp]
         L.taco_update_scale.argtypes = [vp, i64, vp]
         L.qta_copy.argtypes = [vp, vp, sz, vp]
         L.qta_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
-        for name in ("taco_compress", "taco_decompress", "qar_reduce", "qar_requant", "taco_update_scale",
-                     "qta_copy", "qta_device_error"):
+        for name in ("taco_compress", "taco_decompress", "qar_reduce", "qar_requant", "qar_reduce_requant",
+                     "taco_update_scale", "qta_copy", "qta_device_error"):
             getattr(L, name).restype = ctypes.c_int
         L.qta_status_string.argtypes = [ctypes.c_int]
         L.qta_status_string.restype = ctypes.c_char_p
@@ -195,6 +196,16 @@ def qar_reduce(d: Desc, shards, row_begin: int, row_end: int, sum_out, stream=No
     arr = (QTensorC * max(n, 1))(*[s.c() for s in shards])
     _check("qar_reduce", lib().qar_reduce(ctypes.byref(d), arr, n, row_begin, row_end, _ptr(sum_out),
                                           _stream(stream)))
+
+
+def qar_reduce_requant(d: Desc, shards, row_begin: int, row_end: int, out_desc: Desc, out: QTensor,
+                       mode: int = SCALE_DELAYED, stream=None) -> None:
+    n = len(shards)
+    arr = (QTensorC * max(n, 1))(*[s.c() for s in shards])
+    q = out.c()
+    _check("qar_reduce_requant", lib().qar_reduce_requant(ctypes.byref(d), arr, n, row_begin, row_end,
+                                                          ctypes.byref(out_desc), ctypes.byref(q), mode,
+                                                          _stream(stream)))
 
 
 def qar_requant(d: Desc, sum_in, out: QTensor, mode: int = SCALE_DELAYED, stream=None) -> None:

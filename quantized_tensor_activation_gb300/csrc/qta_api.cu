@@ -373,8 +373,9 @@ qta_status taco_decompress(const qta_desc* d, const qta_qtensor* in, void* y, in
     return cuda_status(launch_decompress(d->scheme, y_dtype, p, grid, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-qta_status qar_reduce(const qta_desc* d, const qta_qtensor* shards, int32_t n_ranks, int64_t row_begin,
-                      int64_t row_end, float* sum_out, qta_stream_t stream)
+// Shared argument checks and parameters of qar_reduce / qar_reduce_requant.
+static qta_status reduce_params(const qta_desc* d, const qta_qtensor* shards, int32_t n_ranks, int64_t row_begin,
+                                int64_t row_end, ReduceParams* p, int* sms, int* smem_sm, bool* empty)
 {
     qta_status st = check_desc(d);
     if (st != QTA_OK) return st;
@@ -383,37 +384,88 @@ qta_status qar_reduce(const qta_desc* d, const qta_qtensor* shards, int32_t n_ra
     if (n_ranks > MAX_RANKS) return QTA_ERR_UNSUPPORTED;
     if (row_begin < 0 || row_end < row_begin || row_end > d->rows) return QTA_ERR_INVALID_ARG;
     if (!shards) return QTA_ERR_INVALID_ARG;
-    if (row_end == row_begin || d->cols == 0) return QTA_OK;
-    if (!sum_out) return QTA_ERR_INVALID_ARG;
-    if (!aligned(sum_out, 16)) return QTA_ERR_ALIGNMENT;
+    *empty = (row_end == row_begin || d->cols == 0);
+    if (*empty) return QTA_OK;
     for (int r = 0; r < n_ranks; ++r)
         if ((st = check_qtensor(d, &shards[r])) != QTA_OK) return st;
-    if (!encoder_ready()) return QTA_ERR_CUDA;
-    int sms = 0, smem_sm = 0;
-    unsigned int* err = nullptr;
-    if (device_info(&sms, &smem_sm, &err) != cudaSuccess) return QTA_ERR_CUDA;
+    return QTA_OK;
+}
 
+static qta_status reduce_fill(const qta_desc* d, const qta_qtensor* shards, int32_t n_ranks, int64_t row_begin,
+                              int64_t row_end, ReduceParams* p, int* sms, int* smem_sm)
+{
+    if (!encoder_ready()) return QTA_ERR_CUDA;
+    unsigned int* err = nullptr;
+    if (device_info(sms, smem_sm, &err) != cudaSuccess) return QTA_ERR_CUDA;
     const int64_t segs = n_elems(d) / 64;
     const int64_t per_row = d->cols / 64;
-    ReduceParams p;
-    std::memset(&p, 0, sizeof(p));
+    std::memset(p, 0, sizeof(*p));
     for (int r = 0; r < n_ranks; ++r) {
-        if (!map_codes(&p.in_map[r], d->scheme, shards[r].codes, segs)) return QTA_ERR_CUDA;
-        p.scales[r] = shards[r].scales;
-        p.zeros[r] = shards[r].zeros;
-        p.state[r] = shards[r].state;
+        if (!map_codes(&p->in_map[r], d->scheme, shards[r].codes, segs)) return QTA_ERR_CUDA;
+        p->scales[r] = shards[r].scales;
+        p->zeros[r] = shards[r].zeros;
+        p->state[r] = shards[r].state;
     }
     const int64_t m_out = (row_end - row_begin) * per_row;
-    if (!map_f32(&p.out_map, sum_out, m_out)) return QTA_ERR_CUDA;
-    p.err = err;
-    p.n_ranks = n_ranks;
-    p.seg_begin = static_cast<int>(row_begin * per_row);
-    p.M_out = static_cast<int>(m_out);
-    p.n_warp_tiles = static_cast<int>((m_out + 31) / 32);
-    p.lanes_per_block = lanes_of(d);
-    p.lanes_log2 = log2i(p.lanes_per_block);
-    p.inv_block = 1.0f / static_cast<float>(d->block);
-    const int grid = grid_for(p.n_warp_tiles, reduce_warps(), reduce_smem(d->scheme), sms, smem_sm);
+    p->err = err;
+    p->n_ranks = n_ranks;
+    p->seg_begin = static_cast<int>(row_begin * per_row);
+    p->M_out = static_cast<int>(m_out);
+    p->n_warp_tiles = static_cast<int>((m_out + 31) / 32);
+    p->lanes_per_block = lanes_of(d);
+    p->lanes_log2 = log2i(p->lanes_per_block);
+    p->inv_block = 1.0f / static_cast<float>(d->block);
+    return QTA_OK;
+}
+
+qta_status qar_reduce_requant(const qta_desc* d, const qta_qtensor* shards, int32_t n_ranks, int64_t row_begin,
+                              int64_t row_end, const qta_desc* od, const qta_qtensor* out, int32_t mode,
+                              qta_stream_t stream)
+{
+    ReduceParams p;
+    int sms = 0, smem_sm = 0;
+    bool empty = false;
+    qta_status st = reduce_params(d, shards, n_ranks, row_begin, row_end, &p, &sms, &smem_sm, &empty);
+    if (st != QTA_OK) return st;
+    if ((st = check_desc(od)) != QTA_OK) return st;
+    if (od->cols != d->cols || od->batch * od->rows != row_end - row_begin) return QTA_ERR_INVALID_ARG;
+    if (od->scheme == QTA_TACO_FP8 && mode != QTA_SCALE_DELAYED && mode != QTA_SCALE_CURRENT)
+        return QTA_ERR_INVALID_ARG;
+    if (!reduce_requant_supported(d->scheme, od->scheme)) return QTA_ERR_UNSUPPORTED;
+    if (empty) return QTA_OK;
+    if ((st = check_qtensor(od, out)) != QTA_OK) return st;
+    if ((st = reduce_fill(d, shards, n_ranks, row_begin, row_end, &p, &sms, &smem_sm)) != QTA_OK) return st;
+    if (!map_codes(&p.out_map, od->scheme, out->codes, static_cast<uint64_t>(p.M_out))) return QTA_ERR_CUDA;
+    p.q_scales = out->scales;
+    p.q_zeros = out->zeros;
+    p.q_state = out->state;
+    p.q_lanes_per_block = lanes_of(od);
+    p.q_lanes_log2 = log2i(p.q_lanes_per_block);
+    p.q_seg_per_tensor = make_fastdiv(static_cast<uint32_t>(od->rows * od->cols / 64));
+    const int grid = grid_for(p.n_warp_tiles, reduce_warps(), reduce_smem(d->scheme, od->scheme), sms, smem_sm);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (od->scheme == QTA_TACO_FP8 && mode == QTA_SCALE_CURRENT) {
+        cudaError_t e = launch_state(out->state, od->batch, STATE_RESET_AMAX, s);
+        if (e == cudaSuccess) e = launch_reduce_requant(d->scheme, od->scheme, true, p, grid, s);
+        if (e == cudaSuccess) e = launch_state(out->state, od->batch, STATE_SET_SCALE, s);
+        if (e != cudaSuccess) return QTA_ERR_CUDA;
+    }
+    return cuda_status(launch_reduce_requant(d->scheme, od->scheme, false, p, grid, s));
+}
+
+qta_status qar_reduce(const qta_desc* d, const qta_qtensor* shards, int32_t n_ranks, int64_t row_begin,
+                      int64_t row_end, float* sum_out, qta_stream_t stream)
+{
+    ReduceParams p;
+    int sms = 0, smem_sm = 0;
+    bool empty = false;
+    qta_status st = reduce_params(d, shards, n_ranks, row_begin, row_end, &p, &sms, &smem_sm, &empty);
+    if (st != QTA_OK || empty) return st;
+    if (!sum_out) return QTA_ERR_INVALID_ARG;
+    if (!aligned(sum_out, 16)) return QTA_ERR_ALIGNMENT;
+    if ((st = reduce_fill(d, shards, n_ranks, row_begin, row_end, &p, &sms, &smem_sm)) != QTA_OK) return st;
+    if (!map_f32(&p.out_map, sum_out, static_cast<uint64_t>(p.M_out))) return QTA_ERR_CUDA;
+    const int grid = grid_for(p.n_warp_tiles, reduce_warps(), reduce_smem(d->scheme, OUT_F32), sms, smem_sm);
     return cuda_status(launch_reduce(d->scheme, p, grid, reinterpret_cast<cudaStream_t>(stream)));
 }
 

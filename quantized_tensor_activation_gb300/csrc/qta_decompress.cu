@@ -1,5 +1,4 @@
-// qta_decompress.cu -- instantiations and launchers of the decompress and
-// dequantize-reduce kernels.
+// qta_decompress.cu -- instantiations and launcher of the decompress kernels.
 #include "qta_launch.h"
 
 namespace qta {
@@ -8,7 +7,6 @@ int decompress_warps(int out_kind)
 {
     return out_kind == IN_FP32 ? DecompressCfg<S_TACO, IN_FP32>::WARPS : DecompressCfg<S_TACO, IN_BF16>::WARPS;
 }
-int reduce_warps() { return ReduceCfg<S_TACO>::WARPS; }
 
 int decompress_smem(int scheme, int out_kind)
 {
@@ -18,7 +16,6 @@ int decompress_smem(int scheme, int out_kind)
     return a4 ? DecompressCfg<S_ASYM4, IN_BF16>::SMEM : DecompressCfg<S_TACO, IN_BF16>::SMEM;
 }
 
-int reduce_smem(int scheme) { return scheme == S_ASYM4 ? ReduceCfg<S_ASYM4>::SMEM : ReduceCfg<S_TACO>::SMEM; }
 
 template <int SCH, int OUT>
 static cudaError_t launch_d(const DecompressParams& p, int grid, cudaStream_t stream)
@@ -50,29 +47,6 @@ cudaError_t launch_decompress(int scheme, int out_kind, const DecompressParams& 
     case S_INT8SYM: return launch_d_out<S_INT8SYM>(out_kind, p, grid, stream);
     case S_ASYM4: return launch_d_out<S_ASYM4>(out_kind, p, grid, stream);
     case S_ASYM8: return launch_d_out<S_ASYM8>(out_kind, p, grid, stream);
-    default: return cudaErrorInvalidValue;
-    }
-}
-
-template <int SCH>
-static cudaError_t launch_r(const ReduceParams& p, int grid, cudaStream_t stream)
-{
-    using C = ReduceCfg<SCH>;
-    static std::atomic<unsigned> done{0};
-    auto fn = reduce_kernel<SCH>;
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(fn), C::SMEM, &done);
-    if (e != cudaSuccess) return e;
-    fn<<<grid, C::WARPS * 32, C::SMEM, stream>>>(p);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_reduce(int scheme, const ReduceParams& p, int grid, cudaStream_t stream)
-{
-    switch (scheme) {
-    case S_TACO: return launch_r<S_TACO>(p, grid, stream);
-    case S_INT8SYM: return launch_r<S_INT8SYM>(p, grid, stream);
-    case S_ASYM4: return launch_r<S_ASYM4>(p, grid, stream);
-    case S_ASYM8: return launch_r<S_ASYM8>(p, grid, stream);
     default: return cudaErrorInvalidValue;
     }
 }

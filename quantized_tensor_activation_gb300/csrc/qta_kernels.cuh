@@ -59,7 +59,7 @@ struct DecompressParams {
 
 struct ReduceParams {
     CUtensorMap in_map[MAX_RANKS];  // codes of each shard
-    CUtensorMap out_map;            // fp32 {32,2,M_out}
+    CUtensorMap out_map;            // fp32 sum {32,2,M_out}, or the requantized codes
     const void* scales[MAX_RANKS];
     const void* zeros[MAX_RANKS];
     const float* state[MAX_RANKS];
@@ -68,9 +68,16 @@ struct ReduceParams {
     int seg_begin;                  // first input segment (row_begin * cols / 64)
     int M_out;                      // output segments
     int n_warp_tiles;
-    int lanes_per_block;
+    int lanes_per_block;            // of the shards' blocks
     int lanes_log2;
     float inv_block;
+    // requantization of the sum (fused reduce + requant only)
+    void* q_scales;
+    void* q_zeros;
+    float* q_state;
+    int q_lanes_per_block;
+    int q_lanes_log2;
+    FastDiv q_seg_per_tensor;
 };
 
 // ------------------------------------------------------------ configuration
@@ -103,12 +110,16 @@ struct DecompressCfg {
     static constexpr int SMEM = WARPS * WARP_SMEM + WARPS * STAGES * 8 + 1024;
 };
 
-template <int SCH>
+// OSCH: OUT_F32 for the FP32 sum (qar_reduce), else the requantization scheme
+// of the fused reduce + requant.
+constexpr int OUT_F32 = -1;
+
+template <int SCH, int OSCH = OUT_F32>
 struct ReduceCfg {
     static constexpr int WARPS = 12;
     static constexpr int IN_SEG = (SCH == S_ASYM4) ? 32 : 64;
-    static constexpr int OUT_SEG = 256;
-    static constexpr int STAGES = (SCH == S_ASYM4) ? 8 : 4;
+    static constexpr int OUT_SEG = (OSCH == OUT_F32) ? 256 : (OSCH == S_ASYM4) ? 32 : 64;
+    static constexpr int STAGES = (OSCH == OUT_F32) ? ((SCH == S_ASYM4) ? 8 : 4) : ((SCH == S_ASYM4) ? 16 : 8);
     static constexpr int IN_BYTES = 32 * IN_SEG;
     static constexpr int OUT_BYTES = 32 * OUT_SEG;
     static constexpr int OUT_BUFS = 1;
@@ -314,90 +325,57 @@ __device__ __forceinline__ void drain_ring(uint64_t* bars, int stages, int stage
     }
 }
 
-// ------------------------------------------------------------ compress
-// taco_compress / qar_requant / CURRENT-mode amax pre-pass (AMAX_ONLY).
-template <int IN, int SCH, bool AMAX_ONLY>
-__global__ void __launch_bounds__(CompressCfg<IN, SCH>::WARPS * 32, 1)
-compress_kernel(const __grid_constant__ CompressParams p)
-{
-    using C = CompressCfg<IN, SCH>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = aligned_smem(smem_raw);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint8_t* wb = smem + warp * C::WARP_SMEM;
-    uint8_t* outb = wb + C::STAGES * C::IN_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::WARPS * C::WARP_SMEM) + warp * C::STAGES;
+// ------------------------------------------------------------ quantizer
+// Output side of a quantization: where the per-block metadata goes.
+struct QuantOut {
+    void* scales;
+    void* zeros;
+    float* state;
+    int M;                  // segments of the quantized tensor (all batches)
+    int lanes_per_block;
+    int lanes_log2;
+    FastDiv seg_per_tensor;
+};
 
-    const int W = gridDim.x * C::WARPS;
-    const int first = blockIdx.x * C::WARPS + warp;
-    if (lane == 0) {
-        for (int s = 0; s < C::STAGES; ++s) mbar_init(&bars[s], 1);
-        fence_barrier_init();
-        for (int s = 0; s < C::STAGES; ++s) {
-            const int wt = first + s * W;
-            if (wt >= p.n_warp_tiles) break;
-            issue_in16or32<IN>(&p.in_map, wb + s * C::IN_BYTES, wt * 32, &bars[s]);
-        }
-    }
-    __syncwarp();
-
+// Quantizes one warp tile (one 64-element segment per lane, values in the
+// original domain) into code words `ow`, writes the per-block metadata and
+// accumulates the per-tensor amax (TACO).  Carries the per-warp scale cache
+// and amax tracker across tiles.
+template <int SCH>
+struct Quantizer {
     AmaxTracker amax;
     int cached_tensor = -1;
     float S = 1.0f, tinv = 0.0f;
-    const int L = p.lanes_per_block;
-    int stage = 0;
-    uint32_t phase = 0;
-    int k = 0;
-    bool aborted = false;
 
-    for (int wt = first; wt < p.n_warp_tiles; wt += W, ++k) {
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[stage], phase, p.err));
-        if (!ok) {
-            aborted = true;
-            break;
-        }
-        u64 v[32];
-        load_segment<IN>(wb + stage * C::IN_BYTES, lane, v);
-        __syncwarp();
-        {   // refill this stage with the tile STAGES ahead
-            const int nwt = wt + C::STAGES * W;
-            if (nwt < p.n_warp_tiles && lane == 0) {
-                fence_proxy_async_smem();
-                issue_in16or32<IN>(&p.in_map, wb + stage * C::IN_BYTES, nwt * 32, &bars[stage]);
-            }
-        }
-        if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
-        }
-
-        const int g = wt * 32 + lane;     // global segment of this lane
-        const bool valid = g < p.M;
-
-        uint32_t ow[16];                  // output code words of this lane
+    // AMAX_ONLY: transform and record the amax, write nothing else.
+    template <bool AMAX_ONLY>
+    __device__ __forceinline__ void run(u64 (&v)[32], const QuantOut& o, int tile_first, int lane,
+                                        uint32_t (&ow)[16])
+    {
+        const int g = tile_first + lane;
+        const bool valid = g < o.M;
+        const int L = o.lanes_per_block;
         if constexpr (SCH == S_TACO) {
-            const int g_last = min(wt * 32 + 31, p.M - 1);
-            const int t_first = (int)fdiv((uint32_t)(wt * 32), p.seg_per_tensor);
-            const int t_last = (int)fdiv((uint32_t)g_last, p.seg_per_tensor);
+            const int g_last = min(tile_first + 31, o.M - 1);
+            const int t_first = (int)fdiv((uint32_t)tile_first, o.seg_per_tensor);
+            const int t_last = (int)fdiv((uint32_t)g_last, o.seg_per_tensor);
             const bool uniform = (t_first == t_last);
-            const int tens = uniform ? t_first : (int)fdiv((uint32_t)min(g, p.M - 1), p.seg_per_tensor);
+            const int tens = uniform ? t_first : (int)fdiv((uint32_t)min(g, o.M - 1), o.seg_per_tensor);
             fwht64_local(v);
             fwht_cross(v, L, lane);
             const float a = absmax64(v);
             if (uniform) {
                 if (tens != amax.tensor) {
-                    amax.flush(p.state, lane);
+                    amax.flush(o.state, lane);
                     amax.tensor = tens;
                 }
                 amax.m = fmaxf(amax.m, a);
             } else if (valid && a > 0.0f) {
-                atomicMax(reinterpret_cast<unsigned int*>(p.state + 2 * tens + 1), __float_as_uint(a));
+                atomicMax(reinterpret_cast<unsigned int*>(o.state + 2 * tens + 1), __float_as_uint(a));
             }
-            if constexpr (AMAX_ONLY) {
-                continue;
-            } else {
+            if constexpr (!AMAX_ONLY) {
                 if (!uniform || tens != cached_tensor) {
-                    S = __ldg(p.state + 2 * tens);
+                    S = __ldg(o.state + 2 * tens);
                     tinv = __frcp_rn(__fmul_rn(448.0f, S));
                     cached_tensor = uniform ? tens : -1;
                 }
@@ -414,7 +392,7 @@ compress_kernel(const __grid_constant__ CompressParams p)
                     ow[w] = join16(e4m3x2_encode(q0.x, q0.y), e4m3x2_encode(q1.x, q1.y));
                 }
                 if (valid && (lane & (L - 1)) == 0)
-                    static_cast<uint8_t*>(p.scales)[g >> p.lanes_log2] = static_cast<uint8_t>(r);
+                    static_cast<uint8_t*>(o.scales)[g >> o.lanes_log2] = static_cast<uint8_t>(r);
             }
         } else if constexpr (SCH == S_INT8SYM) {
             const float a = absmax64(v);
@@ -433,7 +411,7 @@ compress_kernel(const __grid_constant__ CompressParams p)
                 const u64 r1 = rint_bits2(pk2(fmaxf(y1.x, -127.0f), fmaxf(y1.y, -127.0f)));
                 ow[w] = bytes4(lo32(r0), hi32(r0), lo32(r1), hi32(r1));
             }
-            if (valid) static_cast<float*>(p.scales)[g] = s;
+            if (valid) static_cast<float*>(o.scales)[g] = s;
         } else {
             constexpr float Q = (SCH == S_ASYM4) ? 15.0f : 255.0f;
             float mn = up2(v[0]).x, mx = mn;
@@ -473,39 +451,108 @@ compress_kernel(const __grid_constant__ CompressParams p)
                 for (int w = 0; w < 16; ++w) ow[w] = bytes4(rb[4 * w], rb[4 * w + 1], rb[4 * w + 2], rb[4 * w + 3]);
             }
             if (valid && (lane & 1) == 0) {
-                static_cast<__half*>(p.scales)[g >> 1] = s16;
-                static_cast<__half*>(p.zeros)[g >> 1] = z16;
-            }
-        }
-
-        if constexpr (!AMAX_ONLY) {
-            // stage the codes and store them with one TMA per warp tile
-            uint8_t* ob = outb + (k % C::OUT_BUFS) * C::OUT_BYTES;
-            if (lane == 0) {
-                if constexpr (C::OUT_BUFS == 1)
-                    bulk_wait_read<0>();
-                else
-                    bulk_wait_read<1>();
-            }
-            __syncwarp();
-            if constexpr (SCH == S_ASYM4) {
-#pragma unroll
-                for (int c = 0; c < 2; ++c)
-                    sts128(ob, sw32(lane, c), make_uint4(ow[4 * c], ow[4 * c + 1], ow[4 * c + 2], ow[4 * c + 3]));
-            } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    sts128(ob, sw64(lane, c), make_uint4(ow[4 * c], ow[4 * c + 1], ow[4 * c + 2], ow[4 * c + 3]));
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                tma_store_2d(&p.out_map, 0, wt * 32, ob);
-                bulk_commit();
+                static_cast<__half*>(o.scales)[g >> 1] = s16;
+                static_cast<__half*>(o.zeros)[g >> 1] = z16;
             }
         }
     }
-    if constexpr (SCH == S_TACO) amax.flush(p.state, lane);
+
+    __device__ __forceinline__ void finish(const QuantOut& o, int lane)
+    {
+        if constexpr (SCH == S_TACO) amax.flush(o.state, lane);
+    }
+};
+
+// Stage one warp tile of code words in shared memory and store it with one
+// TMA tensor store (8-bit codes: 64 B rows, SW64; 4-bit: 32 B rows, SW32).
+template <int SCH, int OUT_BUFS>
+__device__ __forceinline__ void store_codes(uint8_t* ob, const CUtensorMap* map, int row, int lane,
+                                            const uint32_t (&ow)[16])
+{
+    if (lane == 0) {
+        if constexpr (OUT_BUFS == 1)
+            bulk_wait_read<0>();
+        else
+            bulk_wait_read<1>();
+    }
+    __syncwarp();
+    if constexpr (SCH == S_ASYM4) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+            sts128(ob, sw32(lane, c), make_uint4(ow[4 * c], ow[4 * c + 1], ow[4 * c + 2], ow[4 * c + 3]));
+    } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            sts128(ob, sw64(lane, c), make_uint4(ow[4 * c], ow[4 * c + 1], ow[4 * c + 2], ow[4 * c + 3]));
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(map, 0, row, ob);
+        bulk_commit();
+    }
+}
+
+// ------------------------------------------------------------ compress
+// taco_compress / qar_requant / CURRENT-mode amax pre-pass (AMAX_ONLY).
+template <int IN, int SCH, bool AMAX_ONLY>
+__global__ void __launch_bounds__(CompressCfg<IN, SCH>::WARPS * 32, 1)
+compress_kernel(const __grid_constant__ CompressParams p)
+{
+    using C = CompressCfg<IN, SCH>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = aligned_smem(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t* wb = smem + warp * C::WARP_SMEM;
+    uint8_t* outb = wb + C::STAGES * C::IN_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::WARPS * C::WARP_SMEM) + warp * C::STAGES;
+
+    const int W = gridDim.x * C::WARPS;
+    const int first = blockIdx.x * C::WARPS + warp;
+    if (lane == 0) {
+        for (int s = 0; s < C::STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_barrier_init();
+        for (int s = 0; s < C::STAGES; ++s) {
+            const int wt = first + s * W;
+            if (wt >= p.n_warp_tiles) break;
+            issue_in16or32<IN>(&p.in_map, wb + s * C::IN_BYTES, wt * 32, &bars[s]);
+        }
+    }
+    __syncwarp();
+
+    const QuantOut qo{p.scales, p.zeros, p.state, p.M, p.lanes_per_block, p.lanes_log2, p.seg_per_tensor};
+    Quantizer<SCH> quant;
+    int stage = 0;
+    uint32_t phase = 0;
+    int k = 0;
+    bool aborted = false;
+
+    for (int wt = first; wt < p.n_warp_tiles; wt += W, ++k) {
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[stage], phase, p.err));
+        if (!ok) {
+            aborted = true;
+            break;
+        }
+        u64 v[32];
+        load_segment<IN>(wb + stage * C::IN_BYTES, lane, v);
+        __syncwarp();
+        {   // refill this stage with the tile STAGES ahead
+            const int nwt = wt + C::STAGES * W;
+            if (nwt < p.n_warp_tiles && lane == 0) {
+                fence_proxy_async_smem();
+                issue_in16or32<IN>(&p.in_map, wb + stage * C::IN_BYTES, nwt * 32, &bars[stage]);
+            }
+        }
+        if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+        }
+        uint32_t ow[16];
+        quant.template run<AMAX_ONLY>(v, qo, wt * 32, lane, ow);
+        if constexpr (!AMAX_ONLY)
+            store_codes<SCH, C::OUT_BUFS>(outb + (k % C::OUT_BUFS) * C::OUT_BYTES, &p.out_map, wt * 32, lane, ow);
+    }
+    quant.finish(qo, lane);
     if (lane == 0) {
         bulk_wait_all();
         if (aborted) drain_ring(bars, C::STAGES, stage, phase, p.err);
@@ -642,11 +689,11 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
 
 // ------------------------------------------------------------ reduce
 // Units of the stage ring are (warp tile, rank) pairs, rank fastest.
-template <int SCH>
+template <int SCH, int OSCH>
 __device__ __forceinline__ void reduce_issue(const ReduceParams& p, uint8_t* wb, uint64_t* bars,
                                              int stage, int unit, int first, int W)
 {
-    using C = ReduceCfg<SCH>;
+    using C = ReduceCfg<SCH, OSCH>;
     const int t = unit / p.n_ranks, r = unit - t * p.n_ranks;
     const int wt = first + t * W;
     mbar_arrive_expect_tx(&bars[stage], C::IN_BYTES);
@@ -685,11 +732,16 @@ __device__ __forceinline__ void reduce_meta_load(const ReduceParams& p, int t, i
     }
 }
 
-template <int SCH>
-__global__ void __launch_bounds__(ReduceCfg<SCH>::WARPS * 32, 1)
+// qar_reduce (OSCH = OUT_F32) and the fused qar_reduce_requant (OSCH = the
+// requantization scheme; AMAX_ONLY = its CURRENT-mode pre-pass).  The sum of
+// a warp tile is formed exactly as qar_reduce forms it and then quantized
+// exactly as qar_requant quantizes an FP32 input, so the fused result is
+// bit-identical to the two calls.
+template <int SCH, int OSCH, bool AMAX_ONLY>
+__global__ void __launch_bounds__(ReduceCfg<SCH, OSCH>::WARPS * 32, 1)
 reduce_kernel(const __grid_constant__ ReduceParams p)
 {
-    using C = ReduceCfg<SCH>;
+    using C = ReduceCfg<SCH, OSCH>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = aligned_smem(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -704,7 +756,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
     if (lane == 0) {
         for (int s = 0; s < C::STAGES; ++s) mbar_init(&bars[s], 1);
         fence_barrier_init();
-        for (int u = 0; u < C::STAGES && u < total_units; ++u) reduce_issue<SCH>(p, wb, bars, u, u, first, W);
+        for (int u = 0; u < C::STAGES && u < total_units; ++u) reduce_issue<SCH, OSCH>(p, wb, bars, u, u, first, W);
     }
     __syncwarp();
     const int L = p.lanes_per_block;
@@ -713,6 +765,9 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
     uint32_t phase = 0;
     int unit = 0;
     bool aborted = false;
+    const QuantOut qo{p.q_scales, p.q_zeros, p.q_state, p.M_out, p.q_lanes_per_block, p.q_lanes_log2,
+                      p.q_seg_per_tensor};
+    Quantizer<(OSCH == OUT_F32) ? S_TACO : OSCH> quant;
     SegMeta<SCH> nxt[RANK_CHUNK];
     if (my_tiles > 0) reduce_meta_load<SCH>(p, 0, 0, first, W, lane, nxt);
     for (int t = 0; t < my_tiles && !aborted; ++t) {
@@ -744,7 +799,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                 __syncwarp();
                 if (lane == 0 && unit + C::STAGES < total_units) {
                     fence_proxy_async_smem();
-                    reduce_issue<SCH>(p, wb, bars, stage, unit + C::STAGES, first, W);
+                    reduce_issue<SCH, OSCH>(p, wb, bars, stage, unit + C::STAGES, first, W);
                 }
                 ++unit;
                 if (++stage == C::STAGES) {
@@ -757,20 +812,37 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
         if constexpr (SCH == S_TACO) {
             fwht64_local(acc);
             fwht_cross(acc, L, lane);
-            const u64 ib = pk2(p.inv_block, p.inv_block);
+            if constexpr (OSCH == OUT_F32) {
+                const u64 ib = pk2(p.inv_block, p.inv_block);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc[j] = mul2(acc[j], ib);
+                for (int j = 0; j < 32; ++j) acc[j] = mul2(acc[j], ib);
+            } else {
+                // scalar rounded multiplies: the requantizer's butterfly adds
+                // follow, and a packed multiply would be contracted into them
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float2 t2 = up2(acc[j]);
+                    acc[j] = pk2(__fmul_rn(t2.x, p.inv_block), __fmul_rn(t2.y, p.inv_block));
+                }
+            }
         }
-        if (lane == 0) bulk_wait_read<0>();
-        __syncwarp();
-        store_segment<IN_FP32>(outb, lane, acc);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            store_out16or32<IN_FP32>(&p.out_map, outb, wt * 32);
-            bulk_commit();
+        if constexpr (OSCH == OUT_F32) {
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+            store_segment<IN_FP32>(outb, lane, acc);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                store_out16or32<IN_FP32>(&p.out_map, outb, wt * 32);
+                bulk_commit();
+            }
+        } else {
+            uint32_t ow[16];
+            quant.template run<AMAX_ONLY>(acc, qo, wt * 32, lane, ow);
+            if constexpr (!AMAX_ONLY) store_codes<OSCH, 1>(outb, &p.out_map, wt * 32, lane, ow);
         }
     }
+    if constexpr (OSCH != OUT_F32) quant.finish(qo, lane);
     if (lane == 0) {
         bulk_wait_all();
         if (aborted) drain_ring(bars, C::STAGES, stage, phase, p.err);

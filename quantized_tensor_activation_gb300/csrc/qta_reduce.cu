@@ -1,0 +1,60 @@
+// qta_reduce.cu -- instantiations and launchers of the dequantize-reduce
+// kernels: qar_reduce (FP32 sum) and the fused qar_reduce_requant.
+#include "qta_launch.h"
+
+namespace qta {
+
+int reduce_warps() { return ReduceCfg<S_TACO>::WARPS; }
+
+int reduce_smem(int scheme, int out_scheme)
+{
+    if (out_scheme == OUT_F32) return scheme == S_ASYM4 ? ReduceCfg<S_ASYM4>::SMEM : ReduceCfg<S_TACO>::SMEM;
+    switch (scheme * 4 + out_scheme) {
+    case S_TACO * 4 + S_TACO: return ReduceCfg<S_TACO, S_TACO>::SMEM;
+    case S_INT8SYM * 4 + S_INT8SYM: return ReduceCfg<S_INT8SYM, S_INT8SYM>::SMEM;
+    case S_ASYM4 * 4 + S_ASYM8: return ReduceCfg<S_ASYM4, S_ASYM8>::SMEM;
+    case S_ASYM8 * 4 + S_ASYM8: return ReduceCfg<S_ASYM8, S_ASYM8>::SMEM;
+    default: return 0;
+    }
+}
+
+bool reduce_requant_supported(int scheme, int out_scheme) { return reduce_smem(scheme, out_scheme) > 0 && out_scheme != OUT_F32; }
+
+template <int SCH, int OSCH, bool AMAX>
+static cudaError_t launch_r(const ReduceParams& p, int grid, cudaStream_t stream)
+{
+    using C = ReduceCfg<SCH, OSCH>;
+    static std::atomic<unsigned> done{0};
+    auto fn = reduce_kernel<SCH, OSCH, AMAX>;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(fn), C::SMEM, &done);
+    if (e != cudaSuccess) return e;
+    fn<<<grid, C::WARPS * 32, C::SMEM, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_reduce(int scheme, const ReduceParams& p, int grid, cudaStream_t stream)
+{
+    switch (scheme) {
+    case S_TACO: return launch_r<S_TACO, OUT_F32, false>(p, grid, stream);
+    case S_INT8SYM: return launch_r<S_INT8SYM, OUT_F32, false>(p, grid, stream);
+    case S_ASYM4: return launch_r<S_ASYM4, OUT_F32, false>(p, grid, stream);
+    case S_ASYM8: return launch_r<S_ASYM8, OUT_F32, false>(p, grid, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_reduce_requant(int scheme, int out_scheme, bool amax_only, const ReduceParams& p, int grid,
+                                  cudaStream_t stream)
+{
+    switch (scheme * 4 + out_scheme) {
+    case S_TACO * 4 + S_TACO:
+        return amax_only ? launch_r<S_TACO, S_TACO, true>(p, grid, stream)
+                         : launch_r<S_TACO, S_TACO, false>(p, grid, stream);
+    case S_INT8SYM * 4 + S_INT8SYM: return launch_r<S_INT8SYM, S_INT8SYM, false>(p, grid, stream);
+    case S_ASYM4 * 4 + S_ASYM8: return launch_r<S_ASYM4, S_ASYM8, false>(p, grid, stream);
+    case S_ASYM8 * 4 + S_ASYM8: return launch_r<S_ASYM8, S_ASYM8, false>(p, grid, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace qta

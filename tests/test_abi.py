@@ -107,3 +107,22 @@ def test_argument_checks(L):
     assert L.qta_copy(16, 32, 0, None) == OK
     assert L.qta_device_error(None, 0) == INV
     assert L.qta_status_string(qta.QTA_ERR_ALIGNMENT) == b"QTA_ERR_ALIGNMENT"
+
+
+def test_reduce_requant_argument_checks(L):
+    D = lambda *a: ctypes.byref(qta.desc(*a))
+    OK, INV, ALN, UNS = qta.QTA_OK, qta.QTA_ERR_INVALID_ARG, qta.QTA_ERR_ALIGNMENT, qta.QTA_ERR_UNSUPPORTED
+    arr = (qta.QTensorC * 2)(qta.QTensorC(16, 16, 16, 16), qta.QTensorC(16, 16, 16, 16))
+    out = ctypes.byref(qta.QTensorC(16, 16, 16, 16))
+    f = L.qar_reduce_requant
+    assert f(D(0, 128, 8, 256), arr, 2, 0, 8, D(1, 64, 8, 256), out, 0, None) == UNS     # TACO -> INT8
+    assert f(D(2, 128, 8, 256), arr, 2, 0, 8, D(0, 128, 8, 256), out, 0, None) == UNS
+    assert f(D(0, 128, 8, 256), arr, 2, 0, 8, D(0, 128, 3, 256, 2), out, 0, None) == INV  # 2*3 != 8 rows
+    assert f(D(0, 128, 8, 256), arr, 2, 0, 8, D(0, 128, 8, 512), out, 0, None) == INV    # cols differ
+    assert f(D(0, 128, 8, 256), arr, 2, 0, 8, D(0, 128, 4, 256, 2), out, 7, None) == INV  # mode
+    assert f(D(0, 128, 8, 256), arr, 2, 4, 4, D(0, 128, 0, 256, 1), out, 0, None) == OK   # empty range
+    assert f(D(0, 128, 8, 256), arr, 2, 0, 8, D(0, 128, 4, 256, 2),
+             ctypes.byref(qta.QTensorC(24, 16, 16, 16)), 0, None) == ALN
+    assert f(D(0, 128, 8, 256), arr, 17, 0, 8, D(0, 128, 8, 256), out, 0, None) == UNS
+    assert f(D(2, 128, 8, 256), arr, 2, 0, 8, D(3, 128, 8, 256),
+             ctypes.byref(qta.QTensorC(16, 16, None, 16)), 0, None) == INV                # zeros needed

@@ -264,3 +264,50 @@ def test_copy_kernel(dev):
     qta.qta_copy(src, dst, n)
     torch.cuda.synchronize()
     assert torch.equal(src, dst)
+
+
+@pytest.mark.parametrize("scheme,B,gscheme,gB", [(qta.TACO_FP8, 128, qta.TACO_FP8, 128),
+                                                 (qta.TACO_FP8, 256, qta.TACO_FP8, 128),
+                                                 (qta.TACO_FP8, 64, qta.TACO_FP8, 256),
+                                                 (qta.INT8_SYM_B64, 64, qta.INT8_SYM_B64, 64),
+                                                 (qta.INT4_ASYM_G128, 128, qta.INT8_ASYM_G128, 128),
+                                                 (qta.INT8_ASYM_G128, 128, qta.INT8_ASYM_G128, 128)])
+@pytest.mark.parametrize("n", [1, 3, 8])
+@pytest.mark.parametrize("mode", [qta.SCALE_CURRENT, qta.SCALE_DELAYED])
+def test_reduce_requant_fused(dev, scheme, B, gscheme, gB, n, mode):
+    # the fused call equals qar_reduce followed by qar_requant, computed by
+    # the oracle (reduce, then compress of the FP32 sum), bit for bit
+    rows, cols = 96, 1024
+    rng = np.random.default_rng(hash((scheme, B, gscheme, n, mode)) % 2 ** 32)
+    shards = _oracle_shards(scheme, B, n, rows, cols, rng)
+    d, ds = _to_dev(scheme, B, rows, cols, shards, dev)
+    for rb, re_, nb in ((0, rows, 4), (8, 56, 3), (95, 96, 1)):
+        gr = (re_ - rb) // nb
+        dg = qta.desc(gscheme, gB, gr, cols, batch=nb)
+        g = qta.alloc_qtensor(dg, dev)
+        st0 = None
+        if g.state is not None:
+            st0 = np.zeros(2 * nb, dtype=np.float32)
+            st0[0::2] = [0.003 * (j + 1) for j in range(nb)]
+            st0[1::2] = [0.5 * j for j in range(nb)]
+            g.state.copy_(torch.from_numpy(st0))
+        qta.qar_reduce_requant(d, ds, rb, re_, dg, g, mode)
+        osum = orc.reduce(ORC_SCH[scheme], B, shards, rows, cols, rb, re_)
+        ref = oracle_compress(gscheme, gB, torch.from_numpy(osum), qta.FP32, nb, gr, cols,
+                              orc.CURRENT if mode == qta.SCALE_CURRENT else orc.DELAYED, state=st0)
+        torch.cuda.synchronize()
+        compare_qtensor(f"fused rows {rb}:{re_}", g, ref)
+    assert qta.qta_device_error() == 0
+
+
+def test_reduce_requant_rejects_unsupported_pairs(dev):
+    d = qta.desc(qta.TACO_FP8, 128, 8, 256)
+    q = qta.alloc_qtensor(d, dev)
+    dg = qta.desc(qta.INT8_SYM_B64, 64, 8, 256)
+    g = qta.alloc_qtensor(dg, dev)
+    with pytest.raises(qta.QtaError) as e:
+        qta.qar_reduce_requant(d, [q], 0, 8, dg, g)
+    assert e.value.status == qta.QTA_ERR_UNSUPPORTED
+    with pytest.raises(qta.QtaError) as e:
+        qta.qar_reduce_requant(d, [q], 0, 8, qta.desc(qta.TACO_FP8, 128, 3, 256, batch=2), q)
+    assert e.value.status == qta.QTA_ERR_INVALID_ARG
