@@ -130,6 +130,24 @@ def _smi_gpu_id(torch, local: int) -> str:
         return str(local)
 
 
+def max_over_ranks(value: float, device="cpu") -> float:
+    """The largest value over all ranks of the process group (the value itself
+    without one): the job's step time is that of its slowest replica."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank_step: float, ms_step_max: float, world_size: int) -> float:
+    """Whole-job GB/s of 16-bit input: every replica processes its own batch
+    in the same (slowest-rank) step time."""
+    return bytes_per_rank_step * world_size / (ms_step_max * 1e-3) / 1e9
+
+
 def _cpu_oracle_path(w: workloads.Workload, rows: int, seed: int = 0):
     """The oracle's full path over a row sample of every rank; returns
     (seconds, 16-bit input bytes processed, threads used)."""
@@ -345,11 +363,7 @@ def run_qta(args, w):
     for e in evs:
         for j, k in enumerate(per):
             per[k].append(e[j].elapsed_time(e[j + 1]))
-    ms_step = total_ms / args.steps
-    if ws > 1:
-        t = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(total_ms / args.steps, dev)
     # the other path (two calls, FP32 sum through HBM), for comparison
     evs2, s2a, s2b, _ = timed(not fused)
     torch.cuda.synchronize()
@@ -398,7 +412,7 @@ def run_qta(args, w):
         return
 
     in_bytes = 2 * N * R * C
-    value = in_bytes / (ms_step * 1e-3) / 1e9 * ws
+    value = job_throughput(in_bytes, ms_step, ws)
     peak, peak_kind = _peaks()
     alg = algorithmic_bytes(w)
     names = {"K1": "taco_compress", "K2": "qar_reduce_requant" if fused else "qar_reduce",
