@@ -8,7 +8,9 @@ One step = one pass of the whole path over one batch of synthetic input:
      taco_update_scale (both stages' per-tensor scales, one launch)
 Metric: GB/s of 16-bit input processed (2 bytes x elements x ranks / step
 time), with the fraction of the measured HBM bandwidth reached by the
-dominant kernel (K1) reported in "roofline".
+dominant kernel (K1) reported in "roofline".  The timed steps replay the step
+captured once as a CUDA graph (--no-graph: eager launches); per-kernel times
+come from the same step launched eagerly with CUDA events between the calls.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl qta|reference]
 
@@ -339,6 +341,22 @@ def run_qta(args, w):
         t1.record(stream)
         return evs, t0, t1, launches[0]
 
+    # the step as a CUDA graph (kernel parameters, tensor maps included, are
+    # fixed at capture; every replay recomputes the whole step)
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step(fused=fused)
+        graph.replay()
+        torch.cuda.synchronize()
+
+    def run_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            step(fused=fused)
+
     # ---- timed region: inputs resident in HBM
     clocks = ClockSampler(None if args.no_clocks else _smi_gpu_id(torch, local))
     if ws > 1:
@@ -348,25 +366,35 @@ def run_qta(args, w):
     if not args.no_clocks:
         time.sleep(0.3)
     for _ in range(pad):
-        step(fused=fused)
+        run_step()
     if ws > 1:
         torch.cuda.synchronize()
         torch.distributed.barrier()
-    evs, t_start, t_end, n_launch = timed(fused)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        run_step()
+    t_end.record(stream)
+    n_launch = args.steps * ((3 if fused else 4) + int(n_state > 0))
     for _ in range(pad):
-        step(fused=fused)
+        run_step()
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
     if clk is not None:
         clk["window"] = f"sampled every 100 ms over {2 * pad + args.steps} back-to-back steps around and including the timed ones"
-    total_ms = t_start.elapsed_time(t_end)
+    ms_step = max_over_ranks(t_start.elapsed_time(t_end) / args.steps, dev)
+
+    # per-kernel times: the same step launched eagerly with events between the calls
+    evs, e0, e1, _ = timed(fused)
+    torch.cuda.synchronize()
+    eager_ms = e0.elapsed_time(e1) / args.steps
     per = {k: [] for k in ("K1", "K2", "K3", "K4", "U")}
     for e in evs:
         for j, k in enumerate(per):
             per[k].append(e[j].elapsed_time(e[j + 1]))
-    ms_step = max_over_ranks(total_ms / args.steps, dev)
     # the other path (two calls, FP32 sum through HBM), for comparison
     evs2, s2a, s2b, _ = timed(not fused)
     torch.cuda.synchronize()
@@ -451,6 +479,8 @@ def run_qta(args, w):
                      "frac": achieved / peak, "traffic": traffic, "kernel": "K1 taco_compress",
                      "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes": alg["K1"]},
         "path": "fused reduce+requant (qar_reduce_requant)" if fused else "qar_reduce + qar_requant",
+        "launch": "CUDA graph of one step, replayed" if graph is not None else "eager",
+        "eager_ms_per_step": eager_ms,
         "kernels": kern,
         "step_frac_of_hbm": step_bytes / (ms_step * 1e-3) / 1e9 / peak,
         "other_path": {"path": "qar_reduce + qar_requant" if fused else "qar_reduce_requant",
@@ -478,6 +508,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="skip the nvidia-smi clock window (profiling runs)")
+    ap.add_argument("--no-graph", action="store_true", help="launch the timed steps eagerly instead of as a CUDA graph")
     ap.add_argument("--path", default="fused", choices=["fused", "split"],
                     help="fused: qar_reduce_requant; split: qar_reduce then qar_requant (FP32 sum in HBM)")
     args = ap.parse_args(argv)
