@@ -407,10 +407,25 @@ def run_qta(args, w):
         xh = x.cpu().pin_memory()
         yh = torch.empty((R, C), dtype=tdt).pin_memory()
         xd = torch.empty_like(x)
+        # the per-rank inputs travel on several copy streams at once
+        copy_streams = [torch.cuda.Stream() for _ in range(min(4, N))]
+        done = [torch.cuda.Event() for _ in copy_streams]
         torch.cuda.synchronize()
 
+        def copy_in():
+            ready = torch.cuda.Event()
+            ready.record(stream)
+            for i, (cs, ev) in enumerate(zip(copy_streams, done)):
+                cs.wait_event(ready)
+                with torch.cuda.stream(cs):
+                    for r in range(i, N, len(copy_streams)):
+                        xd[r].copy_(xh[r], non_blocking=True)
+                    ev.record(cs)
+            for ev in done:
+                stream.wait_event(ev)
+
         def e2e_step():
-            xd.copy_(xh, non_blocking=True)
+            copy_in()
             qta.taco_compress(d_in, xd, in_dt, q, qta.SCALE_DELAYED)
             if fused:
                 qta.qar_reduce_requant(d_sh, shards, 0, R, d_g, g, qta.SCALE_DELAYED)
