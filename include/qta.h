@@ -162,20 +162,24 @@ qta_status qar_reduce(const qta_desc* d, const qta_qtensor* shards, int32_t n_ra
                       int64_t row_begin, int64_t row_end, float* sum_out,
                       qta_stream_t stream);
 
-/* qar_reduce_requant -- qar_reduce followed by qar_requant in one kernel: the
- * FP32 sum of rows [row_begin, row_end) is formed exactly as qar_reduce forms
- * it and quantized exactly as qar_requant quantizes an FP32 input, without
- * writing the sum to memory; codes, scales, zeros and state are bit-identical
- * to the two calls.  This is the receiving side of one step of the two-step
- * all-reduce [FLASH: local FP32 sum, then INT8 requantization before the
- * All-Gather; TACO Fig. 9: one fused operator instead of several kernels].
- * `d` and `shards` as for qar_reduce; `out_desc` describes the requantized
- * rows as out_desc->batch shards of out_desc->rows rows each
- * (batch * rows == row_end - row_begin, same cols), `out` its buffers, `mode`
- * its scale mode (QTA_TACO_FP8 output).  Supported scheme pairs (shards ->
- * output): TACO_FP8 -> TACO_FP8, INT8_SYM_B64 -> INT8_SYM_B64,
- * INT4_ASYM_G128 -> INT8_ASYM_G128, INT8_ASYM_G128 -> INT8_ASYM_G128; other
- * pairs return QTA_ERR_UNSUPPORTED (use the two calls). */
+/* qar_reduce_requant -- the receiving side of one step of the two-step
+ * all-reduce in one kernel: dequantize-reduce rows [row_begin, row_end) of
+ * the shards and requantize the sums for the gather stage, without writing
+ * an FP32 sum to memory [FLASH: local FP32 sum, then INT8 requantization
+ * before the All-Gather; TACO Fig. 9: one fused operator instead of several
+ * kernels].  QTA_TACO_FP8 -> QTA_TACO_FP8 with equal blocks: the sums are
+ * formed in the Hadamard domain as qar_reduce forms them, and since they are
+ * the transform of the reduced rows they are requantized there directly
+ * (dual-scale rule of taco_compress; the inverse and forward transforms,
+ * which cancel, are skipped).  Every other pair: bit-identical to qar_reduce
+ * followed by qar_requant.  `d` and `shards` as for qar_reduce; `out_desc`
+ * describes the requantized rows as out_desc->batch shards of out_desc->rows
+ * rows each (batch * rows == row_end - row_begin, same cols), `out` its
+ * buffers, `mode` its scale mode (QTA_TACO_FP8 output).  Supported scheme
+ * pairs (shards -> output): TACO_FP8 -> TACO_FP8, INT8_SYM_B64 ->
+ * INT8_SYM_B64, INT4_ASYM_G128 -> INT8_ASYM_G128, INT8_ASYM_G128 ->
+ * INT8_ASYM_G128; other pairs return QTA_ERR_UNSUPPORTED (use the two
+ * calls). */
 qta_status qar_reduce_requant(const qta_desc* d, const qta_qtensor* shards, int32_t n_ranks,
                               int64_t row_begin, int64_t row_end, const qta_desc* out_desc,
                               const qta_qtensor* out, int32_t mode, qta_stream_t stream);

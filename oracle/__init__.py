@@ -82,6 +82,9 @@ def lib():
             L.orc_decompress.restype = i32
             L.orc_reduce.argtypes = [i32, i32, i32, vp, vp, vp, vp, i64, i64, i64, i64, fp]
             L.orc_reduce.restype = i32
+            L.orc_reduce_requant.argtypes = [i32, i32, i32, vp, vp, vp, vp, i64, i64, i64, i64,
+                                             i32, i32, i64, fp, i32, vp, vp, vp]
+            L.orc_reduce_requant.restype = i32
             _lib = L
     return _lib
 
@@ -215,3 +218,39 @@ def reduce(scheme: int, B: int, shards, rows: int, cols: int, row_begin: int = 0
     if rc:
         raise ValueError(f"oracle reduce rejected the arguments ({rc})")
     return out
+
+
+def _shard_arrays(shards):
+    n = len(shards)
+    keep = [tuple(None if a is None else np.ascontiguousarray(a) for a in s) for s in shards]
+    VP = ctypes.c_void_p * n
+    codes = VP(*[_ptr(s[0]) for s in keep])
+    scales = VP(*[_ptr(s[1]) for s in keep])
+    zeros = VP(*[_ptr(s[2]) for s in keep]) if keep[0][2] is not None else None
+    st_keep = [None if s[3] is None else np.ascontiguousarray(s[3], dtype=np.float32) for s in keep]
+    states = VP(*[_ptr(a) for a in st_keep]) if st_keep[0] is not None else None
+    return keep, st_keep, codes, scales, zeros, states
+
+
+def reduce_requant(scheme: int, B: int, shards, rows: int, cols: int, row_begin: int, row_end: int,
+                   out_scheme: int, out_B: int, out_batch: int, out_state=None, mode: int = DELAYED):
+    """Fused dequantize-reduce + requantize; returns (codes, scales, zeros) of
+    the output tensors and updates ``out_state`` in place (TACO output)."""
+    keep, st_keep, codes, scales, zeros, states = _shard_arrays(shards)
+    E = (row_end - row_begin) * cols
+    oc = np.zeros(codes_nbytes(out_scheme, E), dtype=np.int8 if out_scheme == INT8_SYM else np.uint8)
+    oz = None
+    if out_scheme == TACO_FP8:
+        os_ = np.zeros(E // out_B, dtype=np.uint8)
+        assert out_state is not None and out_state.dtype == np.float32 and out_state.size == 2 * out_batch
+    elif out_scheme == INT8_SYM:
+        os_ = np.zeros(E // 64, dtype=np.float32)
+    else:
+        os_ = np.zeros(E // 128, dtype=np.uint16)
+        oz = np.zeros(E // 128, dtype=np.uint16)
+    rc = lib().orc_reduce_requant(scheme, B, len(shards), codes, scales, zeros, states, rows, cols,
+                                  row_begin, row_end, out_scheme, out_B, out_batch, _ptr(out_state), mode,
+                                  _ptr(oc), _ptr(os_), _ptr(oz))
+    if rc:
+        raise ValueError(f"oracle reduce_requant rejected the arguments ({rc})")
+    return oc, os_, oz

@@ -197,18 +197,13 @@ void orc_taco_update_scale(float* state, int64_t batch)
  * R2: blocks are B contiguous elements along the hidden (last) axis.
  * R4: block scale r_b = E4M3(a_b / (448 S)) stored as one E4M3 byte relative
  *     to the per-tensor FP32 scale S; s_b = S * r_b; codes E4M3(y * 1/s_b). */
-static void taco_compress_tensor(const void* x, int dtype, int64_t off, int64_t E,
-                                 int B, float* st, int mode, uint8_t* codes,
-                                 uint8_t* scales, float* y)
+/* Dual-scale FP8 quantization of nblk transformed blocks y (R4, R5). */
+static void taco_quantize_blocks(const float* y, int64_t nblk, int B, float* st, int mode,
+                                 uint8_t* codes, uint8_t* scales)
 {
-    int64_t nblk = E / B;
     if (mode == ORC_CURRENT) {
         float amax = 0.0f;
-        for (int64_t b = 0; b < nblk; ++b) {
-            for (int i = 0; i < B; ++i) y[i] = load_elem(x, dtype, off + b * B + i);
-            orc_fwht(y, B);
-            for (int i = 0; i < B; ++i) amax = fmaxf(amax, fabsf(y[i]));
-        }
+        for (int64_t i = 0; i < nblk * B; ++i) amax = fmaxf(amax, fabsf(y[i]));
         st[0] = orc_scale_from_amax(amax);
         st[1] = 0.0f;
     }
@@ -216,19 +211,32 @@ static void taco_compress_tensor(const void* x, int dtype, int64_t off, int64_t 
     float tinv = 1.0f / (448.0f * S);
     float amax_t = 0.0f;
     for (int64_t b = 0; b < nblk; ++b) {
-        for (int i = 0; i < B; ++i) y[i] = load_elem(x, dtype, off + b * B + i);
-        orc_fwht(y, B);
+        const float* yb = y + b * B;
         float a = 0.0f;
-        for (int i = 0; i < B; ++i) a = fmaxf(a, fabsf(y[i]));
+        for (int i = 0; i < B; ++i) a = fmaxf(a, fabsf(yb[i]));
         amax_t = fmaxf(amax_t, a);
         uint8_t r = orc_e4m3_encode(a * tinv);
         if (r == 0 && a > 0.0f) r = 0x01;
         float sb = S * orc_e4m3_decode(r);
         float inv = (sb > 0.0f) ? 1.0f / sb : 0.0f;
-        for (int i = 0; i < B; ++i) codes[b * B + i] = orc_e4m3_encode(y[i] * inv);
+        for (int i = 0; i < B; ++i) codes[b * B + i] = orc_e4m3_encode(yb[i] * inv);
         scales[b] = r;
     }
     st[1] = fmaxf(st[1], amax_t);
+}
+
+/* ---- TACO FP8 compress of one tensor ([TACO] Core claim, Fig. 7):
+ * the block Hadamard of every block, then the dual-scale quantization. */
+static int taco_compress_tensor(const void* x, int dtype, int64_t off, int64_t E, int B, float* st,
+                                int mode, uint8_t* codes, uint8_t* scales)
+{
+    float* y = (float*)malloc(sizeof(float) * (size_t)(E > 0 ? E : 1));
+    if (!y) return -2;
+    for (int64_t i = 0; i < E; ++i) y[i] = load_elem(x, dtype, off + i);
+    orc_fwht_rows(y, E / B, B);
+    taco_quantize_blocks(y, E / B, B, st, mode, codes, scales);
+    free(y);
+    return 0;
 }
 
 /* ---- block-symmetric INT8, one FP32 scale per 64 ([EQuARX] What carries
@@ -323,12 +331,10 @@ int orc_compress(int scheme, int B, const void* x, int in_dtype, int64_t batch,
     if (check_shape(scheme, B, batch, rows, cols)) return -1;
     int64_t E = rows * cols;
     if (scheme == ORC_TACO_FP8) {
-        float* y = (float*)malloc(sizeof(float) * (size_t)B);
-        if (!y) return -2;
         for (int64_t t = 0; t < batch; ++t)
-            taco_compress_tensor(x, in_dtype, t * E, E, B, state + 2 * t, mode,
-                                 (uint8_t*)codes + t * E, (uint8_t*)scales + t * (E / B), y);
-        free(y);
+            if (taco_compress_tensor(x, in_dtype, t * E, E, B, state + 2 * t, mode,
+                                     (uint8_t*)codes + t * E, (uint8_t*)scales + t * (E / B)))
+                return -2;
     } else if (scheme == ORC_INT8_SYM) {
         for (int64_t t = 0; t < batch; ++t)
             int8sym_compress_tensor(x, in_dtype, t * E, E, (int8_t*)codes + t * E,
@@ -431,6 +437,33 @@ int orc_decompress(int scheme, int B, const void* codes, const void* scales,
  *   ASYM:        acc = fmaf(q_0, s_0, z_0);  acc = acc + fmaf(q_r, s_r, z_r)
  * TACO sums in the Hadamard domain and applies the inverse transform once to
  * the sum (then 1/B). */
+/* The per-element sums of rows [row_begin, row_end) before any transform
+ * (R9), written to acc. */
+static void reduce_sums(int scheme, int B, int n_ranks, const void* const* codes,
+                        const void* const* scales, const void* const* zeros,
+                        const float* const* states, int64_t cols, int64_t row_begin,
+                        int64_t row_end, float* acc_out)
+{
+    int64_t e0 = row_begin * cols, e1 = row_end * cols;
+    for (int64_t e = e0; e < e1; ++e) {
+        float acc = 0.0f;
+        for (int r = 0; r < n_ranks; ++r) {
+            const void* z = zeros ? zeros[r] : 0;
+            const float* st = states ? states[r] : 0;
+            if (r == 0) {
+                acc = dequant(scheme, B, codes[r], scales[r], z, st, e);
+            } else if (scheme == ORC_TACO_FP8 || scheme == ORC_INT8_SYM) {
+                float code, sc;
+                code_and_scale(scheme, B, codes[r], scales[r], st, e, &code, &sc);
+                acc = fmaf(code, sc, acc);
+            } else {
+                acc = acc + dequant(scheme, B, codes[r], scales[r], z, st, e);
+            }
+        }
+        acc_out[e - e0] = acc;
+    }
+}
+
 int orc_reduce(int scheme, int B, int n_ranks, const void* const* codes,
                const void* const* scales, const void* const* zeros,
                const float* const* states, int64_t rows, int64_t cols,
@@ -438,29 +471,52 @@ int orc_reduce(int scheme, int B, int n_ranks, const void* const* codes,
 {
     if (check_shape(scheme, B, 1, rows, cols)) return -1;
     if (n_ranks < 1 || row_begin < 0 || row_end < row_begin || row_end > rows) return -1;
-    int64_t e0 = row_begin * cols, e1 = row_end * cols;
-    for (int64_t b0 = e0; b0 < e1; b0 += B) {
-        for (int i = 0; i < B; ++i) {
-            float acc = 0.0f;
-            for (int r = 0; r < n_ranks; ++r) {
-                const void* z = zeros ? zeros[r] : 0;
-                const float* st = states ? states[r] : 0;
-                if (r == 0) {
-                    acc = dequant(scheme, B, codes[r], scales[r], z, st, b0 + i);
-                } else if (scheme == ORC_TACO_FP8 || scheme == ORC_INT8_SYM) {
-                    float code, sc;
-                    code_and_scale(scheme, B, codes[r], scales[r], st, b0 + i, &code, &sc);
-                    acc = fmaf(code, sc, acc);
-                } else {
-                    acc = acc + dequant(scheme, B, codes[r], scales[r], z, st, b0 + i);
-                }
-            }
-            sum_out[b0 - e0 + i] = acc;
-        }
-        if (scheme == ORC_TACO_FP8) {
-            orc_fwht(sum_out + (b0 - e0), B);
-            for (int i = 0; i < B; ++i) sum_out[b0 - e0 + i] = sum_out[b0 - e0 + i] * (1.0f / (float)B);
+    reduce_sums(scheme, B, n_ranks, codes, scales, zeros, states, cols, row_begin, row_end, sum_out);
+    if (scheme == ORC_TACO_FP8) {
+        int64_t n = (row_end - row_begin) * cols;
+        for (int64_t b0 = 0; b0 < n; b0 += B) {
+            orc_fwht(sum_out + b0, B);
+            for (int i = 0; i < B; ++i) sum_out[b0 + i] = sum_out[b0 + i] * (1.0f / (float)B);
         }
     }
     return 0;
+}
+
+/* Fused dequantize-reduce + requantize of rows [row_begin, row_end) into
+ * out_batch output tensors of (row_end-row_begin)/out_batch rows each.
+ * TACO -> TACO with equal blocks: the sums are already in the Hadamard
+ * domain of the output blocks -- they are the transform of the reduced rows
+ * -- so they are requantized there directly (the inverse and the forward
+ * transform, which cancel, are not applied).  Every other pair: qar_reduce
+ * then the compress of its FP32 rows (R10). */
+int orc_reduce_requant(int scheme, int B, int n_ranks, const void* const* codes,
+                       const void* const* scales, const void* const* zeros,
+                       const float* const* states, int64_t rows, int64_t cols,
+                       int64_t row_begin, int64_t row_end, int out_scheme, int out_B,
+                       int64_t out_batch, float* out_state, int mode, void* out_codes,
+                       void* out_scales, void* out_zeros)
+{
+    if (check_shape(scheme, B, 1, rows, cols)) return -1;
+    if (n_ranks < 1 || row_begin < 0 || row_end < row_begin || row_end > rows) return -1;
+    int64_t nrows = row_end - row_begin;
+    if (out_batch < 1 || nrows % out_batch) return -1;
+    if (check_shape(out_scheme, out_B, out_batch, nrows / out_batch, cols)) return -1;
+    float* acc = (float*)malloc(sizeof(float) * (size_t)(nrows * cols > 0 ? nrows * cols : 1));
+    if (!acc) return -2;
+    int rc = 0;
+    if (scheme == ORC_TACO_FP8 && out_scheme == ORC_TACO_FP8 && B == out_B) {
+        reduce_sums(scheme, B, n_ranks, codes, scales, zeros, states, cols, row_begin, row_end, acc);
+        int64_t Et = nrows / out_batch * cols;
+        for (int64_t t = 0; t < out_batch; ++t)
+            taco_quantize_blocks(acc + t * Et, Et / B, B, out_state + 2 * t, mode,
+                                 (uint8_t*)out_codes + t * Et, (uint8_t*)out_scales + t * (Et / B));
+    } else {
+        rc = orc_reduce(scheme, B, n_ranks, codes, scales, zeros, states, rows, cols, row_begin,
+                        row_end, acc);
+        if (!rc)
+            rc = orc_compress(out_scheme, out_B, acc, ORC_FP32, out_batch, nrows / out_batch, cols,
+                              out_state, mode, out_codes, out_scales, out_zeros);
+    }
+    free(acc);
+    return rc;
 }

@@ -74,6 +74,14 @@ int orc_reduce(int scheme, int B, int n_ranks, const void* const* codes,
                const float* const* states, int64_t rows, int64_t cols,
                int64_t row_begin, int64_t row_end, float* sum_out);
 
+/* ---- fused dequantize-reduce + requantize ---- */
+int orc_reduce_requant(int scheme, int B, int n_ranks, const void* const* codes,
+                       const void* const* scales, const void* const* zeros,
+                       const float* const* states, int64_t rows, int64_t cols,
+                       int64_t row_begin, int64_t row_end, int out_scheme, int out_B,
+                       int64_t out_batch, float* out_state, int mode, void* out_codes,
+                       void* out_scales, void* out_zeros);
+
 #ifdef __cplusplus
 }
 #endif

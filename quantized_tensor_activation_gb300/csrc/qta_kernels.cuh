@@ -348,9 +348,10 @@ struct Quantizer {
     float S = 1.0f, tinv = 0.0f;
 
     // AMAX_ONLY: transform and record the amax, write nothing else.
+    // transformed (TACO): v already holds the Hadamard-domain values.
     template <bool AMAX_ONLY>
     __device__ __forceinline__ void run(u64 (&v)[32], const QuantOut& o, int tile_first, int lane,
-                                        uint32_t (&ow)[16])
+                                        uint32_t (&ow)[16], bool transformed = false)
     {
         const int g = tile_first + lane;
         const bool valid = g < o.M;
@@ -361,8 +362,10 @@ struct Quantizer {
             const int t_last = (int)fdiv((uint32_t)g_last, o.seg_per_tensor);
             const bool uniform = (t_first == t_last);
             const int tens = uniform ? t_first : (int)fdiv((uint32_t)min(g, o.M - 1), o.seg_per_tensor);
-            fwht64_local(v);
-            fwht_cross(v, L, lane);
+            if (!transformed) {
+                fwht64_local(v);
+                fwht_cross(v, L, lane);
+            }
             const float a = absmax64(v);
             if (uniform) {
                 if (tens != amax.tensor) {
@@ -735,8 +738,9 @@ __device__ __forceinline__ void reduce_meta_load(const ReduceParams& p, int t, i
 // qar_reduce (OSCH = OUT_F32) and the fused qar_reduce_requant (OSCH = the
 // requantization scheme; AMAX_ONLY = its CURRENT-mode pre-pass).  The sum of
 // a warp tile is formed exactly as qar_reduce forms it and then quantized
-// exactly as qar_requant quantizes an FP32 input, so the fused result is
-// bit-identical to the two calls.
+// exactly as qar_requant quantizes an FP32 input -- bit-identical to the two
+// calls -- except for TACO -> TACO with equal blocks, where the Hadamard-
+// domain sum is requantized directly.
 template <int SCH, int OSCH, bool AMAX_ONLY>
 __global__ void __launch_bounds__(ReduceCfg<SCH, OSCH>::WARPS * 32, 1)
 reduce_kernel(const __grid_constant__ ReduceParams p)
@@ -809,7 +813,11 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
             }
         }
         if (aborted) break;
-        if constexpr (SCH == S_TACO) {
+        // TACO -> TACO with equal blocks: the sums already are the Hadamard
+        // transform of the reduced rows, so they are requantized as they are
+        // (the inverse and forward transforms cancel and are skipped).
+        const bool direct = (SCH == S_TACO) && (OSCH == S_TACO) && (p.q_lanes_per_block == L);
+        if (SCH == S_TACO && !direct) {
             fwht64_local(acc);
             fwht_cross(acc, L, lane);
             if constexpr (OSCH == OUT_F32) {
@@ -838,7 +846,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
             }
         } else {
             uint32_t ow[16];
-            quant.template run<AMAX_ONLY>(acc, qo, wt * 32, lane, ow);
+            quant.template run<AMAX_ONLY>(acc, qo, wt * 32, lane, ow, direct);
             if constexpr (!AMAX_ONLY) store_codes<OSCH, 1>(outb, &p.out_map, wt * 32, lane, ow);
         }
     }

@@ -275,8 +275,9 @@ def test_copy_kernel(dev):
 @pytest.mark.parametrize("n", [1, 3, 8])
 @pytest.mark.parametrize("mode", [qta.SCALE_CURRENT, qta.SCALE_DELAYED])
 def test_reduce_requant_fused(dev, scheme, B, gscheme, gB, n, mode):
-    # the fused call equals qar_reduce followed by qar_requant, computed by
-    # the oracle (reduce, then compress of the FP32 sum), bit for bit
+    # the fused call against the oracle's fused reduce + requant (TACO ->
+    # TACO with equal blocks requantizes the Hadamard-domain sums; every
+    # other pair is reduce, then compress of the FP32 sum), bit for bit
     rows, cols = 96, 1024
     rng = np.random.default_rng(hash((scheme, B, gscheme, n, mode)) % 2 ** 32)
     shards = _oracle_shards(scheme, B, n, rows, cols, rng)
@@ -292,9 +293,10 @@ def test_reduce_requant_fused(dev, scheme, B, gscheme, gB, n, mode):
             st0[1::2] = [0.5 * j for j in range(nb)]
             g.state.copy_(torch.from_numpy(st0))
         qta.qar_reduce_requant(d, ds, rb, re_, dg, g, mode)
-        osum = orc.reduce(ORC_SCH[scheme], B, shards, rows, cols, rb, re_)
-        ref = oracle_compress(gscheme, gB, torch.from_numpy(osum), qta.FP32, nb, gr, cols,
-                              orc.CURRENT if mode == qta.SCALE_CURRENT else orc.DELAYED, state=st0)
+        st_ref = None if st0 is None else st0.copy()
+        c, s, z = orc.reduce_requant(ORC_SCH[scheme], B, shards, rows, cols, rb, re_, ORC_SCH[gscheme], gB,
+                                     nb, st_ref, orc.CURRENT if mode == qta.SCALE_CURRENT else orc.DELAYED)
+        ref = (c, s, z, st_ref)
         torch.cuda.synchronize()
         compare_qtensor(f"fused rows {rb}:{re_}", g, ref)
     assert qta.qta_device_error() == 0

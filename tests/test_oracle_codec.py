@@ -310,3 +310,61 @@ def test_reduce_accumulates_with_one_rounding_per_rank(orc, scheme, B):
     if scheme == orc.TACO_FP8:
         ref = (orc.fwht(ref, B) * np.float32(1.0 / B)).astype(np.float32)
     assert np.array_equal(out.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("scheme,B,oscheme,oB", [(1, 64, 1, 64), (2, 128, 3, 128), (3, 128, 3, 128),
+                                                 (0, 128, 0, 256), (0, 256, 0, 64)])
+def test_reduce_requant_equals_two_calls(orc, scheme, B, oscheme, oB):
+    # every pair but TACO -> TACO with equal blocks is reduce, then compress
+    rows, cols, n = 16, 512, 3
+    shards, _ = _make_shards(orc, scheme, B, n, rows, cols, seed=21)
+    st1 = np.array([0.01, 0.0, 0.02, 0.1], dtype=np.float32)
+    st2 = st1.copy()
+    f = orc.reduce_requant(scheme, B, shards, rows, cols, 2, 10, oscheme, oB, 2, st1 if oscheme == 0 else None)
+    s = orc.reduce(scheme, B, shards, rows, cols, 2, 10)
+    c = orc.compress(oscheme, oB, s, orc.FP32, 2, 4, cols, st2 if oscheme == 0 else None)
+    for a, b in zip(f, c):
+        assert (a is None and b is None) or np.array_equal(a, b)
+    assert np.array_equal(st1, st2)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_reduce_requant_taco_hadamard_domain(orc, mode):
+    # TACO -> TACO, equal blocks: the codes quantize the exact FP32 Hadamard-
+    # domain sums (emulated with exact rationals) -- every code is the nearest
+    # E4M3 value to sum/s_b and every block byte the nearest to a_b/(448 S) --
+    # and decompressing them approximates the float64 sum of the inputs within
+    # the FP8 error of Eq. (3) (TACO Fig. 6).
+    from fractions import Fraction
+    B, rows, cols, n = 128, 2, 256, 3
+    shards, deq = _make_shards(orc, 0, B, n, rows, cols, seed=5)
+    st = np.array([0.02, 0.0], dtype=np.float32)
+    c, s, _ = orc.reduce_requant(0, B, shards, rows, cols, 0, rows, 0, B, 1, st, mode)
+    table = _e4m3_pos()
+    E = rows * cols
+    y = np.zeros(E)
+    for e in range(E):
+        a = None
+        for r, (cc, ss, z, sts) in enumerate(shards):
+            code = Fraction(float(table[cc[e]]))
+            sc = Fraction(float(np.float32(sts[0]) * table[ss[e // B]]))
+            a = _round_f32(code * sc) if r == 0 else _round_f32(code * sc + Fraction(a))
+        y[e] = a
+    y = y.astype(np.float32).reshape(-1, B)
+    a_b = np.abs(y).max(axis=1).astype(np.float64)
+    if mode == 1:
+        assert st[1] == np.float32(a_b.max()) and st[0] == orc.scale_from_amax(st[1])
+    S = float(st[0])
+    ok = _nearest_codes(a_b / (448.0 * S), table)[np.arange(len(a_b)), s]
+    assert np.all(ok | ((s == 1) & (a_b > 0)))
+    sb = (np.float32(S) * table[s]).astype(np.float64)
+    for b in range(len(a_b)):
+        near = _nearest_codes(np.clip(y[b] / sb[b], -448, 448), table)
+        assert np.all(near[np.arange(B), c.reshape(-1, B)[b]])
+    # round trip to the original domain against the float64 sum of the inputs
+    out = orc.decompress(0, B, c, s, None, st, 1, rows, cols, orc.FP32).astype(np.float64)
+    ref = np.stack(deq).astype(np.float64).sum(axis=0)
+    err = np.sqrt(((out - ref) ** 2).reshape(-1, B).sum(axis=1))
+    bound = np.sqrt((np.abs(y).astype(np.float64) ** 2).sum(axis=1)) / np.sqrt(B) * (2.0 ** -4 + 1e-5) \
+        + n * 1e-6 * np.abs(ref).reshape(-1, B).max(axis=1) * np.sqrt(B)
+    assert np.all(err <= bound)
