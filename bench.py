@@ -176,10 +176,9 @@ def _cpu_oracle_path(w: workloads.Workload, rows: int, seed: int = 0):
     nb = E // B
     shards = [(c[r * cb:(r + 1) * cb], s[r * nb:(r + 1) * nb], None if z is None else z[r * nb:(r + 1) * nb],
                None if st is None else st[2 * r:2 * r + 2]) for r in range(N)]
-    ssum = orc.reduce(s1, B, shards, rows, C)
     gr = max(1, rows // N)
     st2 = np.zeros(2 * N, dtype=np.float32) if s2 == orc.TACO_FP8 else None
-    c2, sc2, z2 = orc.compress(s2, gB, ssum[: N * gr * C], orc.FP32, N, gr, C, st2, orc.CURRENT)
+    c2, sc2, z2 = orc.reduce_requant(s1, B, shards, rows, C, 0, N * gr, s2, gB, N, st2, orc.CURRENT)
     orc.decompress(s2, gB, c2, sc2, z2, st2, N, gr, C, dt)
     dt_s = time.perf_counter() - t0
     return dt_s, 2 * E * N, 1
