@@ -346,6 +346,25 @@ struct Quantizer {
     AmaxTracker amax;
     int cached_tensor = -1;
     float S = 1.0f, tinv = 0.0f;
+    // tensor of the coming tile and its scale, fetched ahead by begin()
+    bool uniform = true;
+    int tens = 0;
+    float S_next = 1.0f;
+
+    // Start of a warp tile: locate its tensor and fetch the per-tensor scale
+    // early, so that the load has landed when run() needs it.
+    __device__ __forceinline__ void begin(const QuantOut& o, int tile_first, int lane)
+    {
+        if constexpr (SCH == S_TACO) {
+            const int g = tile_first + lane;
+            const int g_last = min(tile_first + 31, o.M - 1);
+            const int t_first = (int)fdiv((uint32_t)tile_first, o.seg_per_tensor);
+            const int t_last = (int)fdiv((uint32_t)g_last, o.seg_per_tensor);
+            uniform = (t_first == t_last);
+            tens = uniform ? t_first : (int)fdiv((uint32_t)min(g, o.M - 1), o.seg_per_tensor);
+            if (!uniform || tens != cached_tensor) S_next = __ldg(o.state + 2 * tens);
+        }
+    }
 
     // AMAX_ONLY: transform and record the amax, write nothing else.
     // transformed (TACO): v already holds the Hadamard-domain values.
@@ -357,11 +376,6 @@ struct Quantizer {
         const bool valid = g < o.M;
         const int L = o.lanes_per_block;
         if constexpr (SCH == S_TACO) {
-            const int g_last = min(tile_first + 31, o.M - 1);
-            const int t_first = (int)fdiv((uint32_t)tile_first, o.seg_per_tensor);
-            const int t_last = (int)fdiv((uint32_t)g_last, o.seg_per_tensor);
-            const bool uniform = (t_first == t_last);
-            const int tens = uniform ? t_first : (int)fdiv((uint32_t)min(g, o.M - 1), o.seg_per_tensor);
             if (!transformed) {
                 fwht64_local(v);
                 fwht_cross(v, L, lane);
@@ -378,7 +392,7 @@ struct Quantizer {
             }
             if constexpr (!AMAX_ONLY) {
                 if (!uniform || tens != cached_tensor) {
-                    S = __ldg(o.state + 2 * tens);
+                    S = S_next;
                     tinv = __frcp_rn(__fmul_rn(448.0f, S));
                     cached_tensor = uniform ? tens : -1;
                 }
@@ -531,6 +545,7 @@ compress_kernel(const __grid_constant__ CompressParams p)
     bool aborted = false;
 
     for (int wt = first; wt < p.n_warp_tiles; wt += W, ++k) {
+        quant.begin(qo, wt * 32, lane);
         const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[stage], phase, p.err));
         if (!ok) {
             aborted = true;
@@ -776,6 +791,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
     if (my_tiles > 0) reduce_meta_load<SCH>(p, 0, 0, first, W, lane, nxt);
     for (int t = 0; t < my_tiles && !aborted; ++t) {
         const int wt = first + t * W;
+        if constexpr (OSCH != OUT_F32) quant.begin(qo, wt * 32, lane);
         u64 acc[32];
         for (int c = 0; c < n_chunks && !aborted; ++c) {
             SegMeta<SCH> cur[RANK_CHUNK];
