@@ -706,16 +706,27 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
 }
 
 // ------------------------------------------------------------ reduce
-// Units of the stage ring are (warp tile, rank) pairs, rank fastest.
+// Units of the stage ring are (warp tile, rank) pairs, rank fastest; the
+// issuing lane walks them with a cursor (tile index t, rank r).
+struct UnitCursor {
+    int t = 0, r = 0;
+    __device__ __forceinline__ void advance(int n_ranks)
+    {
+        if (++r == n_ranks) {
+            r = 0;
+            ++t;
+        }
+    }
+};
+
 template <int SCH, int OSCH>
 __device__ __forceinline__ void reduce_issue(const ReduceParams& p, uint8_t* wb, uint64_t* bars,
-                                             int stage, int unit, int first, int W)
+                                             int stage, const UnitCursor& u, int first, int W)
 {
     using C = ReduceCfg<SCH, OSCH>;
-    const int t = unit / p.n_ranks, r = unit - t * p.n_ranks;
-    const int wt = first + t * W;
+    const int wt = first + u.t * W;
     mbar_arrive_expect_tx(&bars[stage], C::IN_BYTES);
-    tma_load_2d(wb + stage * C::IN_BYTES, &p.in_map[r], 0, p.seg_begin + wt * 32, &bars[stage]);
+    tma_load_2d(wb + stage * C::IN_BYTES, &p.in_map[u.r], 0, p.seg_begin + wt * 32, &bars[stage]);
 }
 
 // Ranks are processed in chunks of RANK_CHUNK; the scale metadata of the next
@@ -772,10 +783,14 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
     const int n = p.n_ranks;
     const int my_tiles = (first < p.n_warp_tiles) ? (p.n_warp_tiles - first + W - 1) / W : 0;
     const int total_units = my_tiles * n;
+    UnitCursor next_unit;   // next unit to load (meaningful in lane 0)
     if (lane == 0) {
         for (int s = 0; s < C::STAGES; ++s) mbar_init(&bars[s], 1);
         fence_barrier_init();
-        for (int u = 0; u < C::STAGES && u < total_units; ++u) reduce_issue<SCH, OSCH>(p, wb, bars, u, u, first, W);
+        for (int u = 0; u < C::STAGES && u < total_units; ++u) {
+            reduce_issue<SCH, OSCH>(p, wb, bars, u, next_unit, first, W);
+            next_unit.advance(n);
+        }
     }
     __syncwarp();
     const int L = p.lanes_per_block;
@@ -819,7 +834,8 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                 __syncwarp();
                 if (lane == 0 && unit + C::STAGES < total_units) {
                     fence_proxy_async_smem();
-                    reduce_issue<SCH, OSCH>(p, wb, bars, stage, unit + C::STAGES, first, W);
+                    reduce_issue<SCH, OSCH>(p, wb, bars, stage, next_unit, first, W);
+                    next_unit.advance(n);
                 }
                 ++unit;
                 if (++stage == C::STAGES) {
