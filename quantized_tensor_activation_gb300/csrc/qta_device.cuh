@@ -339,6 +339,14 @@ __device__ __forceinline__ u64 rint_bits2(u64 y)
     return add2(y, pk2(12582912.0f, 12582912.0f));
 }
 
+// Round to the nearest integer (ties to even) and clamp to [0, 255].
+__device__ __forceinline__ uint32_t cvt_rni_sat_u8(float y)
+{
+    uint32_t r;
+    asm("cvt.rni.sat.u8.f32 %0, %1;" : "=r"(r) : "f"(y));
+    return r;
+}
+
 // Low bytes of four words into one word: (a, b, c, d) -> bytes [a b c d].
 __device__ __forceinline__ uint32_t bytes4(uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {

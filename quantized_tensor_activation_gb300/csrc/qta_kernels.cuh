@@ -116,10 +116,15 @@ constexpr int OUT_F32 = -1;
 
 template <int SCH, int OSCH = OUT_F32>
 struct ReduceCfg {
-    static constexpr int WARPS = 12;
+    // the INT4 fused kernel fits 128 registers and gains from 16 warps; the
+    // others need more registers and run 12
+    static constexpr bool W16 = (SCH == S_ASYM4) && (OSCH != OUT_F32);
+    static constexpr int WARPS = W16 ? 16 : 12;
     static constexpr int IN_SEG = (SCH == S_ASYM4) ? 32 : 64;
     static constexpr int OUT_SEG = (OSCH == OUT_F32) ? 256 : (OSCH == S_ASYM4) ? 32 : 64;
-    static constexpr int STAGES = (OSCH == OUT_F32) ? ((SCH == S_ASYM4) ? 8 : 4) : ((SCH == S_ASYM4) ? 16 : 8);
+    static constexpr int STAGES = (OSCH == OUT_F32) ? ((SCH == S_ASYM4) ? 8 : 4) : ((SCH == S_ASYM4) ? 12 : 8);
+    // ranks whose scale metadata is fetched together, one chunk ahead
+    static constexpr int RANK_CHUNK = W16 ? 8 : 4;
     static constexpr int IN_BYTES = 32 * IN_SEG;
     static constexpr int OUT_BYTES = 32 * OUT_SEG;
     static constexpr int OUT_BUFS = 1;
@@ -212,28 +217,22 @@ __device__ __forceinline__ void load_codes4(const uint8_t* st, int lane, uint32_
 }
 
 // Dequantization of one segment's codes (before any transform).
-// MODE 0 (assign):     TACO E4M3(q)*s, INT8 q*s   -- scalar mul.rn
+// MODE 0 (assign):     TACO E4M3(q)*s, INT8 q*s
 //                      ASYM fmaf(q, s, z)
 // MODE 1 (accumulate): TACO/INT8 v = fmaf(code, s, v)
 //                      ASYM      v = v + fmaf(q, s, z)
-// The assigning multiply is scalar because ptxas contracts a packed
-// multiply into a packed add that consumes it in the same basic block;
-// scalar mul.rn is never contracted, so the product is rounded on its own
-// exactly as defined.
+// ptxas contracts a packed multiply into a packed add that consumes it in
+// the same basic block.  The products of MODE 0 are only ever consumed by a
+// fused multiply-add, a scalar add.rn (the first butterfly stage, which is
+// never contracted), a multiply, a conversion or a store, so they keep their
+// own rounding as defined.
 template <int SCH, int MODE>
 __device__ __forceinline__ void dequant_segment(const uint8_t* st, int lane, float s, float z, u64 (&v)[32])
 {
     const u64 s2 = pk2(s, s);
     const u64 z2 = pk2(z, z);
     // code pair c (exact) -> v[j]
-    auto sym = [&](int j, u64 c) {
-        if constexpr (MODE == 0) {
-            const float2 t = up2(c);
-            v[j] = pk2(__fmul_rn(t.x, s), __fmul_rn(t.y, s));
-        } else {
-            v[j] = fma2(c, s2, v[j]);
-        }
-    };
+    auto sym = [&](int j, u64 c) { v[j] = (MODE == 0) ? mul2(c, s2) : fma2(c, s2, v[j]); };
     auto asym = [&](int j, u64 c) {
         const u64 d = fma2(c, s2, z2);
         v[j] = (MODE == 0) ? d : add2(v[j], d);
@@ -452,9 +451,15 @@ struct Quantizer {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const float2 y = up2(mul2(sub2(v[j], z2), inv2));
-                const u64 r = rint_bits2(pk2(fminf(fmaxf(y.x, 0.0f), Q), fminf(fmaxf(y.y, 0.0f), Q)));
-                rb[2 * j] = lo32(r);
-                rb[2 * j + 1] = hi32(r);
+                if constexpr (SCH == S_ASYM8) {
+                    // round to nearest even and clamp to [0, 255] in one conversion
+                    rb[2 * j] = cvt_rni_sat_u8(y.x);
+                    rb[2 * j + 1] = cvt_rni_sat_u8(y.y);
+                } else {
+                    const u64 r = rint_bits2(pk2(fminf(fmaxf(y.x, 0.0f), Q), fminf(fmaxf(y.y, 0.0f), Q)));
+                    rb[2 * j] = lo32(r);
+                    rb[2 * j + 1] = hi32(r);
+                }
             }
             if constexpr (SCH == S_ASYM4) {
 #pragma unroll
@@ -731,9 +736,7 @@ __device__ __forceinline__ void reduce_issue(const ReduceParams& p, uint8_t* wb,
 
 // Ranks are processed in chunks of RANK_CHUNK; the scale metadata of the next
 // chunk is fetched while the current one is accumulated.
-constexpr int RANK_CHUNK = 4;
-
-template <int SCH>
+template <int SCH, int RANK_CHUNK>
 __device__ __forceinline__ void reduce_meta_load(const ReduceParams& p, int t, int c, int first, int W, int lane,
                                                  SegMeta<SCH> (&m)[RANK_CHUNK])
 {
@@ -794,6 +797,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
     }
     __syncwarp();
     const int L = p.lanes_per_block;
+    constexpr int RANK_CHUNK = C::RANK_CHUNK;
     const int n_chunks = (n + RANK_CHUNK - 1) / RANK_CHUNK;
     int stage = 0;
     uint32_t phase = 0;
@@ -803,7 +807,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                       p.q_seg_per_tensor};
     Quantizer<(OSCH == OUT_F32) ? S_TACO : OSCH> quant;
     SegMeta<SCH> nxt[RANK_CHUNK];
-    if (my_tiles > 0) reduce_meta_load<SCH>(p, 0, 0, first, W, lane, nxt);
+    if (my_tiles > 0) reduce_meta_load<SCH, RANK_CHUNK>(p, 0, 0, first, W, lane, nxt);
     for (int t = 0; t < my_tiles && !aborted; ++t) {
         const int wt = first + t * W;
         if constexpr (OSCH != OUT_F32) quant.begin(qo, wt * 32, lane);
@@ -813,9 +817,9 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
 #pragma unroll
             for (int kk = 0; kk < RANK_CHUNK; ++kk) cur[kk] = nxt[kk];
             if (c + 1 < n_chunks)
-                reduce_meta_load<SCH>(p, t, c + 1, first, W, lane, nxt);
+                reduce_meta_load<SCH, RANK_CHUNK>(p, t, c + 1, first, W, lane, nxt);
             else if (t + 1 < my_tiles)
-                reduce_meta_load<SCH>(p, t + 1, 0, first, W, lane, nxt);
+                reduce_meta_load<SCH, RANK_CHUNK>(p, t + 1, 0, first, W, lane, nxt);
 #pragma unroll
             for (int kk = 0; kk < RANK_CHUNK; ++kk) {
                 const int r = c * RANK_CHUNK + kk;
