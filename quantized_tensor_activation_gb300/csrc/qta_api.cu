@@ -205,6 +205,8 @@ cudaError_t ensure_smem_attr(const void* func, int smem, std::atomic<unsigned>* 
 
 __global__ void state_kernel(float* state, long long n, int op)
 {
+    pdl_wait();
+    pdl_trigger();
     const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
     if (t >= n) return;
     if (op == STATE_UPDATE) {
@@ -239,8 +241,7 @@ cudaError_t launch_state(float* state, long long n, int op, cudaStream_t stream)
     if (n <= 0) return cudaSuccess;
     const int threads = 128;
     const long long blocks = (n + threads - 1) / threads;
-    state_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(state, n, op);
-    return cudaGetLastError();
+    return launch_pdl(state_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream, state, n, op);
 }
 
 cudaError_t launch_copy(const void* src, void* dst, size_t bytes, int grid, cudaStream_t stream)

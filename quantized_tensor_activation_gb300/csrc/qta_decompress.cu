@@ -25,8 +25,7 @@ static cudaError_t launch_d(const DecompressParams& p, int grid, cudaStream_t st
     auto fn = decompress_kernel<SCH, OUT>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(fn), C::SMEM, &done);
     if (e != cudaSuccess) return e;
-    fn<<<grid, C::WARPS * 32, C::SMEM, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(fn, dim3(grid), dim3(C::WARPS * 32), C::SMEM, stream, p);
 }
 
 template <int SCH>

@@ -90,6 +90,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
     return mbar_wait_slow(bar, parity, err);
 }
 
+// ------------------------------------------- programmatic dependent launch
+// The kernels are launched with programmatic stream serialization: a kernel
+// may start while its predecessor on the stream drains.  Every thread waits
+// for the predecessor's completion (and memory) before its first global
+// access; the trigger lets the successor be scheduled as SMs free up.  Both
+// are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
                                             uint64_t* bar)

@@ -534,6 +534,10 @@ compress_kernel(const __grid_constant__ CompressParams p)
     if (lane == 0) {
         for (int s = 0; s < C::STAGES; ++s) mbar_init(&bars[s], 1);
         fence_barrier_init();
+    }
+    pdl_wait();
+    pdl_trigger();
+    if (lane == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             const int wt = first + s * W;
             if (wt >= p.n_warp_tiles) break;
@@ -635,6 +639,10 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
     if (lane == 0) {
         for (int s = 0; s < C::STAGES; ++s) mbar_init(&bars[s], 1);
         fence_barrier_init();
+    }
+    pdl_wait();
+    pdl_trigger();
+    if (lane == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             const int wt = first + s * W;
             if (wt >= p.n_warp_tiles) break;
@@ -790,6 +798,10 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
     if (lane == 0) {
         for (int s = 0; s < C::STAGES; ++s) mbar_init(&bars[s], 1);
         fence_barrier_init();
+    }
+    pdl_wait();
+    pdl_trigger();
+    if (lane == 0) {
         for (int u = 0; u < C::STAGES && u < total_units; ++u) {
             reduce_issue<SCH, OSCH>(p, wb, bars, u, next_unit, first, W);
             next_unit.advance(n);

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <atomic>
+#include <utility>
 
 #include "qta_kernels.cuh"
 
@@ -27,6 +28,24 @@ cudaError_t launch_reduce_requant(int scheme, int out_scheme, bool amax_only, co
                                   cudaStream_t stream);
 cudaError_t launch_state(float* state, long long n, int op, cudaStream_t stream);
 cudaError_t launch_copy(const void* src, void* dst, size_t bytes, int grid, cudaStream_t stream);
+
+// Launch with programmatic stream serialization (see pdl_wait / pdl_trigger).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Per-device one-time setting of the dynamic shared-memory limit of a kernel.
 cudaError_t ensure_smem_attr(const void* func, int smem, std::atomic<unsigned>* done_mask);

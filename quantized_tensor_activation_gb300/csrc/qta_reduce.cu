@@ -28,8 +28,7 @@ static cudaError_t launch_r(const ReduceParams& p, int grid, cudaStream_t stream
     auto fn = reduce_kernel<SCH, OSCH, AMAX>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(fn), C::SMEM, &done);
     if (e != cudaSuccess) return e;
-    fn<<<grid, C::WARPS * 32, C::SMEM, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(fn, dim3(grid), dim3(C::WARPS * 32), C::SMEM, stream, p);
 }
 
 cudaError_t launch_reduce(int scheme, const ReduceParams& p, int grid, cudaStream_t stream)
