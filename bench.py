@@ -477,6 +477,24 @@ def run_qta(args, w):
     tr = NCU_TRAFFIC.get(("taco_compress", w.name))
     traffic = tr["bytes"] if tr and tr.get("src") == _src_digest() else None
 
+    # reconstruction error of the step's output against the exact sum of the
+    # ranks' inputs (float64), and of one rank's compress -> decompress
+    recon = None
+    if not args.no_recon:
+        with torch.no_grad():
+            exact = x.double().sum(dim=0)
+            err = y.double() - exact
+            mse = float((err * err).mean())
+            d0 = qta.desc(sch[w.scheme], w.block, R, C)
+            y0 = torch.empty((R, C), dtype=torch.float32, device=dev)
+            qta.taco_decompress(d0, shards[0], y0, qta.FP32)
+            e0 = y0.double() - x[0].double()
+            recon = {"allreduce_mse": mse, "allreduce_nmse": mse / float((exact * exact).mean()),
+                     "stage1_mse_rank0": float((e0 * e0).mean()),
+                     "stage1_nmse_rank0": float((e0 * e0).mean()) / float((x[0].double() ** 2).mean()),
+                     "note": "output of the timed step vs the float64 sum of the 16-bit inputs"}
+            del exact, err, e0, y0
+
     cpu = None
     if not args.no_cpu_baseline and ws == 1:
         rows = args.cpu_rows or w.rows
@@ -499,6 +517,7 @@ def run_qta(args, w):
         "step_frac_of_hbm": step_bytes / (ms_step * 1e-3) / 1e9 / peak,
         "other_path": {"path": "qar_reduce + qar_requant" if fused else "qar_reduce_requant",
                        "ms_per_step": other_ms, "value": in_bytes / (other_ms * 1e-3) / 1e9 * ws},
+        "recon": recon,
         "cpu_baseline": cpu,
         "clocks": clk,
         "e2e": e2e,
@@ -522,6 +541,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="skip the nvidia-smi clock window (profiling runs)")
+    ap.add_argument("--no-recon", action="store_true", help="skip the reconstruction-error report")
     ap.add_argument("--no-graph", action="store_true", help="launch the timed steps eagerly instead of as a CUDA graph")
     ap.add_argument("--path", default="fused", choices=["fused", "split"],
                     help="fused: qar_reduce_requant; split: qar_reduce then qar_requant (FP32 sum in HBM)")
