@@ -108,6 +108,14 @@ def step_factor(w: Workload, step: int, seed: int = 0) -> float:
     return math.exp(lo + (hi - lo) * u)
 
 
+def laplace_from_uniform(r: torch.Tensor, b: float) -> torch.Tensor:
+    """Laplace(0, b) by the inverse CDF, evaluated at the cell midpoints
+    (k + 1/2)/2^24 of float32 uniforms r = k/2^24, so |u| < 1/2 and every
+    draw is finite (r = 0 would otherwise give -inf)."""
+    u = (r.double() + 2.0 ** -25) - 0.5
+    return (-b * torch.sign(u) * torch.log1p(-2.0 * u.abs())).float()
+
+
 def rank_values_f32(w: Workload, rank: int, rows: int | None = None, cols: int | None = None,
                     seed: int = 0, device="cpu", step: int = 0) -> torch.Tensor:
     """float32 values of one rank's tensor before rounding to the 16-bit dtype."""
@@ -122,8 +130,7 @@ def rank_values_f32(w: Workload, rank: int, rows: int | None = None, cols: int |
         pick = torch.rand(shape, generator=g, device=device) < p["p_out"]
         x = torch.where(pick, out, base)
     elif w.dist == "laplace":
-        u = torch.rand(shape, generator=g, device=device) - 0.5
-        x = -p["b"] * torch.sign(u) * torch.log1p(-2.0 * u.abs())
+        x = laplace_from_uniform(torch.rand(shape, generator=g, device=device), p["b"])
     elif w.dist == "normal_drift":
         x = torch.randn(shape, generator=g, device=device) * (p["sigma"] * step_factor(w, step, seed))
     elif w.dist == "normal":
