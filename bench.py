@@ -42,8 +42,9 @@ FALLBACK_HBM_GBS = 6800.0
 # one ncu capture, keyed by (kernel, workload) together with the digest of
 # the CUDA sources it was measured on; a changed source makes it stale (null).
 NCU_TRAFFIC = {
-    # ncu --set full of compress_kernel<bf16, TACO> on gpt_tp (profiles/gpt_tp_step.md)
-    ("taco_compress", "gpt_tp"): {"bytes": 536.919040e6 + 235.449088e6, "src": "18bbfe9475e42d6b"},
+    # ncu dram__bytes_read.sum + dram__bytes_write.sum of one compress_kernel<bf16, TACO>
+    # launch on gpt_tp (profiles/gpt_tp_step.md), valid for the CUDA sources it was taken on
+    ("taco_compress", "gpt_tp"): {"bytes": 536904192 + 231982848, "src": "a85db131db64e393"},
 }
 
 
@@ -390,10 +391,6 @@ def run_qta(args, w):
     evs, e0, e1, _ = timed(fused)
     torch.cuda.synchronize()
     eager_ms = e0.elapsed_time(e1) / args.steps
-    per = {k: [] for k in ("K1", "K2", "K3", "K4", "U")}
-    for e in evs:
-        for j, k in enumerate(per):
-            per[k].append(e[j].elapsed_time(e[j + 1]))
     # the other path (two calls, FP32 sum through HBM), for comparison
     evs2, s2a, s2b, _ = timed(not fused)
     torch.cuda.synchronize()
@@ -460,20 +457,28 @@ def run_qta(args, w):
     value = job_throughput(in_bytes, ms_step, ws)
     peak, peak_kind = _peaks()
     alg = algorithmic_bytes(w)
-    names = {"K1": "taco_compress", "K2": "qar_reduce_requant" if fused else "qar_reduce",
-             "K3": None if fused else "qar_requant", "K4": "taco_decompress"}
-    kern = {}
-    for k in ("K1", "K2", "K3", "K4"):
-        if names[k] is None:
-            continue
-        ms = statistics.mean(per[k])
-        nbytes = alg["K23"] if (k == "K2" and fused) else alg[k]
-        kern[k] = {"call": names[k], "ms": ms, "gb_s": nbytes / (ms * 1e-3) / 1e9,
-                   "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / peak, "algorithmic_bytes": nbytes}
-    kern["U"] = {"call": "taco_update_scale", "ms": statistics.mean(per["U"])}
+
+    def kernel_table(ev_list, fused_path):
+        per_k = {k: [] for k in ("K1", "K2", "K3", "K4", "U")}
+        for e in ev_list:
+            for j, k in enumerate(per_k):
+                per_k[k].append(e[j].elapsed_time(e[j + 1]))
+        names = {"K1": "taco_compress", "K2": "qar_reduce_requant" if fused_path else "qar_reduce",
+                 "K3": None if fused_path else "qar_requant", "K4": "taco_decompress"}
+        table = {}
+        for k in ("K1", "K2", "K3", "K4"):
+            if names[k] is None:
+                continue
+            ms = statistics.mean(per_k[k])
+            nbytes = alg["K23"] if (k == "K2" and fused_path) else alg[k]
+            table[k] = {"call": names[k], "ms": ms, "gb_s": nbytes / (ms * 1e-3) / 1e9,
+                        "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / peak, "algorithmic_bytes": nbytes}
+        table["U"] = {"call": "taco_update_scale", "ms": statistics.mean(per_k["U"])}
+        return table
+
+    kern = kernel_table(evs, fused)
     step_bytes = alg["K1"] + alg["K4"] + (alg["K23"] if fused else alg["K2"] + alg["K3"])
-    k1_ms = statistics.mean(per["K1"])
-    achieved = alg["K1"] / (k1_ms * 1e-3) / 1e9
+    achieved = alg["K1"] / (kern["K1"]["ms"] * 1e-3) / 1e9
     tr = NCU_TRAFFIC.get(("taco_compress", w.name))
     traffic = tr["bytes"] if tr and tr.get("src") == _src_digest() else None
 
@@ -516,7 +521,8 @@ def run_qta(args, w):
         "kernels": kern,
         "step_frac_of_hbm": step_bytes / (ms_step * 1e-3) / 1e9 / peak,
         "other_path": {"path": "qar_reduce + qar_requant" if fused else "qar_reduce_requant",
-                       "ms_per_step": other_ms, "value": in_bytes / (other_ms * 1e-3) / 1e9 * ws},
+                       "ms_per_step": other_ms, "value": in_bytes / (other_ms * 1e-3) / 1e9 * ws,
+                       "kernels": kernel_table(evs2, not fused)},
         "recon": recon,
         "cpu_baseline": cpu,
         "clocks": clk,

@@ -326,18 +326,37 @@ __device__ __forceinline__ void s8x4_to_pairs(uint32_t w, u64& p01, u64& p23)
     p23 = sub2(pk2(__uint_as_float(prmt(wb, magic, 0x7652u)), __uint_as_float(prmt(wb, magic, 0x7653u))), off);
 }
 
-// Eight nibbles of w (element 2k low nibble of byte k, 2k+1 high nibble) as
-// four float pairs (exact).
-__device__ __forceinline__ void u4x8_to_pairs(uint32_t w, u64 (&p)[4])
+// Eight nibbles of w (element i in bits 4i..4i+3) dequantized as
+// f[i] = fmaf(n_i, s, z) with s an fp16 scale and z a widened fp16 zero.
+// A nibble n OR'd under the fp16 pattern 0x6400 is 1024 + n (or 1024 + 16n
+// for an upper nibble of a byte), so one LOP3 yields two fp16 values and
+// one f16x2 subtract (or fma by 1/16, -64) leaves n exactly.  The
+// mixed-precision fma.rn.f32.f16 multiplies two fp16 operands exactly and
+// adds the f32 zero with one rounding: fmaf(n, s, z) bit for bit.
+__device__ __forceinline__ void fma_f16_pair(uint32_t q2, uint16_t s, float z, float& lo, float& hi)
 {
-    const uint32_t even = w & 0x0F0F0F0Fu;          // elements 0,2,4,6 in bytes 0..3
-    const uint32_t odd = (w >> 4) & 0x0F0F0F0Fu;    // elements 1,3,5,7
-    const uint32_t magic = 0x4B000000u;
-    const u64 off = pk2(8388608.0f, 8388608.0f);
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-        p[k] = sub2(pk2(__uint_as_float(prmt(even, magic, 0x7650u + k)), __uint_as_float(prmt(odd, magic, 0x7650u + k))),
-                    off);
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "fma.rn.f32.f16 %0, l, %3, %4;\n\tfma.rn.f32.f16 %1, h, %3, %4;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(q2), "h"(s), "f"(z));
+}
+
+__device__ __forceinline__ void u4x8_dequant(uint32_t w, uint16_t s, float z, float (&f)[8])
+{
+    const uint32_t w8 = w >> 8;
+    uint32_t h04 = (w & 0x000F000Fu) | 0x64006400u;    // 1024 + n0, 1024 + n4
+    uint32_t h15 = (w & 0x00F000F0u) | 0x64006400u;    // 1024 + 16 n1, 1024 + 16 n5
+    uint32_t h26 = (w8 & 0x000F000Fu) | 0x64006400u;   // 1024 + n2, 1024 + n6
+    uint32_t h37 = (w8 & 0x00F000F0u) | 0x64006400u;   // 1024 + 16 n3, 1024 + 16 n7
+    const uint32_t k1024 = 0x64006400u, k16th = 0x2C002C00u, km64 = 0xD400D400u;
+    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(h04) : "r"(k1024));
+    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(h26) : "r"(k1024));
+    asm("fma.rn.f16x2 %0, %0, %1, %2;" : "+r"(h15) : "r"(k16th), "r"(km64));
+    asm("fma.rn.f16x2 %0, %0, %1, %2;" : "+r"(h37) : "r"(k16th), "r"(km64));
+    fma_f16_pair(h04, s, z, f[0], f[4]);
+    fma_f16_pair(h15, s, z, f[1], f[5]);
+    fma_f16_pair(h26, s, z, f[2], f[6]);
+    fma_f16_pair(h37, s, z, f[3], f[7]);
 }
 
 // Round-to-nearest-even to an integer through the FP32 adder: for |y| < 2^22

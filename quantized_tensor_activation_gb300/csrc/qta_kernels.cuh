@@ -221,13 +221,15 @@ __device__ __forceinline__ void load_codes4(const uint8_t* st, int lane, uint32_
 //                      ASYM fmaf(q, s, z)
 // MODE 1 (accumulate): TACO/INT8 v = fmaf(code, s, v)
 //                      ASYM      v = v + fmaf(q, s, z)
+// INT4 takes its scale as the fp16 bits s16 (mixed-precision multiply-add).
 // ptxas contracts a packed multiply into a packed add that consumes it in
 // the same basic block.  The products of MODE 0 are only ever consumed by a
 // fused multiply-add, a scalar add.rn (the first butterfly stage, which is
 // never contracted), a multiply, a conversion or a store, so they keep their
 // own rounding as defined.
 template <int SCH, int MODE>
-__device__ __forceinline__ void dequant_segment(const uint8_t* st, int lane, float s, float z, u64 (&v)[32])
+__device__ __forceinline__ void dequant_segment(const uint8_t* st, int lane, float s, float z, u64 (&v)[32],
+                                                uint16_t s16 = 0)
 {
     const u64 s2 = pk2(s, s);
     const u64 z2 = pk2(z, z);
@@ -242,10 +244,13 @@ __device__ __forceinline__ void dequant_segment(const uint8_t* st, int lane, flo
         load_codes4(st, lane, q);
 #pragma unroll
         for (int w = 0; w < 8; ++w) {
-            u64 p[4];
-            u4x8_to_pairs(q[w], p);
+            float f[8];
+            u4x8_dequant(q[w], s16, z, f);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) asym(w * 4 + k, p[k]);
+            for (int k = 0; k < 4; ++k) {
+                const u64 d = pk2(f[2 * k], f[2 * k + 1]);
+                v[w * 4 + k] = (MODE == 0) ? d : add2(v[w * 4 + k], d);
+            }
         }
     } else {
         uint32_t q[16];
@@ -675,7 +680,7 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
         float s, z;
         cur.decode(s, z);
         u64 v[32];
-        dequant_segment<SCH, 0>(wb + stage * C::IN_BYTES, lane, s, z, v);
+        dequant_segment<SCH, 0>(wb + stage * C::IN_BYTES, lane, s, z, v, static_cast<uint16_t>(cur.raw));
         __syncwarp();
         {
             const int nwt = wt + C::STAGES * W;
@@ -843,10 +848,11 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                 }
                 float s, z;
                 cur[kk].decode(s, z);
+                const uint16_t s16 = static_cast<uint16_t>(cur[kk].raw);
                 if (r == 0)
-                    dequant_segment<SCH, 0>(wb + stage * C::IN_BYTES, lane, s, z, acc);
+                    dequant_segment<SCH, 0>(wb + stage * C::IN_BYTES, lane, s, z, acc, s16);
                 else
-                    dequant_segment<SCH, 1>(wb + stage * C::IN_BYTES, lane, s, z, acc);
+                    dequant_segment<SCH, 1>(wb + stage * C::IN_BYTES, lane, s, z, acc, s16);
                 __syncwarp();
                 if (lane == 0 && unit + C::STAGES < total_units) {
                     fence_proxy_async_smem();
