@@ -85,6 +85,8 @@ def lib():
             L.orc_reduce_requant.argtypes = [i32, i32, i32, vp, vp, vp, vp, i64, i64, i64, i64,
                                              i32, i32, i64, fp, i32, vp, vp, vp]
             L.orc_reduce_requant.restype = i32
+            L.orc_dequant_add.argtypes = [i32, i32, vp, vp, vp, fp, i64, i64, i64, vp, i32, fp]
+            L.orc_dequant_add.restype = i32
             _lib = L
     return _lib
 
@@ -254,3 +256,95 @@ def reduce_requant(scheme: int, B: int, shards, rows: int, cols: int, row_begin:
     if rc:
         raise ValueError(f"oracle reduce_requant rejected the arguments ({rc})")
     return oc, os_, oz
+
+
+# ---------------------------------------------------------------- ring
+def dequant_add(scheme: int, B: int, codes, scales, zeros, state, batch: int, rows: int, cols: int,
+                x: np.ndarray, x_dtype: int) -> np.ndarray:
+    """One ring hop at the receiver: the incoming partial sum dequantized to
+    FP32 as ``decompress`` does it, plus the local tensor x (one FP32 rounding
+    per element).  x: 16-bit bits (uint16) or float32 values."""
+    E = batch * rows * cols
+    x = np.ascontiguousarray(x)
+    assert x.size == E
+    out = np.zeros(E, dtype=np.float32)
+    st = None if state is None else np.ascontiguousarray(state, dtype=np.float32)
+    rc = lib().orc_dequant_add(scheme, B, _ptr(np.ascontiguousarray(codes)),
+                               _ptr(np.ascontiguousarray(scales)),
+                               _ptr(None if zeros is None else np.ascontiguousarray(zeros)),
+                               _ptr(st), batch, rows, cols, _ptr(x), x_dtype, _ptr(out))
+    if rc:
+        raise ValueError(f"oracle dequant_add rejected the arguments ({rc})")
+    return out
+
+
+def _compress_current(scheme: int, B: int, x, dtype: int, rows: int, cols: int):
+    st = np.zeros(2, dtype=np.float32) if scheme == TACO_FP8 else None
+    c, s, z = compress(scheme, B, x, dtype, 1, rows, cols, st, CURRENT)
+    return c, s, z, st
+
+
+def ring_chain(scheme: int, B: int, parts, dtype: int, rows: int, cols: int):
+    """Adder chain [EQuARX Figs. 4-5]: the first rank quantizes its tensor;
+    every following rank dequantizes the incoming partial sum, adds its own
+    tensor in FP32 and requantizes the sum (CURRENT scale for TACO) before it
+    travels on.  parts: the chain's tensors in visiting order.  Returns the
+    quantized partial sum (codes, scales, zeros, state) leaving the last rank."""
+    q = _compress_current(scheme, B, parts[0], dtype, rows, cols)
+    for x in parts[1:]:
+        s = dequant_add(scheme, B, *q, 1, rows, cols, x, dtype)
+        q = _compress_current(scheme, B, s, FP32, rows, cols)
+    return q
+
+
+def ring_chunk_orders(n: int, j: int, semi: bool):
+    """Visiting orders of the chains that end at the owner j of chunk j.
+    Full loop: one chain j+1, j+2, ..., j+n-1.  Semi loop: two chains that
+    meet at the owner, j+h, ..., j+1 and j-(n-1-h), ..., j-1 with h = n // 2."""
+    if not semi:
+        return [[(j + k) % n for k in range(1, n)]]
+    h = n // 2
+    chains = [[(j + k) % n for k in range(h, 0, -1)]]
+    if n - 1 - h > 0:
+        chains.append([(j - k) % n for k in range(n - 1 - h, 0, -1)])
+    return chains
+
+
+def ring_reduce_scatter(scheme: int, B: int, xs, dtype: int, rows: int, cols: int,
+                        semi: bool = False) -> np.ndarray:
+    """Quantized ring reduce-scatter of n = len(xs) tensors [rows, cols]:
+    chunk j (rows j*rows/n .. (j+1)*rows/n) is reduced along the chain(s) of
+    ring_chunk_orders and finished at its owner j, which adds its own chunk
+    to the first chain's partial sum and then the second chain's (each
+    dequantized to FP32 first).  Returns the FP32 sums [rows * cols]."""
+    n = len(xs)
+    assert n >= 2 and rows % n == 0
+    rc = rows // n
+    out = np.zeros(rows * cols, dtype=np.float32)
+    for j in range(n):
+        def chunk(r):
+            return np.ascontiguousarray(np.asarray(xs[r]).reshape(rows, cols)[j * rc:(j + 1) * rc]).reshape(-1)
+        qs = [ring_chain(scheme, B, [chunk(r) for r in order], dtype, rc, cols)
+              for order in ring_chunk_orders(n, j, semi)]
+        s = dequant_add(scheme, B, *qs[0], 1, rc, cols, chunk(j), dtype)
+        for q in qs[1:]:
+            s = dequant_add(scheme, B, *q, 1, rc, cols, s, FP32)
+        out[j * rc * cols:(j + 1) * rc * cols] = s
+    return out
+
+
+def ring_allreduce(scheme: int, B: int, xs, dtype: int, rows: int, cols: int, semi: bool = False,
+                   out_dtype: int = FP32):
+    """Ring reduce-scatter, then the quantized all-gather: every reduced chunk
+    is requantized (CURRENT scale for TACO) and every rank dequantizes the
+    gathered chunks.  Returns (reduce-scatter FP32 sums, all-reduce output in
+    out_dtype), both [rows * cols]."""
+    s = ring_reduce_scatter(scheme, B, xs, dtype, rows, cols, semi)
+    n = len(xs)
+    rc = rows // n
+    y = np.zeros(rows * cols, dtype=np.float32 if out_dtype == FP32 else np.uint16)
+    for j in range(n):
+        part = s[j * rc * cols:(j + 1) * rc * cols]
+        q = _compress_current(scheme, B, part, FP32, rc, cols)
+        y[j * rc * cols:(j + 1) * rc * cols] = decompress(scheme, B, *q, 1, rc, cols, out_dtype)
+    return s, y

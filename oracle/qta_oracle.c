@@ -520,3 +520,21 @@ int orc_reduce_requant(int scheme, int B, int n_ranks, const void* const* codes,
     free(acc);
     return rc;
 }
+
+/* One hop of a ring reduce-scatter [EQuARX] What carries the argument (each
+ * received shard is dequantized to FP32 before it is added; the partial sum
+ * is requantized before it travels on) and Figs. 4-5 (full-loop and
+ * semi-loop adder chains): the incoming quantized partial sum is dequantized
+ * to FP32 exactly as orc_decompress does it (TACO: inverse transform, then
+ * 1/B), and the receiver's own tensor x (bf16, fp16 or fp32) is added with
+ * one FP32 rounding per element.  sum_out: f32 [batch, rows, cols]. */
+int orc_dequant_add(int scheme, int B, const void* codes, const void* scales, const void* zeros,
+                    const float* state, int64_t batch, int64_t rows, int64_t cols, const void* x,
+                    int x_dtype, float* sum_out)
+{
+    int rc = orc_decompress(scheme, B, codes, scales, zeros, state, batch, rows, cols, sum_out, ORC_FP32);
+    if (rc) return rc;
+    int64_t n = batch * rows * cols;
+    for (int64_t e = 0; e < n; ++e) sum_out[e] = sum_out[e] + load_elem(x, x_dtype, e);
+    return 0;
+}

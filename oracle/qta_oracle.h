@@ -14,6 +14,7 @@
  *            Machine Learning Acceleration" (review page): What carries the
  *            argument (block-wise int8, one FP32 scale per 64 entries,
  *            Qp1/Qp2, dequantize to FP32 before adding).
+ *            Figs. 4-5 (full-loop / semi-loop adder chains of the ring).
  *   [FLASH]  "Flash Communication: Reducing Tensor Parallelization Bottleneck
  *            for Fast Large Language Model Inference" (review page): What
  *            carries the argument (asymmetric group-128 quantization, two-step
@@ -81,6 +82,11 @@ int orc_reduce_requant(int scheme, int B, int n_ranks, const void* const* codes,
                        int64_t row_begin, int64_t row_end, int out_scheme, int out_B,
                        int64_t out_batch, float* out_state, int mode, void* out_codes,
                        void* out_scales, void* out_zeros);
+
+/* ---- ring hop: dequantize the incoming partial sum, add the local tensor ---- */
+int orc_dequant_add(int scheme, int B, const void* codes, const void* scales, const void* zeros,
+                    const float* state, int64_t batch, int64_t rows, int64_t cols, const void* x,
+                    int x_dtype, float* sum_out);
 
 #ifdef __cplusplus
 }
