@@ -237,6 +237,55 @@ def algorithmic_bytes(w):
     return {"K1": k1, "K2": k2, "K3": k3, "K23": k23, "K4": k4}
 
 
+def ring_report(qta, w, x, steps: int):
+    """EQuARX full-loop and semi-loop adder chains (ring reduce-scatter with
+    the partial sum requantized at every hop, then the quantized all-gather)
+    over the workload's ranks: time of the reduce-scatter chains (CUDA events,
+    eager launches) and mean squared errors against the float64 sums."""
+    import torch
+    from quantized_tensor_activation_gb300 import ring
+
+    N, R, C = x.shape
+    d = qta.desc(w.scheme, w.block, R, C)
+    rc = R // N
+    exact = x.double().sum(dim=0)
+    out = {"ranks": N, "shape": [R, C], "scheme": w.scheme, "block": w.block,
+           "note": "chunk j owned by rank j; CURRENT scale per hop for TACO; MSE vs the float64 sum"}
+    for semi in (False, True):
+        name = "semi_loop" if semi else "full_loop"
+        ring.reduce_scatter(d, x, semi)                      # warm-up
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            ring.reduce_scatter(d, x, semi)
+        b.record()
+        torch.cuda.synchronize()
+        s, y = ring.allreduce(d, x, semi, torch.float32)
+        e_rs = s.double() - exact
+        e_ar = y.double() - exact
+        out[name] = {"reduce_scatter_ms": a.elapsed_time(b) / steps,
+                     "requantizations_per_chunk": max(len(c) for c in ring.chunk_orders(N, 0, semi)),
+                     "reduce_scatter_mse": float((e_rs * e_rs).mean()),
+                     "allreduce_mse": float((e_ar * e_ar).mean())}
+        del s, y, e_rs, e_ar
+    # error of the full-loop partial sums after each hop
+    parts = []
+    ring.reduce_scatter(d, x, False, hop_partials=parts)
+    per_hop = []
+    for k, p in enumerate(parts):
+        err = 0.0
+        for j in range(N):
+            ranks = [(j + i) % N for i in range(1, k + 2)]
+            ex = x[ranks, j * rc:(j + 1) * rc].double().sum(dim=0)
+            e = p[j * rc:(j + 1) * rc].double() - ex
+            err += float((e * e).sum())
+        per_hop.append(err / (R * C))
+    out["full_loop"]["mse_after_hop"] = per_hop
+    del parts
+    assert qta.qta_device_error() == 0
+    return out
+
+
 def run_qta(args, w):
     import torch
 
@@ -500,6 +549,8 @@ def run_qta(args, w):
                      "note": "output of the timed step vs the float64 sum of the 16-bit inputs"}
             del exact, err, e0, y0
 
+    ring_rep = ring_report(qta, w, x, 3) if args.ring else None
+
     cpu = None
     if not args.no_cpu_baseline and ws == 1:
         rows = args.cpu_rows or w.rows
@@ -524,6 +575,7 @@ def run_qta(args, w):
                        "ms_per_step": other_ms, "value": in_bytes / (other_ms * 1e-3) / 1e9 * ws,
                        "kernels": kernel_table(evs2, not fused)},
         "recon": recon,
+        "ring": ring_rep,
         "cpu_baseline": cpu,
         "clocks": clk,
         "e2e": e2e,
@@ -548,6 +600,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="skip the nvidia-smi clock window (profiling runs)")
     ap.add_argument("--no-recon", action="store_true", help="skip the reconstruction-error report")
+    ap.add_argument("--ring", action="store_true",
+                    help="add the ring adder-chain report (full loop / semi loop) of the workload")
     ap.add_argument("--no-graph", action="store_true", help="launch the timed steps eagerly instead of as a CUDA graph")
     ap.add_argument("--path", default="fused", choices=["fused", "split"],
                     help="fused: qar_reduce_requant; split: qar_reduce then qar_requant (FP32 sum in HBM)")

@@ -191,6 +191,29 @@ qta_status qar_reduce_requant(const qta_desc* d, const qta_qtensor* shards, int3
 qta_status qar_requant(const qta_desc* d, const float* sum, const qta_qtensor* out,
                        int32_t mode, qta_stream_t stream);
 
+/* qar_dequant_add -- one hop of a quantized ring reduce-scatter at the
+ * receiving rank [EQuARX What carries the argument: every received shard is
+ * dequantized to FP32 before the addition; Figs. 4-5: the full-loop and
+ * semi-loop adder chains are sequences of such hops].  The incoming partial
+ * sum `in` (described by `d`, any batch) is dequantized exactly as
+ * taco_decompress dequantizes it to FP32 (TACO: inverse butterfly, then
+ * 1/B), and the receiver's own tensor x is added, one FP32 rounding per
+ * element.  x: device [batch, rows, cols] of x_dtype (bf16, fp16 or fp32),
+ * 16-byte aligned; sum_out: device f32 of the same shape, 16-byte aligned,
+ * not overlapping x or `in`.  Caller-owned buffers; errors as for the other
+ * calls. */
+qta_status qar_dequant_add(const qta_desc* d, const qta_qtensor* in, const void* x,
+                           int32_t x_dtype, float* sum_out, qta_stream_t stream);
+
+/* qar_dequant_add_requant -- the same hop with the partial sum requantized
+ * before it travels on, in one kernel: bit-identical to qar_dequant_add
+ * followed by qar_requant with `d` (same scheme, block and shape as the
+ * incoming tensor; `mode` is the scale mode of a TACO output, whose state is
+ * out->state).  `out` must not overlap `in` or x. */
+qta_status qar_dequant_add_requant(const qta_desc* d, const qta_qtensor* in, const void* x,
+                                   int32_t x_dtype, const qta_qtensor* out, int32_t mode,
+                                   qta_stream_t stream);
+
 /* taco_update_scale -- end-of-step update of the dual-scale state of
  * n_tensors tensors [TACO Core claim: stability across training steps]:
  * S = amax/448 (S = 1 if zero, non-finite or below FLT_MIN), amax = 0.

@@ -75,11 +75,14 @@ def lib():
         L.qar_reduce.argtypes = [PD, PQ, i32, i64, i64, vp, vp]
         L.qar_requant.argtypes = [PD, vp, PQ, i32, vp]
         L.qar_reduce_requant.argtypes = [PD, PQ, i32, i64, i64, PD, PQ, i32, vp]
+        L.qar_dequant_add.argtypes = [PD, PQ, vp, i32, vp, vp]
+        L.qar_dequant_add_requant.argtypes = [PD, PQ, vp, i32, PQ, i32, vp]
         L.taco_update_scale.argtypes = [vp, i64, vp]
         L.qta_copy.argtypes = [vp, vp, sz, vp]
         L.qta_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
         for name in ("taco_compress", "taco_decompress", "qar_reduce", "qar_requant", "qar_reduce_requant",
-                     "taco_update_scale", "qta_copy", "qta_device_error"):
+                     "qar_dequant_add", "qar_dequant_add_requant", "taco_update_scale", "qta_copy",
+                     "qta_device_error"):
             getattr(L, name).restype = ctypes.c_int
         L.qta_status_string.argtypes = [ctypes.c_int]
         L.qta_status_string.restype = ctypes.c_char_p
@@ -212,6 +215,20 @@ def qar_requant(d: Desc, sum_in, out: QTensor, mode: int = SCALE_DELAYED, stream
     q = out.c()
     _check("qar_requant", lib().qar_requant(ctypes.byref(d), _ptr(sum_in), ctypes.byref(q), mode,
                                             _stream(stream)))
+
+
+def qar_dequant_add(d: Desc, q_in: QTensor, x, x_dtype: int, sum_out, stream=None) -> None:
+    qi = q_in.c()
+    _check("qar_dequant_add", lib().qar_dequant_add(ctypes.byref(d), ctypes.byref(qi), _ptr(x), x_dtype,
+                                                    _ptr(sum_out), _stream(stream)))
+
+
+def qar_dequant_add_requant(d: Desc, q_in: QTensor, x, x_dtype: int, out: QTensor, mode: int = SCALE_DELAYED,
+                            stream=None) -> None:
+    qi, qo = q_in.c(), out.c()
+    _check("qar_dequant_add_requant", lib().qar_dequant_add_requant(ctypes.byref(d), ctypes.byref(qi), _ptr(x),
+                                                                    x_dtype, ctypes.byref(qo), mode,
+                                                                    _stream(stream)))
 
 
 def taco_update_scale(state, n_tensors: int, stream=None) -> None:

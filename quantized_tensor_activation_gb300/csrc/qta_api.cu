@@ -470,6 +470,74 @@ qta_status qar_reduce(const qta_desc* d, const qta_qtensor* shards, int32_t n_ra
     return cuda_status(launch_reduce(d->scheme, p, grid, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// Shared implementation of qar_dequant_add (sum_out) and
+// qar_dequant_add_requant (out).
+static qta_status accum_impl(const qta_desc* d, const qta_qtensor* in, const void* x, int32_t x_dtype,
+                             float* sum_out, const qta_qtensor* out, int32_t mode, qta_stream_t stream)
+{
+    qta_status st = check_desc(d);
+    if (st != QTA_OK) return st;
+    if (x_dtype != QTA_BF16 && x_dtype != QTA_FP16 && x_dtype != QTA_FP32) return QTA_ERR_UNSUPPORTED;
+    const bool requant = out != nullptr;
+    if (requant && d->scheme == QTA_TACO_FP8 && mode != QTA_SCALE_DELAYED && mode != QTA_SCALE_CURRENT)
+        return QTA_ERR_INVALID_ARG;
+    if (n_elems(d) == 0) return QTA_OK;
+    if (!x || (!requant && !sum_out)) return QTA_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || (!requant && !aligned(sum_out, 16))) return QTA_ERR_ALIGNMENT;
+    if ((st = check_qtensor(d, in)) != QTA_OK) return st;
+    if (requant && (st = check_qtensor(d, out)) != QTA_OK) return st;
+    if (!encoder_ready()) return QTA_ERR_CUDA;
+    int sms = 0, smem_sm = 0;
+    unsigned int* err = nullptr;
+    if (device_info(&sms, &smem_sm, &err) != cudaSuccess) return QTA_ERR_CUDA;
+
+    const int64_t segs = n_elems(d) / 64;
+    AccumParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (!map_codes(&p.in_map, d->scheme, in->codes, segs)) return QTA_ERR_CUDA;
+    if (!map_values(&p.x_map, x_dtype, x, segs)) return QTA_ERR_CUDA;
+    if (requant ? !map_codes(&p.out_map, d->scheme, out->codes, segs) : !map_f32(&p.out_map, sum_out, segs))
+        return QTA_ERR_CUDA;
+    p.scales = in->scales;
+    p.zeros = in->zeros;
+    p.state = in->state;
+    p.err = err;
+    p.M = static_cast<int>(segs);
+    p.n_warp_tiles = static_cast<int>((segs + 31) / 32);
+    p.lanes_per_block = lanes_of(d);
+    p.lanes_log2 = log2i(p.lanes_per_block);
+    p.inv_block = 1.0f / static_cast<float>(d->block);
+    p.seg_per_tensor = make_fastdiv(static_cast<uint32_t>(d->rows * d->cols / 64));
+    if (requant) {
+        p.q_scales = out->scales;
+        p.q_zeros = out->zeros;
+        p.q_state = out->state;
+    }
+    const int grid = grid_for(p.n_warp_tiles, accum_warps(x_dtype, requant), accum_smem(x_dtype, requant), sms,
+                              smem_sm);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (requant && d->scheme == QTA_TACO_FP8 && mode == QTA_SCALE_CURRENT) {
+        cudaError_t e = launch_state(out->state, d->batch, STATE_RESET_AMAX, s);
+        if (e == cudaSuccess) e = launch_accum(d->scheme, x_dtype, true, true, p, grid, s);
+        if (e == cudaSuccess) e = launch_state(out->state, d->batch, STATE_SET_SCALE, s);
+        if (e != cudaSuccess) return QTA_ERR_CUDA;
+    }
+    return cuda_status(launch_accum(d->scheme, x_dtype, requant, false, p, grid, s));
+}
+
+qta_status qar_dequant_add(const qta_desc* d, const qta_qtensor* in, const void* x, int32_t x_dtype, float* sum_out,
+                           qta_stream_t stream)
+{
+    return accum_impl(d, in, x, x_dtype, sum_out, nullptr, QTA_SCALE_DELAYED, stream);
+}
+
+qta_status qar_dequant_add_requant(const qta_desc* d, const qta_qtensor* in, const void* x, int32_t x_dtype,
+                                   const qta_qtensor* out, int32_t mode, qta_stream_t stream)
+{
+    if (!out) return QTA_ERR_INVALID_ARG;
+    return accum_impl(d, in, x, x_dtype, nullptr, out, mode, stream);
+}
+
 qta_status taco_update_scale(float* state, int64_t n_tensors, qta_stream_t stream)
 {
     if (n_tensors < 0) return QTA_ERR_INVALID_ARG;

@@ -80,6 +80,27 @@ struct ReduceParams {
     FastDiv q_seg_per_tensor;
 };
 
+// One ring hop: the incoming quantized partial sum plus the local tensor x,
+// stored as an FP32 sum or requantized with the incoming scheme and block.
+struct AccumParams {
+    CUtensorMap in_map;   // incoming codes, as the decompress in_map
+    CUtensorMap x_map;    // local tensor, as the compress in_map
+    CUtensorMap out_map;  // fp32 sum {32,2,M}, or the requantized codes
+    const void* scales;
+    const void* zeros;
+    const float* state;
+    unsigned int* err;
+    int M;
+    int n_warp_tiles;
+    int lanes_per_block;
+    int lanes_log2;
+    float inv_block;
+    FastDiv seg_per_tensor;
+    void* q_scales;       // requantization outputs
+    void* q_zeros;
+    float* q_state;
+};
+
 // ------------------------------------------------------------ configuration
 // Per kernel family: warps per CTA (one CTA per SM; __launch_bounds__ caps
 // the registers at 64K / threads), stages of the per-warp TMA ring, and
@@ -129,6 +150,22 @@ struct ReduceCfg {
     static constexpr int OUT_BYTES = 32 * OUT_SEG;
     static constexpr int OUT_BUFS = 1;
     static constexpr int WARP_SMEM = STAGES * IN_BYTES + OUT_BUFS * OUT_BYTES;
+    static constexpr int SMEM = WARPS * WARP_SMEM + WARPS * STAGES * 8 + 1024;
+};
+
+// Ring hop: a stage holds a warp tile of incoming codes (2 KB slot) and of
+// the local tensor (4 KB 16-bit, 8 KB fp32); OSCH as for ReduceCfg.
+template <int XIN, int OSCH>
+struct AccumCfg {
+    static constexpr bool F32X = XIN == IN_FP32;
+    static constexpr bool F32O = OSCH == OUT_F32;
+    static constexpr int WARPS = (F32X && F32O) ? 6 : 8;
+    static constexpr int STAGES = 2;
+    static constexpr int IN_BYTES = 32 * 64;
+    static constexpr int X_BYTES = 32 * (F32X ? 256 : 128);
+    static constexpr int STAGE_BYTES = IN_BYTES + X_BYTES;
+    static constexpr int OUT_BYTES = 32 * (F32O ? 256 : 64);
+    static constexpr int WARP_SMEM = STAGES * STAGE_BYTES + OUT_BYTES;
     static constexpr int SMEM = WARPS * WARP_SMEM + WARPS * STAGES * 8 + 1024;
 };
 
@@ -229,7 +266,7 @@ __device__ __forceinline__ void load_codes4(const uint8_t* st, int lane, uint32_
 // own rounding as defined.
 template <int SCH, int MODE>
 __device__ __forceinline__ void dequant_segment(const uint8_t* st, int lane, float s, float z, u64 (&v)[32],
-                                                uint16_t s16 = 0)
+                                                uint16_t s16)
 {
     const u64 s2 = pk2(s, s);
     const u64 z2 = pk2(z, z);
@@ -901,6 +938,131 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
         } else {
             uint32_t ow[16];
             quant.template run<AMAX_ONLY>(acc, qo, wt * 32, lane, ow, direct);
+            if constexpr (!AMAX_ONLY) store_codes<OSCH, 1>(outb, &p.out_map, wt * 32, lane, ow);
+        }
+    }
+    if constexpr (OSCH != OUT_F32) quant.finish(qo, lane);
+    if (lane == 0) {
+        bulk_wait_all();
+        if (aborted) drain_ring(bars, C::STAGES, stage, phase, p.err);
+    }
+}
+
+// ------------------------------------------------------------ ring hop
+// qar_dequant_add (OSCH = OUT_F32) and qar_dequant_add_requant (OSCH = SCH;
+// AMAX_ONLY = its CURRENT-mode pre-pass): the incoming codes are dequantized
+// exactly as taco_decompress dequantizes them to FP32 (TACO: inverse
+// butterfly, then 1/B), the local tensor is added with one scalar FP32
+// rounding per element, and the sum is stored, or quantized exactly as
+// qar_requant quantizes an FP32 input.
+template <int SCH, int XIN, int OSCH, bool AMAX_ONLY>
+__global__ void __launch_bounds__(AccumCfg<XIN, OSCH>::WARPS * 32, 1)
+accum_kernel(const __grid_constant__ AccumParams p)
+{
+    using C = AccumCfg<XIN, OSCH>;
+    constexpr int CODE_BYTES = 32 * ((SCH == S_ASYM4) ? 32 : 64);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = aligned_smem(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t* wb = smem + warp * C::WARP_SMEM;
+    uint8_t* outb = wb + C::STAGES * C::STAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::WARPS * C::WARP_SMEM) + warp * C::STAGES;
+    const int W = gridDim.x * C::WARPS;
+    const int first = blockIdx.x * C::WARPS + warp;
+    auto issue = [&](int s, int wt) {
+        uint8_t* st = wb + s * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&bars[s], CODE_BYTES + C::X_BYTES);
+        tma_load_2d(st, &p.in_map, 0, wt * 32, &bars[s]);
+        if constexpr (XIN == IN_FP32) {
+            tma_load_3d(st + C::IN_BYTES, &p.x_map, 0, 0, wt * 32, &bars[s]);
+            tma_load_3d(st + C::IN_BYTES + 4096, &p.x_map, 0, 1, wt * 32, &bars[s]);
+        } else {
+            tma_load_2d(st + C::IN_BYTES, &p.x_map, 0, wt * 32, &bars[s]);
+        }
+    };
+    if (lane == 0) {
+        for (int s = 0; s < C::STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_barrier_init();
+    }
+    pdl_wait();
+    pdl_trigger();
+    if (lane == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            const int wt = first + s * W;
+            if (wt >= p.n_warp_tiles) break;
+            issue(s, wt);
+        }
+    }
+    __syncwarp();
+    const int L = p.lanes_per_block;
+    const QuantOut qo{p.q_scales, p.q_zeros, p.q_state, p.M, p.lanes_per_block, p.lanes_log2, p.seg_per_tensor};
+    Quantizer<(OSCH == OUT_F32) ? S_TACO : OSCH> quant;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool aborted = false;
+    SegMeta<SCH> meta;   // metadata of the next warp tile, fetched one tile ahead
+    if (first < p.n_warp_tiles && first * 32 + lane < p.M)
+        meta.load(p.scales, p.zeros, p.state, first * 32 + lane, p.lanes_log2, p.seg_per_tensor);
+    for (int wt = first; wt < p.n_warp_tiles; wt += W) {
+        SegMeta<SCH> cur = meta;
+        {
+            const int gn = (wt + W) * 32 + lane;
+            if (wt + W < p.n_warp_tiles && gn < p.M)
+                meta.load(p.scales, p.zeros, p.state, gn, p.lanes_log2, p.seg_per_tensor);
+        }
+        if constexpr (OSCH != OUT_F32) quant.begin(qo, wt * 32, lane);
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[stage], phase, p.err));
+        if (!ok) {
+            aborted = true;
+            break;
+        }
+        float s, z;
+        cur.decode(s, z);
+        u64 v[32], xv[32];
+        const uint8_t* st = wb + stage * C::STAGE_BYTES;
+        dequant_segment<SCH, 0>(st, lane, s, z, v, static_cast<uint16_t>(cur.raw));
+        load_segment<XIN>(st + C::IN_BYTES, lane, xv);
+        __syncwarp();
+        {
+            const int nwt = wt + C::STAGES * W;
+            if (nwt < p.n_warp_tiles && lane == 0) {
+                fence_proxy_async_smem();
+                issue(stage, nwt);
+            }
+        }
+        if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+        }
+        if constexpr (SCH == S_TACO) {
+            fwht64_local(v);
+            fwht_cross(v, L, lane);
+        }
+        // times 1/B (TACO), then the local tensor with one rounding per
+        // element: scalar rounded operations, which are never contracted
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            float2 a = up2(v[j]);
+            const float2 b = up2(xv[j]);
+            if constexpr (SCH == S_TACO) {
+                a.x = __fmul_rn(a.x, p.inv_block);
+                a.y = __fmul_rn(a.y, p.inv_block);
+            }
+            v[j] = pk2(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y));
+        }
+        if constexpr (OSCH == OUT_F32) {
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+            store_segment<IN_FP32>(outb, lane, v);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                store_out16or32<IN_FP32>(&p.out_map, outb, wt * 32);
+                bulk_commit();
+            }
+        } else {
+            uint32_t ow[16];
+            quant.template run<AMAX_ONLY>(v, qo, wt * 32, lane, ow);
             if constexpr (!AMAX_ONLY) store_codes<OSCH, 1>(outb, &p.out_map, wt * 32, lane, ow);
         }
     }

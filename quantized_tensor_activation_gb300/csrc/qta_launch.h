@@ -13,11 +13,13 @@ int compress_smem(int in_kind, int scheme);
 int decompress_smem(int scheme, int out_kind);
 int reduce_smem(int scheme, int out_scheme);   // out_scheme: OUT_F32 or the requant scheme
 bool reduce_requant_supported(int scheme, int out_scheme);
+int accum_smem(int x_kind, bool requant);
 
 // Warps per CTA of each kernel family.
 int compress_warps(int in_kind);
 int decompress_warps(int out_kind);
 int reduce_warps();
+int accum_warps(int x_kind, bool requant);
 
 cudaError_t launch_compress(int in_kind, int scheme, bool amax_only, const CompressParams& p, int grid,
                             cudaStream_t stream);
@@ -26,6 +28,8 @@ cudaError_t launch_decompress(int scheme, int out_kind, const DecompressParams& 
 cudaError_t launch_reduce(int scheme, const ReduceParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_reduce_requant(int scheme, int out_scheme, bool amax_only, const ReduceParams& p, int grid,
                                   cudaStream_t stream);
+cudaError_t launch_accum(int scheme, int x_kind, bool requant, bool amax_only, const AccumParams& p, int grid,
+                         cudaStream_t stream);
 cudaError_t launch_state(float* state, long long n, int op, cudaStream_t stream);
 cudaError_t launch_copy(const void* src, void* dst, size_t bytes, int grid, cudaStream_t stream);
 

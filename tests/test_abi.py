@@ -126,3 +126,24 @@ def test_reduce_requant_argument_checks(L):
     assert f(D(0, 128, 8, 256), arr, 17, 0, 8, D(0, 128, 8, 256), out, 0, None) == UNS
     assert f(D(2, 128, 8, 256), arr, 2, 0, 8, D(3, 128, 8, 256),
              ctypes.byref(qta.QTensorC(16, 16, None, 16)), 0, None) == INV                # zeros needed
+
+
+def test_ring_hop_argument_checks(L):
+    D = lambda *a: ctypes.byref(qta.desc(*a))
+    q = ctypes.byref(qta.QTensorC(16, 16, 16, 16))
+    OK, INV, ALN, UNS = qta.QTA_OK, qta.QTA_ERR_INVALID_ARG, qta.QTA_ERR_ALIGNMENT, qta.QTA_ERR_UNSUPPORTED
+    f, g = L.qar_dequant_add, L.qar_dequant_add_requant
+    assert f(None, q, 16, 0, 16, None) == INV
+    assert f(D(0, 96, 4, 192), q, 16, 0, 16, None) == UNS
+    assert f(D(0, 128, 4, 128), q, 16, 5, 16, None) == UNS          # x dtype
+    assert f(D(0, 128, 4, 128), q, None, 0, 16, None) == INV
+    assert f(D(0, 128, 4, 128), q, 16, 0, None, None) == INV         # no sum buffer
+    assert f(D(0, 128, 4, 128), q, 24, 0, 16, None) == ALN
+    assert f(D(0, 128, 4, 128), q, 16, 0, 40, None) == ALN
+    assert f(D(0, 128, 4, 128), None, 16, 0, 16, None) == INV
+    assert f(D(0, 128, 4, 128), ctypes.byref(qta.QTensorC(16, 16, 16, None)), 16, 0, 16, None) == INV
+    assert f(D(0, 128, 0, 128), None, None, 0, None, None) == OK     # empty
+    assert g(D(0, 128, 4, 128), q, 16, 0, None, 0, None) == INV      # no output tensor
+    assert g(D(0, 128, 4, 128), q, 16, 0, q, 9, None) == INV         # TACO scale mode
+    assert g(D(2, 128, 4, 256), q, 16, 1, ctypes.byref(qta.QTensorC(16, 16, None, 16)), 0, None) == INV
+    assert g(D(1, 64, 4, 128), q, 16, 2, ctypes.byref(qta.QTensorC(8, 16, 16, 16)), 0, None) == ALN
