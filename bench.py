@@ -446,6 +446,20 @@ def run_qta(args, w):
     other_ms = s2a.elapsed_time(s2b) / args.steps
     assert qta.qta_device_error() == 0
 
+    # the same step with every call capped to a number of SMs (eager launches)
+    sweep_raw = []
+    if args.sm_sweep:
+        for n_sms in [int(v) for v in args.sm_sweep.split(",")]:
+            for dd in (d_in, d_sh, d_g):
+                dd.max_sms = n_sms
+            timed(fused)
+            evs3, s3a, s3b, _ = timed(fused)
+            torch.cuda.synchronize()
+            sweep_raw.append((n_sms, s3a.elapsed_time(s3b) / args.steps, evs3))
+        for dd in (d_in, d_sh, d_g):
+            dd.max_sms = 0
+        assert qta.qta_device_error() == 0
+
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -550,6 +564,15 @@ def run_qta(args, w):
             del exact, err, e0, y0
 
     ring_rep = ring_report(qta, w, x, 3) if args.ring else None
+    sm_sweep = None
+    if sweep_raw:
+        sm_sweep = []
+        for n_sms, ms, evs3 in sweep_raw:
+            t = kernel_table(evs3, fused)
+            sm_sweep.append({"max_sms": n_sms, "eager_ms_per_step": ms,
+                             "value": in_bytes / (ms * 1e-3) / 1e9 * ws,
+                             "kernels_ms": {k: v["ms"] for k, v in t.items()},
+                             "kernels_frac_of_hbm": {k: v["frac_of_hbm"] for k, v in t.items() if "frac_of_hbm" in v}})
 
     cpu = None
     if not args.no_cpu_baseline and ws == 1:
@@ -576,6 +599,7 @@ def run_qta(args, w):
                        "kernels": kernel_table(evs2, not fused)},
         "recon": recon,
         "ring": ring_rep,
+        "sm_sweep": sm_sweep,
         "cpu_baseline": cpu,
         "clocks": clk,
         "e2e": e2e,
@@ -600,6 +624,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="skip the nvidia-smi clock window (profiling runs)")
     ap.add_argument("--no-recon", action="store_true", help="skip the reconstruction-error report")
+    ap.add_argument("--sm-sweep", default="",
+                    help="comma-separated SM counts: time the step with every call capped to that many SMs")
     ap.add_argument("--ring", action="store_true",
                     help="add the ring adder-chain report (full loop / semi loop) of the workload")
     ap.add_argument("--no-graph", action="store_true", help="launch the timed steps eagerly instead of as a CUDA graph")

@@ -92,15 +92,25 @@ typedef enum {
  *           state[1] with max().
  *  CURRENT: first compute this tensor's amax, set S = amax/448 (S = 1 if
  *           that is zero, non-finite or below FLT_MIN), state[1] = amax,
- *           then compress with it (two passes over the input). */
-typedef enum { QTA_SCALE_DELAYED = 0, QTA_SCALE_CURRENT = 1 } qta_scale_mode;
+ *           then compress with it (two passes over the input).
+ * ROUND_UP: a flag OR'ed into either mode.  The block scale r_b becomes
+ *           the smallest E4M3 value not below a_b/(448 S) instead of the
+ *           nearest one, so y/s_b never exceeds 448 while S covers the tensor
+ *           (no saturated codes, coarser steps) -- the rounding alternative
+ *           to [TACO] Fig. 7's dual scale. */
+typedef enum { QTA_SCALE_DELAYED = 0, QTA_SCALE_CURRENT = 1, QTA_SCALE_ROUND_UP = 4 } qta_scale_mode;
 
 typedef struct {
-    int32_t scheme; /* qta_scheme */
-    int32_t block;  /* see qta_scheme */
-    int64_t batch;  /* independent tensors, each with its own per-tensor scale */
+    int32_t scheme;  /* qta_scheme */
+    int32_t block;   /* see qta_scheme */
+    int64_t batch;   /* independent tensors, each with its own per-tensor scale */
     int64_t rows;
-    int64_t cols;   /* cols % block == 0 */
+    int64_t cols;    /* cols % block == 0 */
+    int32_t max_sms; /* SMs a call may occupy (one CTA each); 0 or >= the GPU's
+                        count: all.  Leaving SMs free lets concurrent compute
+                        kernels overlap the codec [FLASH: the communication
+                        kernel runs on a subset of the SMs].  For calls with
+                        two descriptors, the input descriptor's value counts. */
 } qta_desc;
 
 /* A quantized tensor (device pointers).
@@ -213,6 +223,17 @@ qta_status qar_dequant_add(const qta_desc* d, const qta_qtensor* in, const void*
 qta_status qar_dequant_add_requant(const qta_desc* d, const qta_qtensor* in, const void* x,
                                    int32_t x_dtype, const qta_qtensor* out, int32_t mode,
                                    qta_stream_t stream);
+
+/* qta_sq_error -- *out = sum over i < n of (a_i - b_i)^2, accumulated in
+ * FP64: the squared reconstruction error of a compress -> decompress round
+ * trip, with which a block size is chosen per tensor [TACO Core claim:
+ * data-driven reshaping -- the block size whose round trip loses least].
+ * a: device [n] of a_dtype (bf16, fp16 or fp32), b: device f32 [n], both
+ * 4-byte aligned; out: device double, 8-byte aligned, overwritten (the
+ * order of the FP64 partial sums is not fixed: the result may differ in
+ * the last bits between calls). */
+qta_status qta_sq_error(const void* a, int32_t a_dtype, const float* b, int64_t n, double* out,
+                        qta_stream_t stream);
 
 /* taco_update_scale -- end-of-step update of the dual-scale state of
  * n_tensors tensors [TACO Core claim: stability across training steps]:

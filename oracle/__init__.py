@@ -30,6 +30,7 @@ _LIB = os.path.join(_BUILD, "liboracle.so")
 BF16, FP16, FP32 = 0, 1, 2
 TACO_FP8, INT8_SYM, INT4_ASYM, INT8_ASYM = 0, 1, 2, 3
 DELAYED, CURRENT = 0, 1
+ROUND_UP = 4          # OR into DELAYED / CURRENT: block scales rounded up (TACO)
 
 _lock = threading.Lock()
 _lib = None

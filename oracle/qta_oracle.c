@@ -198,9 +198,16 @@ void orc_taco_update_scale(float* state, int64_t batch)
  * R4: block scale r_b = E4M3(a_b / (448 S)) stored as one E4M3 byte relative
  *     to the per-tensor FP32 scale S; s_b = S * r_b; codes E4M3(y * 1/s_b). */
 /* Dual-scale FP8 quantization of nblk transformed blocks y (R4, R5). */
+/* mode: ORC_DELAYED or ORC_CURRENT, optionally OR'ed with ORC_ROUND_UP: the
+ * block scale r_b is then the smallest E4M3 value not below a_b / (448 S)
+ * instead of the nearest one, so that y / s_b stays within 448 whenever S
+ * covers the tensor (no saturated codes; SURVEY's "round r_b up" variant of
+ * [TACO] Fig. 7's dual scale). */
 static void taco_quantize_blocks(const float* y, int64_t nblk, int B, float* st, int mode,
                                  uint8_t* codes, uint8_t* scales)
 {
+    const int round_up = (mode & ORC_ROUND_UP) != 0;
+    mode &= ~ORC_ROUND_UP;
     if (mode == ORC_CURRENT) {
         float amax = 0.0f;
         for (int64_t i = 0; i < nblk * B; ++i) amax = fmaxf(amax, fabsf(y[i]));
@@ -215,7 +222,9 @@ static void taco_quantize_blocks(const float* y, int64_t nblk, int B, float* st,
         float a = 0.0f;
         for (int i = 0; i < B; ++i) a = fmaxf(a, fabsf(yb[i]));
         amax_t = fmaxf(amax_t, a);
-        uint8_t r = orc_e4m3_encode(a * tinv);
+        const float ratio = a * tinv;
+        uint8_t r = orc_e4m3_encode(ratio);
+        if (round_up && r < 0x7E && orc_e4m3_decode(r) < ratio) r = (uint8_t)(r + 1);
         if (r == 0 && a > 0.0f) r = 0x01;
         float sb = S * orc_e4m3_decode(r);
         float inv = (sb > 0.0f) ? 1.0f / sb : 0.0f;

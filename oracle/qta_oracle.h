@@ -40,7 +40,7 @@ extern "C" {
 
 enum { ORC_BF16 = 0, ORC_FP16 = 1, ORC_FP32 = 2 };
 enum { ORC_TACO_FP8 = 0, ORC_INT8_SYM = 1, ORC_INT4_ASYM = 2, ORC_INT8_ASYM = 3 };
-enum { ORC_DELAYED = 0, ORC_CURRENT = 1 };
+enum { ORC_DELAYED = 0, ORC_CURRENT = 1, ORC_ROUND_UP = 4 };
 
 /* ---- number formats ---- */
 uint8_t  orc_e4m3_encode(float v);

@@ -23,6 +23,7 @@ QTA_OK, QTA_ERR_INVALID_ARG, QTA_ERR_ALIGNMENT, QTA_ERR_UNSUPPORTED, QTA_ERR_CUD
 BF16, FP16, FP32 = 0, 1, 2
 TACO_FP8, INT8_SYM_B64, INT4_ASYM_G128, INT8_ASYM_G128 = 0, 1, 2, 3
 SCALE_DELAYED, SCALE_CURRENT = 0, 1
+SCALE_ROUND_UP = 4    # OR into a TACO scale mode: block scales rounded up
 MAX_RANKS = 16
 
 SCHEMES = {"taco_fp8": TACO_FP8, "int8_sym": INT8_SYM_B64, "int4_asym": INT4_ASYM_G128,
@@ -37,7 +38,7 @@ class QtaError(RuntimeError):
 
 class Desc(ctypes.Structure):
     _fields_ = [("scheme", ctypes.c_int32), ("block", ctypes.c_int32), ("batch", ctypes.c_int64),
-                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64)]
+                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("max_sms", ctypes.c_int32)]
 
 
 class QTensorC(ctypes.Structure):
@@ -77,11 +78,12 @@ def lib():
         L.qar_reduce_requant.argtypes = [PD, PQ, i32, i64, i64, PD, PQ, i32, vp]
         L.qar_dequant_add.argtypes = [PD, PQ, vp, i32, vp, vp]
         L.qar_dequant_add_requant.argtypes = [PD, PQ, vp, i32, PQ, i32, vp]
+        L.qta_sq_error.argtypes = [vp, i32, vp, i64, vp, vp]
         L.taco_update_scale.argtypes = [vp, i64, vp]
         L.qta_copy.argtypes = [vp, vp, sz, vp]
         L.qta_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
         for name in ("taco_compress", "taco_decompress", "qar_reduce", "qar_requant", "qar_reduce_requant",
-                     "qar_dequant_add", "qar_dequant_add_requant", "taco_update_scale", "qta_copy",
+                     "qar_dequant_add", "qar_dequant_add_requant", "qta_sq_error", "taco_update_scale", "qta_copy",
                      "qta_device_error"):
             getattr(L, name).restype = ctypes.c_int
         L.qta_status_string.argtypes = [ctypes.c_int]
@@ -119,10 +121,11 @@ def _stream(stream) -> int | None:
     return stream.cuda_stream
 
 
-def desc(scheme, block: int, rows: int, cols: int, batch: int = 1) -> Desc:
+def desc(scheme, block: int, rows: int, cols: int, batch: int = 1, max_sms: int = 0) -> Desc:
+    """max_sms: SMs the calls may occupy (0: all)."""
     if isinstance(scheme, str):
         scheme = SCHEMES[scheme]
-    return Desc(int(scheme), int(block), int(batch), int(rows), int(cols))
+    return Desc(int(scheme), int(block), int(batch), int(rows), int(cols), int(max_sms))
 
 
 @dataclass
@@ -141,7 +144,7 @@ class QTensor:
         """View of tensor i of a batch as a batch-1 quantized tensor."""
         d = self.desc
         n = d.batch
-        sub = Desc(d.scheme, d.block, 1, d.rows, d.cols)
+        sub = Desc(d.scheme, d.block, 1, d.rows, d.cols, d.max_sms)
         cb, sb, zb = codes_bytes(sub), scales_bytes(sub), zeros_bytes(sub)
         return QTensor(sub, self.codes[i * cb:(i + 1) * cb], self.scales[i * sb:(i + 1) * sb],
                        None if self.zeros is None else self.zeros[i * zb:(i + 1) * zb],
@@ -229,6 +232,11 @@ def qar_dequant_add_requant(d: Desc, q_in: QTensor, x, x_dtype: int, out: QTenso
     _check("qar_dequant_add_requant", lib().qar_dequant_add_requant(ctypes.byref(d), ctypes.byref(qi), _ptr(x),
                                                                     x_dtype, ctypes.byref(qo), mode,
                                                                     _stream(stream)))
+
+
+def qta_sq_error(a, a_dtype: int, b, n: int, out, stream=None) -> None:
+    """out (device float64 [1]) = sum of (a - b)^2 over n elements."""
+    _check("qta_sq_error", lib().qta_sq_error(_ptr(a), a_dtype, _ptr(b), n, _ptr(out), _stream(stream)))
 
 
 def taco_update_scale(state, n_tensors: int, stream=None) -> None:

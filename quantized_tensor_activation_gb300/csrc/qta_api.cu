@@ -144,7 +144,7 @@ qta_status check_desc(const qta_desc* d)
         break;
     default: return QTA_ERR_UNSUPPORTED;
     }
-    if (d->batch < 0 || d->rows < 0 || d->cols < 0) return QTA_ERR_INVALID_ARG;
+    if (d->batch < 0 || d->rows < 0 || d->cols < 0 || d->max_sms < 0) return QTA_ERR_INVALID_ARG;
     if (d->cols % d->block) return QTA_ERR_INVALID_ARG;
     // element count must leave fewer than 2^31 segments
     const long double n = (long double)d->batch * (long double)d->rows * (long double)d->cols;
@@ -178,8 +178,11 @@ qta_status check_qtensor(const qta_desc* d, const qta_qtensor* q)
     return QTA_OK;
 }
 
-int grid_for(int n_warp_tiles, int warps, int smem, int sms, int smem_per_sm)
+// Persistent grid: at most one CTA per SM it may use (max_sms > 0 caps the
+// SMs, see qta_desc), never more CTAs than warp tiles need.
+int grid_for(int n_warp_tiles, int warps, int smem, int sms, int smem_per_sm, int max_sms)
 {
+    if (max_sms > 0 && max_sms < sms) sms = max_sms;
     int per_sm = smem_per_sm / (smem + 1024);
     if (per_sm < 1) per_sm = 1;
     const int ctas = (n_warp_tiles + warps - 1) / warps;
@@ -292,7 +295,8 @@ static qta_status compress_impl(const qta_desc* d, const void* x, int32_t x_dtyp
     qta_status st = check_desc(d);
     if (st != QTA_OK) return st;
     if (x_dtype != QTA_BF16 && x_dtype != QTA_FP16 && x_dtype != QTA_FP32) return QTA_ERR_UNSUPPORTED;
-    if (d->scheme == QTA_TACO_FP8 && mode != QTA_SCALE_DELAYED && mode != QTA_SCALE_CURRENT)
+    const int base_mode = mode & ~QTA_SCALE_ROUND_UP;
+    if (d->scheme == QTA_TACO_FP8 && base_mode != QTA_SCALE_DELAYED && base_mode != QTA_SCALE_CURRENT)
         return QTA_ERR_INVALID_ARG;
     if (n_elems(d) == 0) return QTA_OK;
     if (!x) return QTA_ERR_INVALID_ARG;
@@ -317,10 +321,12 @@ static qta_status compress_impl(const qta_desc* d, const void* x, int32_t x_dtyp
     p.lanes_per_block = lanes_of(d);
     p.lanes_log2 = log2i(p.lanes_per_block);
     p.seg_per_tensor = make_fastdiv(static_cast<uint32_t>(d->rows * d->cols / 64));
+    p.round_up = (mode & QTA_SCALE_ROUND_UP) ? 1 : 0;
     const int sch = d->scheme;  // qta_scheme values equal the kernel scheme kinds
-    const int grid = grid_for(p.n_warp_tiles, compress_warps(x_dtype), compress_smem(x_dtype, sch), sms, smem_sm);
+    const int grid =
+        grid_for(p.n_warp_tiles, compress_warps(x_dtype), compress_smem(x_dtype, sch), sms, smem_sm, d->max_sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (d->scheme == QTA_TACO_FP8 && mode == QTA_SCALE_CURRENT) {
+    if (d->scheme == QTA_TACO_FP8 && base_mode == QTA_SCALE_CURRENT) {
         cudaError_t e = launch_state(out->state, d->batch, STATE_RESET_AMAX, s);
         if (e == cudaSuccess) e = launch_compress(x_dtype, sch, true, p, grid, s);
         if (e == cudaSuccess) e = launch_state(out->state, d->batch, STATE_SET_SCALE, s);
@@ -370,7 +376,8 @@ qta_status taco_decompress(const qta_desc* d, const qta_qtensor* in, void* y, in
     p.lanes_log2 = log2i(p.lanes_per_block);
     p.inv_block = 1.0f / static_cast<float>(d->block);
     p.seg_per_tensor = make_fastdiv(static_cast<uint32_t>(d->rows * d->cols / 64));
-    const int grid = grid_for(p.n_warp_tiles, decompress_warps(y_dtype), decompress_smem(d->scheme, y_dtype), sms, smem_sm);
+    const int grid = grid_for(p.n_warp_tiles, decompress_warps(y_dtype), decompress_smem(d->scheme, y_dtype), sms,
+                              smem_sm, d->max_sms);
     return cuda_status(launch_decompress(d->scheme, y_dtype, p, grid, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -430,7 +437,8 @@ qta_status qar_reduce_requant(const qta_desc* d, const qta_qtensor* shards, int3
     if (st != QTA_OK) return st;
     if ((st = check_desc(od)) != QTA_OK) return st;
     if (od->cols != d->cols || od->batch * od->rows != row_end - row_begin) return QTA_ERR_INVALID_ARG;
-    if (od->scheme == QTA_TACO_FP8 && mode != QTA_SCALE_DELAYED && mode != QTA_SCALE_CURRENT)
+    const int base_mode = mode & ~QTA_SCALE_ROUND_UP;
+    if (od->scheme == QTA_TACO_FP8 && base_mode != QTA_SCALE_DELAYED && base_mode != QTA_SCALE_CURRENT)
         return QTA_ERR_INVALID_ARG;
     if (!reduce_requant_supported(d->scheme, od->scheme)) return QTA_ERR_UNSUPPORTED;
     if (empty) return QTA_OK;
@@ -443,9 +451,11 @@ qta_status qar_reduce_requant(const qta_desc* d, const qta_qtensor* shards, int3
     p.q_lanes_per_block = lanes_of(od);
     p.q_lanes_log2 = log2i(p.q_lanes_per_block);
     p.q_seg_per_tensor = make_fastdiv(static_cast<uint32_t>(od->rows * od->cols / 64));
-    const int grid = grid_for(p.n_warp_tiles, reduce_warps(), reduce_smem(d->scheme, od->scheme), sms, smem_sm);
+    p.q_round_up = (mode & QTA_SCALE_ROUND_UP) ? 1 : 0;
+    const int grid = grid_for(p.n_warp_tiles, reduce_warps(), reduce_smem(d->scheme, od->scheme), sms, smem_sm,
+                              d->max_sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (od->scheme == QTA_TACO_FP8 && mode == QTA_SCALE_CURRENT) {
+    if (od->scheme == QTA_TACO_FP8 && base_mode == QTA_SCALE_CURRENT) {
         cudaError_t e = launch_state(out->state, od->batch, STATE_RESET_AMAX, s);
         if (e == cudaSuccess) e = launch_reduce_requant(d->scheme, od->scheme, true, p, grid, s);
         if (e == cudaSuccess) e = launch_state(out->state, od->batch, STATE_SET_SCALE, s);
@@ -466,7 +476,8 @@ qta_status qar_reduce(const qta_desc* d, const qta_qtensor* shards, int32_t n_ra
     if (!aligned(sum_out, 16)) return QTA_ERR_ALIGNMENT;
     if ((st = reduce_fill(d, shards, n_ranks, row_begin, row_end, &p, &sms, &smem_sm)) != QTA_OK) return st;
     if (!map_f32(&p.out_map, sum_out, static_cast<uint64_t>(p.M_out))) return QTA_ERR_CUDA;
-    const int grid = grid_for(p.n_warp_tiles, reduce_warps(), reduce_smem(d->scheme, OUT_F32), sms, smem_sm);
+    const int grid =
+        grid_for(p.n_warp_tiles, reduce_warps(), reduce_smem(d->scheme, OUT_F32), sms, smem_sm, d->max_sms);
     return cuda_status(launch_reduce(d->scheme, p, grid, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -479,7 +490,8 @@ static qta_status accum_impl(const qta_desc* d, const qta_qtensor* in, const voi
     if (st != QTA_OK) return st;
     if (x_dtype != QTA_BF16 && x_dtype != QTA_FP16 && x_dtype != QTA_FP32) return QTA_ERR_UNSUPPORTED;
     const bool requant = out != nullptr;
-    if (requant && d->scheme == QTA_TACO_FP8 && mode != QTA_SCALE_DELAYED && mode != QTA_SCALE_CURRENT)
+    const int base_mode = mode & ~QTA_SCALE_ROUND_UP;
+    if (requant && d->scheme == QTA_TACO_FP8 && base_mode != QTA_SCALE_DELAYED && base_mode != QTA_SCALE_CURRENT)
         return QTA_ERR_INVALID_ARG;
     if (n_elems(d) == 0) return QTA_OK;
     if (!x || (!requant && !sum_out)) return QTA_ERR_INVALID_ARG;
@@ -512,11 +524,12 @@ static qta_status accum_impl(const qta_desc* d, const qta_qtensor* in, const voi
         p.q_scales = out->scales;
         p.q_zeros = out->zeros;
         p.q_state = out->state;
+        p.round_up = (mode & QTA_SCALE_ROUND_UP) ? 1 : 0;
     }
     const int grid = grid_for(p.n_warp_tiles, accum_warps(x_dtype, requant), accum_smem(x_dtype, requant), sms,
-                              smem_sm);
+                              smem_sm, d->max_sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (requant && d->scheme == QTA_TACO_FP8 && mode == QTA_SCALE_CURRENT) {
+    if (requant && d->scheme == QTA_TACO_FP8 && base_mode == QTA_SCALE_CURRENT) {
         cudaError_t e = launch_state(out->state, d->batch, STATE_RESET_AMAX, s);
         if (e == cudaSuccess) e = launch_accum(d->scheme, x_dtype, true, true, p, grid, s);
         if (e == cudaSuccess) e = launch_state(out->state, d->batch, STATE_SET_SCALE, s);
@@ -536,6 +549,21 @@ qta_status qar_dequant_add_requant(const qta_desc* d, const qta_qtensor* in, con
 {
     if (!out) return QTA_ERR_INVALID_ARG;
     return accum_impl(d, in, x, x_dtype, nullptr, out, mode, stream);
+}
+
+qta_status qta_sq_error(const void* a, int32_t a_dtype, const float* b, int64_t n, double* out,
+                        qta_stream_t stream)
+{
+    if (a_dtype != QTA_BF16 && a_dtype != QTA_FP16 && a_dtype != QTA_FP32) return QTA_ERR_UNSUPPORTED;
+    if (n < 0 || !out) return QTA_ERR_INVALID_ARG;
+    if (n > 0 && (!a || !b)) return QTA_ERR_INVALID_ARG;
+    if (!aligned(out, 8) || !aligned(a, 4) || !aligned(b, 4)) return QTA_ERR_ALIGNMENT;
+    int sms = 0, smem_sm = 0;
+    unsigned int* err = nullptr;
+    if (device_info(&sms, &smem_sm, &err) != cudaSuccess) return QTA_ERR_CUDA;
+    const long long blocks = (n + 255) / 256;
+    const int grid = static_cast<int>(blocks < 4LL * sms ? (blocks > 0 ? blocks : 1) : 4LL * sms);
+    return cuda_status(launch_sq_error(a, a_dtype, b, n, out, grid, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 qta_status taco_update_scale(float* state, int64_t n_tensors, qta_stream_t stream)

@@ -40,6 +40,7 @@ struct CompressParams {
     int lanes_per_block;  // block / 64 (TACO), 1 (INT8 sym), 2 (asym)
     int lanes_log2;
     FastDiv seg_per_tensor;
+    int round_up;         // TACO: block scales rounded up (QTA_SCALE_ROUND_UP)
 };
 
 struct DecompressParams {
@@ -78,6 +79,7 @@ struct ReduceParams {
     int q_lanes_per_block;
     int q_lanes_log2;
     FastDiv q_seg_per_tensor;
+    int q_round_up;
 };
 
 // One ring hop: the incoming quantized partial sum plus the local tensor x,
@@ -99,6 +101,7 @@ struct AccumParams {
     void* q_scales;       // requantization outputs
     void* q_zeros;
     float* q_state;
+    int round_up;
 };
 
 // ------------------------------------------------------------ configuration
@@ -376,6 +379,7 @@ struct QuantOut {
     int lanes_per_block;
     int lanes_log2;
     FastDiv seg_per_tensor;
+    int round_up;           // TACO block scales: smallest E4M3 value >= the ratio
 };
 
 // Quantizes one warp tile (one 64-element segment per lane, values in the
@@ -438,7 +442,9 @@ struct Quantizer {
                     cached_tensor = uniform ? tens : -1;
                 }
                 const float ab = group_max(a, L);
-                uint32_t r = e4m3_encode(__fmul_rn(ab, tinv));
+                const float ratio = __fmul_rn(ab, tinv);
+                uint32_t r = e4m3_encode(ratio);
+                if (o.round_up && r < 0x7Eu && e4m3_decode(r) < ratio) ++r;
                 if (r == 0u && ab > 0.0f) r = 1u;
                 const float sb = __fmul_rn(S, e4m3_decode(r));
                 const float inv = (sb > 0.0f) ? __frcp_rn(sb) : 0.0f;
@@ -588,7 +594,8 @@ compress_kernel(const __grid_constant__ CompressParams p)
     }
     __syncwarp();
 
-    const QuantOut qo{p.scales, p.zeros, p.state, p.M, p.lanes_per_block, p.lanes_log2, p.seg_per_tensor};
+    const QuantOut qo{p.scales, p.zeros, p.state, p.M, p.lanes_per_block, p.lanes_log2, p.seg_per_tensor,
+                      p.round_up};
     Quantizer<SCH> quant;
     int stage = 0;
     uint32_t phase = 0;
@@ -858,7 +865,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
     int unit = 0;
     bool aborted = false;
     const QuantOut qo{p.q_scales, p.q_zeros, p.q_state, p.M_out, p.q_lanes_per_block, p.q_lanes_log2,
-                      p.q_seg_per_tensor};
+                      p.q_seg_per_tensor, p.q_round_up};
     Quantizer<(OSCH == OUT_F32) ? S_TACO : OSCH> quant;
     SegMeta<SCH> nxt[RANK_CHUNK];
     if (my_tiles > 0) reduce_meta_load<SCH, RANK_CHUNK>(p, 0, 0, first, W, lane, nxt);
@@ -995,7 +1002,8 @@ accum_kernel(const __grid_constant__ AccumParams p)
     }
     __syncwarp();
     const int L = p.lanes_per_block;
-    const QuantOut qo{p.q_scales, p.q_zeros, p.q_state, p.M, p.lanes_per_block, p.lanes_log2, p.seg_per_tensor};
+    const QuantOut qo{p.q_scales, p.q_zeros, p.q_state, p.M, p.lanes_per_block, p.lanes_log2, p.seg_per_tensor,
+                      p.round_up};
     Quantizer<(OSCH == OUT_F32) ? S_TACO : OSCH> quant;
     int stage = 0;
     uint32_t phase = 0;

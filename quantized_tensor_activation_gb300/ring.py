@@ -40,7 +40,7 @@ def chunk_orders(n: int, j: int, semi: bool):
 def _chunk_desc(d: Desc, n: int) -> Desc:
     if d.batch != 1 or d.rows % n:
         raise ValueError("the ring takes one [rows, cols] tensor per rank with rows divisible by the ranks")
-    return desc(d.scheme, d.block, d.rows // n, d.cols)
+    return desc(d.scheme, d.block, d.rows // n, d.cols, max_sms=d.max_sms)
 
 
 def reduce_scatter(d: Desc, xs: torch.Tensor, semi: bool = False, hop_partials: list | None = None,

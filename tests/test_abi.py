@@ -68,7 +68,8 @@ def test_argument_checks(L):
     assert L.taco_compress(D(0, 128, 4, 192), 16, 0, Q(), 0, None) == INV      # cols % block
     assert L.taco_compress(D(0, 128, -1, 128), 16, 0, Q(), 0, None) == INV
     assert L.taco_compress(D(0, 128, 4, 128), 16, 7, Q(), 0, None) == UNS      # dtype
-    assert L.taco_compress(D(0, 128, 4, 128), 16, 0, Q(), 5, None) == INV      # mode
+    for bad_mode in (2, 3, 6, 8, -1):                                        # mode (flag 4 allowed)
+        assert L.taco_compress(D(0, 128, 4, 128), 16, 0, Q(), bad_mode, None) == INV
     # pointer problems
     assert L.taco_compress(D(0, 128, 4, 128), None, 0, Q(), 0, None) == INV
     assert L.taco_compress(D(0, 128, 4, 128), 24, 0, Q(), 0, None) == ALN
@@ -147,3 +148,14 @@ def test_ring_hop_argument_checks(L):
     assert g(D(0, 128, 4, 128), q, 16, 0, q, 9, None) == INV         # TACO scale mode
     assert g(D(2, 128, 4, 256), q, 16, 1, ctypes.byref(qta.QTensorC(16, 16, None, 16)), 0, None) == INV
     assert g(D(1, 64, 4, 128), q, 16, 2, ctypes.byref(qta.QTensorC(8, 16, 16, 16)), 0, None) == ALN
+
+
+def test_descriptor_layout_and_sm_cap(L):
+    # the C layout: two int32, three int64, one int32 (+ padding)
+    assert ctypes.sizeof(qta.Desc) == 40
+    assert qta.Desc.max_sms.offset == 32
+    d = qta.desc("taco_fp8", 128, 4, 256, max_sms=48)
+    assert d.max_sms == 48 and qta.desc("int8_sym", 64, 1, 64).max_sms == 0
+    bad = qta.desc("taco_fp8", 128, 4, 256, max_sms=-1)
+    assert L.taco_compress(ctypes.byref(bad), 16, 0, ctypes.byref(qta.QTensorC(16, 16, 16, 16)), 0,
+                           None) == qta.QTA_ERR_INVALID_ARG

@@ -313,3 +313,38 @@ def test_reduce_requant_rejects_unsupported_pairs(dev):
     with pytest.raises(qta.QtaError) as e:
         qta.qar_reduce_requant(d, [q], 0, 8, qta.desc(qta.TACO_FP8, 128, 3, 256, batch=2), q)
     assert e.value.status == qta.QTA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("B", [64, 128, 256])
+@pytest.mark.parametrize("dtype", [qta.BF16, qta.FP32])
+@pytest.mark.parametrize("mode", [qta.SCALE_CURRENT, qta.SCALE_DELAYED])
+def test_taco_compress_round_up(dev, B, dtype, mode):
+    # block scales rounded up to the smallest covering E4M3 value, with the
+    # same stale previous-step scales as above in DELAYED mode
+    batch, rows, cols = 3, 37, 1024
+    rng = np.random.default_rng(7 * B + dtype + 3 * mode)
+    xt = _x(rng, batch, rows, cols, dtype)
+    state = np.array([1e-6, 0.5, 1e3, 0.0, 0.01, 7.0], dtype=np.float32)
+    _, q = gpu_compress(qta.TACO_FP8, B, xt, dtype, batch, rows, cols, mode | qta.SCALE_ROUND_UP, state=state,
+                        dev=dev)
+    omode = (orc.CURRENT if mode == qta.SCALE_CURRENT else orc.DELAYED) | orc.ROUND_UP
+    ref = oracle_compress(qta.TACO_FP8, B, xt, dtype, batch, rows, cols, omode, state=state)
+    torch.cuda.synchronize()
+    compare_qtensor("taco round-up", q, ref)
+
+
+@pytest.mark.parametrize("gB", [128, 256])
+def test_reduce_requant_round_up(dev, gB):
+    rows, cols, n, nb = 64, 1024, 4, 4
+    rng = np.random.default_rng(gB)
+    shards = _oracle_shards(qta.TACO_FP8, 128, n, rows, cols, rng)
+    d, ds = _to_dev(qta.TACO_FP8, 128, rows, cols, shards, dev)
+    dg = qta.desc(qta.TACO_FP8, gB, rows // nb, cols, batch=nb)
+    g = qta.alloc_qtensor(dg, dev)
+    qta.qar_reduce_requant(d, ds, 0, rows, dg, g, qta.SCALE_CURRENT | qta.SCALE_ROUND_UP)
+    st_ref = np.zeros(2 * nb, dtype=np.float32)
+    c, s, z = orc.reduce_requant(orc.TACO_FP8, 128, shards, rows, cols, 0, rows, orc.TACO_FP8, gB, nb, st_ref,
+                                 orc.CURRENT | orc.ROUND_UP)
+    torch.cuda.synchronize()
+    compare_qtensor("fused round-up", g, (c, s, z, st_ref))
+    assert qta.qta_device_error() == 0

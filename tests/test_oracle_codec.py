@@ -102,6 +102,57 @@ def test_taco_codes_and_scales_are_nearest(orc, B):
         assert np.all((c[b][sat] & 0x7F) == 0x7E)
 
 
+@pytest.mark.parametrize("B", [4, 64, 128, 256])
+@pytest.mark.parametrize("mode_name", ["DELAYED", "CURRENT"])
+def test_taco_round_up_scales_are_the_smallest_cover(orc, B, mode_name):
+    """QTA_SCALE_ROUND_UP: the scale byte is the smallest E4M3 code whose
+    value is not below a_b / (448 S) (searched over the table, ratio in
+    float64 from the exact integer transform), and with a current S no code
+    saturates."""
+    rng = np.random.default_rng(40 + B)
+    nb = 48
+    xi = rng.integers(-60, 61, size=(nb, B))
+    xi[::5] *= 9
+    xi[3] = 0
+    x = xi.astype(np.float32).reshape(-1)
+    mode = getattr(orc, mode_name) | orc.ROUND_UP
+    st = np.array([7.3, 0.0], dtype=np.float32)
+    codes, scales, _ = orc.compress(orc.TACO_FP8, B, x, orc.FP32, 1, nb, B, st, mode)
+    y = (xi @ scipy.linalg.hadamard(B).T).astype(np.float64)
+    a = np.abs(y).max(axis=1)
+    S = float(st[0])
+    table = _e4m3_pos()
+    ratio = a / (448.0 * S)
+    pos = table[:0x7F].astype(np.float64)                 # +0 .. 448
+    for b in range(nb):
+        if a[b] == 0:
+            assert scales[b] == 0
+            continue
+        cover = np.nonzero(pos >= ratio[b] * (1 - 2.0 ** -22))[0]
+        want = cover[0] if cover.size else 0x7E
+        # the FP32 ratio may sit a rounding away from the float64 one
+        assert scales[b] in (want, want + 1) and table[scales[b]] >= ratio[b] * (1 - 2.0 ** -22), b
+        if scales[b] == want + 1:
+            assert abs(pos[want] / ratio[b] - 1) < 2.0 ** -20
+    if mode_name == "CURRENT":
+        sb = (np.float32(S) * table[scales]).astype(np.float64)
+        v = np.abs(y) / np.where(sb > 0, sb, 1.0)[:, None]
+        assert v.max() <= 448.0 * (1 + 2.0 ** -20)
+        assert not np.any((codes.reshape(nb, B) & 0x7F) == 0x7F)
+
+
+def test_taco_round_up_never_below_nearest(orc):
+    rng = np.random.default_rng(9)
+    x = (rng.standard_normal(64 * 128) * np.exp(rng.uniform(-3, 3, 64 * 128))).astype(np.float32)
+    s1 = np.zeros(2, np.float32)
+    s2 = np.zeros(2, np.float32)
+    _, near, _ = orc.compress(orc.TACO_FP8, 128, x, orc.FP32, 1, 64, 128, s1, orc.CURRENT)
+    _, up, _ = orc.compress(orc.TACO_FP8, 128, x, orc.FP32, 1, 64, 128, s2, orc.CURRENT | orc.ROUND_UP)
+    assert s1[0] == s2[0]
+    assert np.all((up == near) | (up == near + 1))
+    assert np.any(up == near + 1) and np.any(up == near)
+
+
 def test_taco_current_scale_rule(orc):
     w = workloads.WORKLOADS["taco_tiny"]
     import torch
