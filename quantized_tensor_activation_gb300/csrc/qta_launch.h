@@ -31,6 +31,8 @@ cudaError_t launch_reduce_requant(int scheme, int out_scheme, bool amax_only, co
 cudaError_t launch_accum(int scheme, int x_kind, bool requant, bool amax_only, const AccumParams& p, int grid,
                          cudaStream_t stream);
 cudaError_t launch_state(float* state, long long n, int op, cudaStream_t stream);
+cudaError_t launch_sq_error(const void* a, int a_kind, const float* b, long long n, double* out, int grid,
+                            cudaStream_t stream);
 cudaError_t launch_copy(const void* src, void* dst, size_t bytes, int grid, cudaStream_t stream);
 
 // Launch with programmatic stream serialization (see pdl_wait / pdl_trigger).
