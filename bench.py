@@ -564,6 +564,12 @@ def run_qta(args, w):
             del exact, err, e0, y0
 
     ring_rep = ring_report(qta, w, x, 3) if args.ring else None
+    block_choice = None
+    if args.choose_block:
+        from quantized_tensor_activation_gb300 import calib
+        best, errs = calib.choose_block(x[0])
+        block_choice = {"tensor": "rank 0", "chosen_block": best, "workload_block": w.block,
+                        "mse": {str(b): e / x[0].numel() for b, e in errs.items()}}
     sm_sweep = None
     if sweep_raw:
         sm_sweep = []
@@ -600,6 +606,7 @@ def run_qta(args, w):
         "recon": recon,
         "ring": ring_rep,
         "sm_sweep": sm_sweep,
+        "block_choice": block_choice,
         "cpu_baseline": cpu,
         "clocks": clk,
         "e2e": e2e,
@@ -626,6 +633,8 @@ def main(argv=None):
     ap.add_argument("--no-recon", action="store_true", help="skip the reconstruction-error report")
     ap.add_argument("--sm-sweep", default="",
                     help="comma-separated SM counts: time the step with every call capped to that many SMs")
+    ap.add_argument("--choose-block", action="store_true",
+                    help="add the reconstruction error of rank 0's tensor for TACO blocks 64/128/256")
     ap.add_argument("--ring", action="store_true",
                     help="add the ring adder-chain report (full loop / semi loop) of the workload")
     ap.add_argument("--no-graph", action="store_true", help="launch the timed steps eagerly instead of as a CUDA graph")

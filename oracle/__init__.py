@@ -349,3 +349,33 @@ def ring_allreduce(scheme: int, B: int, xs, dtype: int, rows: int, cols: int, se
         q = _compress_current(scheme, B, part, FP32, rc, cols)
         y[j * rc * cols:(j + 1) * rc * cols] = decompress(scheme, B, *q, 1, rc, cols, out_dtype)
     return s, y
+
+
+# ---------------------------------------------------------------- block choice
+def block_errors(x, x_dtype: int, batch: int, rows: int, cols: int, candidates=(64, 128, 256),
+                 mode: int = CURRENT) -> dict:
+    """Squared reconstruction error of compress (TACO, CURRENT scale) ->
+    decompress (FP32) for every candidate block size dividing cols, summed
+    in float64 ([TACO] Core claim: the reshape is chosen from the data)."""
+    xv = np.ascontiguousarray(x).reshape(-1)
+    if x_dtype == BF16:
+        xw = bf16_to_f32(xv).astype(np.float64)
+    elif x_dtype == FP16:
+        xw = f16_to_f32(xv).astype(np.float64)
+    else:
+        xw = xv.astype(np.float64)
+    errs = {}
+    for B in candidates:
+        if cols % B:
+            continue
+        st = np.zeros(2 * batch, dtype=np.float32)
+        c, s, z = compress(TACO_FP8, B, xv, x_dtype, batch, rows, cols, st, mode)
+        y = decompress(TACO_FP8, B, c, s, z, st, batch, rows, cols, FP32).astype(np.float64)
+        errs[B] = float(((xw - y) ** 2).sum())
+    return errs
+
+
+def choose_block(x, x_dtype: int, batch: int, rows: int, cols: int, candidates=(64, 128, 256)):
+    errs = block_errors(x, x_dtype, batch, rows, cols, candidates)
+    best = min(sorted(errs), key=lambda b: errs[b])
+    return best, errs

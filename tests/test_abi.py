@@ -159,3 +159,14 @@ def test_descriptor_layout_and_sm_cap(L):
     bad = qta.desc("taco_fp8", 128, 4, 256, max_sms=-1)
     assert L.taco_compress(ctypes.byref(bad), 16, 0, ctypes.byref(qta.QTensorC(16, 16, 16, 16)), 0,
                            None) == qta.QTA_ERR_INVALID_ARG
+
+
+def test_sq_error_argument_checks(L):
+    OK, INV, ALN, UNS = qta.QTA_OK, qta.QTA_ERR_INVALID_ARG, qta.QTA_ERR_ALIGNMENT, qta.QTA_ERR_UNSUPPORTED
+    f = L.qta_sq_error
+    assert f(16, 7, 16, 4, 16, None) == UNS
+    assert f(16, 0, 16, -1, 16, None) == INV
+    assert f(16, 0, 16, 4, None, None) == INV
+    assert f(None, 0, 16, 4, 16, None) == INV
+    assert f(16, 0, 18, 4, 16, None) == ALN
+    assert f(16, 0, 16, 4, 20, None) == ALN
