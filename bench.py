@@ -304,7 +304,7 @@ def run_qta(args, w):
     in_dt = qta.BF16 if w.dtype == "bf16" else qta.FP16
     tdt = w.torch_dtype
     x = workloads.make_rank_inputs(w, device=dev, seed=args.seed)            # [N, R, C] resident in HBM
-    d_in = qta.desc(sch[w.scheme], w.block, R, C, batch=N)
+    d_in = qta.desc(sch[w.scheme], w.block, R, C, batch=N, max_sms=args.k1_sms)
     d_sh = qta.desc(sch[w.scheme], w.block, R, C)
     d_g = qta.desc(sch[w.gather_scheme], w.gather_block, R // N, C, batch=N)
     taco1 = w.scheme == "taco_fp8"
@@ -456,60 +456,70 @@ def run_qta(args, w):
             evs3, s3a, s3b, _ = timed(fused)
             torch.cuda.synchronize()
             sweep_raw.append((n_sms, s3a.elapsed_time(s3b) / args.steps, evs3))
-        for dd in (d_in, d_sh, d_g):
-            dd.max_sms = 0
+        d_in.max_sms, d_sh.max_sms, d_g.max_sms = args.k1_sms, 0, 0
         assert qta.qta_device_error() == 0
 
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
         xh = x.cpu().pin_memory()
-        yh = torch.empty((R, C), dtype=tdt).pin_memory()
-        xd = torch.empty_like(x)
-        # the per-rank inputs travel on several copy streams at once
-        copy_streams = [torch.cuda.Stream() for _ in range(min(4, N))]
-        done = [torch.cuda.Event() for _ in copy_streams]
+        yh = [torch.empty((R, C), dtype=tdt).pin_memory() for _ in range(2)]
+        # double-buffered: the upload of step i+1 runs on its own copy stream
+        # while step i computes and downloads its result
+        xd = [torch.empty_like(x) for _ in range(2)]
+        yd = [y, torch.empty_like(y)]
+        h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+        x_free = [torch.cuda.Event() for _ in range(2)]    # the step that last read xd[b] has compressed it
+        y_free = [torch.cuda.Event() for _ in range(2)]    # yd[b] has been copied to the host
+        for ev in x_free + y_free:
+            ev.record(stream)
         torch.cuda.synchronize()
 
-        def copy_in():
-            ready = torch.cuda.Event()
-            ready.record(stream)
-            for i, (cs, ev) in enumerate(zip(copy_streams, done)):
-                cs.wait_event(ready)
-                with torch.cuda.stream(cs):
-                    for r in range(i, N, len(copy_streams)):
-                        xd[r].copy_(xh[r], non_blocking=True)
-                    ev.record(cs)
-            for ev in done:
-                stream.wait_event(ev)
-
-        def e2e_step():
-            copy_in()
-            qta.taco_compress(d_in, xd, in_dt, q, qta.SCALE_DELAYED)
+        def e2e_step(i):
+            bi = i % 2
+            h2d.wait_event(x_free[bi])
+            with torch.cuda.stream(h2d):
+                xd[bi].copy_(xh, non_blocking=True)
+            arrived = torch.cuda.Event()
+            arrived.record(h2d)
+            stream.wait_event(arrived)
+            qta.taco_compress(d_in, xd[bi], in_dt, q, qta.SCALE_DELAYED)
+            x_free[bi].record(stream)
             if fused:
                 qta.qar_reduce_requant(d_sh, shards, 0, R, d_g, g, qta.SCALE_DELAYED)
             else:
                 qta.qar_reduce(d_sh, shards, 0, R, ssum)
                 qta.qar_requant(d_g, ssum, g, qta.SCALE_DELAYED)
-            qta.taco_decompress(d_g, g, y, in_dt)
+            stream.wait_event(y_free[bi])
+            qta.taco_decompress(d_g, g, yd[bi], in_dt)
             if n_state:
                 qta.taco_update_scale(states, n_state)
-            yh.copy_(y, non_blocking=True)
+            done = torch.cuda.Event()
+            done.record(stream)
+            d2h.wait_event(done)
+            with torch.cuda.stream(d2h):
+                yh[bi].copy_(yd[bi], non_blocking=True)
+            y_free[bi].record(d2h)
 
-        for _ in range(2):
-            e2e_step()
+        for i in range(2):
+            e2e_step(i)
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        k = max(3, args.steps // 2)
+        k = max(4, args.steps // 2)
         a.record(stream)
-        for _ in range(k):
-            e2e_step()
+        h2d.wait_event(a)
+        for i in range(k):
+            e2e_step(i)
+        for ev in y_free:
+            stream.wait_event(ev)
         b.record(stream)
         torch.cuda.synchronize()
         e2e_ms = a.elapsed_time(b) / k
         e2e = {"value": 2 * N * R * C / (e2e_ms * 1e-3) / 1e9 * ws, "unit": "GB/s",
                "h2d_bytes_per_step": x.numel() * x.element_size(),
-               "d2h_bytes_per_step": y.numel() * y.element_size(), "ms_per_step": e2e_ms}
+               "d2h_bytes_per_step": y.numel() * y.element_size(), "ms_per_step": e2e_ms,
+               "pipeline": "inputs and outputs double-buffered: the upload of step i+1 overlaps step i's "
+                           "kernels and download; each step copies its own inputs in and its result out"}
 
     if rank != 0:
         if ws > 1:
@@ -591,7 +601,8 @@ def run_qta(args, w):
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": _config(w),
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": dict(_config(w), **({"k1_max_sms": args.k1_sms} if args.k1_sms else {})),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "kernel": "K1 taco_compress",
                      "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes": alg["K1"]},
@@ -631,6 +642,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="skip the nvidia-smi clock window (profiling runs)")
     ap.add_argument("--no-recon", action="store_true", help="skip the reconstruction-error report")
+    ap.add_argument("--k1-sms", type=int, default=0,
+                    help="SMs the compress (K1) may occupy (qta_desc.max_sms; 0: all)")
     ap.add_argument("--sm-sweep", default="",
                     help="comma-separated SM counts: time the step with every call capped to that many SMs")
     ap.add_argument("--choose-block", action="store_true",
