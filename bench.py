@@ -44,7 +44,7 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     # ncu dram__bytes_read.sum + dram__bytes_write.sum of one compress_kernel<bf16, TACO>
     # launch on gpt_tp (profiles/gpt_tp_step.md), valid for the CUDA sources it was taken on
-    ("taco_compress", "gpt_tp"): {"bytes": 536904192 + 231982848, "src": "a85db131db64e393"},
+    ("taco_compress", "gpt_tp"): {"bytes": 536911616 + 233753600, "src": "c3fced13172071ed"},
 }
 
 
@@ -428,6 +428,26 @@ def run_qta(args, w):
         else:
             step(fused=fused)
 
+    # the timed steps as one CUDA graph with a timing event between every two
+    # kernels (event record nodes): the per-kernel times then come from the
+    # timed region itself, free of host launch gaps
+    def graph_with_events(fused_path):
+        try:
+            evl = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)]
+                   for _ in range(args.steps)]
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr):
+                for i in range(args.steps):
+                    step(ev=evl[i], fused=fused_path)
+            gr.replay()
+            torch.cuda.synchronize()
+            evl[0][0].elapsed_time(evl[0][1])
+            return gr, evl
+        except (TypeError, RuntimeError):
+            return None, None
+
+    tgraph, tevs = (None, None) if args.no_graph else graph_with_events(fused)
+
     # ---- timed region: inputs resident in HBM
     clocks = ClockSampler(None if args.no_clocks else _smi_gpu_id(torch, local))
     if ws > 1:
@@ -444,8 +464,11 @@ def run_qta(args, w):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
-    for _ in range(args.steps):
-        run_step()
+    if tgraph is not None:
+        tgraph.replay()
+    else:
+        for _ in range(args.steps):
+            run_step()
     t_end.record(stream)
     n_launch = args.steps * ((3 if fused else 4) + int(n_state > 0))
     for _ in range(pad):
@@ -457,15 +480,36 @@ def run_qta(args, w):
     if clk is not None:
         clk["window"] = f"sampled every 100 ms over {2 * pad + args.steps} back-to-back steps around and including the timed ones"
     ms_step = max_over_ranks(t_start.elapsed_time(t_end) / args.steps, dev)
+    # the same graph of the step without the timing events, for comparison
+    plain_ms = None
+    if graph is not None:
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        p1.record(stream)
+        torch.cuda.synchronize()
+        plain_ms = p0.elapsed_time(p1) / args.steps
 
-    # per-kernel times: the same step launched eagerly with events between the calls
+    # per-kernel times: from the timed graph's events, else from the step
+    # launched eagerly with events between the calls
     evs, e0, e1, _ = timed(fused)
     torch.cuda.synchronize()
     eager_ms = e0.elapsed_time(e1) / args.steps
+    if tevs is not None:
+        evs = tevs
     # the other path (two calls, FP32 sum through HBM), for comparison
-    evs2, s2a, s2b, _ = timed(not fused)
+    g2, evs2 = (None, None) if args.no_graph else graph_with_events(not fused)
+    if g2 is not None:
+        s2a, s2b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2a.record(stream)
+        g2.replay()
+        s2b.record(stream)
+    else:
+        evs2, s2a, s2b, _ = timed(not fused)
     torch.cuda.synchronize()
     other_ms = s2a.elapsed_time(s2b) / args.steps
+    del g2
     assert qta.qta_device_error() == 0
 
     # the same step with every call capped to a number of SMs (eager launches)
@@ -625,7 +669,7 @@ def run_qta(args, w):
         "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": _config(w),
-        "launch": {"k1_max_sms": k1_cap or "all",
+        "k1_sms": {"k1_max_sms": k1_cap or "all",
                    "k1_sms_choice": ("fixed" if k1_tune is None else
                                      "fastest eager step of " + ", ".join(
                                          f"{c or 'all'}: {t * 1e3:.1f} us" for c, t in k1_tune.items()))},
@@ -633,7 +677,11 @@ def run_qta(args, w):
                      "frac": achieved / peak, "traffic": traffic, "kernel": "K1 taco_compress",
                      "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes": alg["K1"]},
         "path": "fused reduce+requant (qar_reduce_requant)" if fused else "qar_reduce + qar_requant",
-        "launch": "CUDA graph of one step, replayed" if graph is not None else "eager",
+        "launch": ("one CUDA graph of the timed steps, with a timing event between every two kernels"
+                   if tgraph is not None else
+                   "CUDA graph of one step, replayed" if graph is not None else "eager"),
+        "ms_per_step_graph_without_events": plain_ms,
+        "kernel_times": "events inside the timed graph" if tevs is not None else "eager step with events",
         "eager_ms_per_step": eager_ms,
         "kernels": kern,
         "step_frac_of_hbm": step_bytes / (ms_step * 1e-3) / 1e9 / peak,

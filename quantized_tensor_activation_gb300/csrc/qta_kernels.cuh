@@ -140,13 +140,13 @@ constexpr int OUT_F32 = -1;
 
 template <int SCH, int OSCH = OUT_F32>
 struct ReduceCfg {
-    // the INT4 fused kernel fits 128 registers and gains from 16 warps; the
-    // others need more registers and run 12
-    static constexpr bool W16 = (SCH == S_ASYM4) && (OSCH != OUT_F32);
+    // the INT4 kernels fit 128 registers and gain from 16 warps (issue-bound
+    // decode); the others need more registers and run 12
+    static constexpr bool W16 = (SCH == S_ASYM4);
     static constexpr int WARPS = W16 ? 16 : 12;
     static constexpr int IN_SEG = (SCH == S_ASYM4) ? 32 : 64;
     static constexpr int OUT_SEG = (OSCH == OUT_F32) ? 256 : (OSCH == S_ASYM4) ? 32 : 64;
-    static constexpr int STAGES = (OSCH == OUT_F32) ? ((SCH == S_ASYM4) ? 8 : 4) : ((SCH == S_ASYM4) ? 12 : 8);
+    static constexpr int STAGES = (OSCH == OUT_F32) ? 4 : ((SCH == S_ASYM4) ? 12 : 8);
     // ranks whose scale metadata is fetched together, one chunk ahead
     static constexpr int RANK_CHUNK = W16 ? 8 : 4;
     static constexpr int IN_BYTES = 32 * IN_SEG;
