@@ -44,7 +44,7 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     # ncu dram__bytes_read.sum + dram__bytes_write.sum of one compress_kernel<bf16, TACO>
     # launch on gpt_tp (profiles/gpt_tp_step.md), valid for the CUDA sources it was taken on
-    ("taco_compress", "gpt_tp"): {"bytes": 536911616 + 233753600, "src": "c3fced13172071ed"},
+    ("taco_compress", "gpt_tp"): {"bytes": 536937984 + 232668672, "src": "f55069903541252e"},
 }
 
 
@@ -443,8 +443,11 @@ def run_qta(args, w):
             torch.cuda.synchronize()
             evl[0][0].elapsed_time(evl[0][1])
             return gr, evl
-        except (TypeError, RuntimeError):
+        except (TypeError, RuntimeError) as e:
+            graph_event_error[0] = f"{type(e).__name__}: {str(e).splitlines()[0][:160]}"
             return None, None
+
+    graph_event_error = [None]
 
     tgraph, tevs = (None, None) if args.no_graph else graph_with_events(fused)
 
@@ -681,7 +684,9 @@ def run_qta(args, w):
                    if tgraph is not None else
                    "CUDA graph of one step, replayed" if graph is not None else "eager"),
         "ms_per_step_graph_without_events": plain_ms,
-        "kernel_times": "events inside the timed graph" if tevs is not None else "eager step with events",
+        "kernel_times": ("events inside the timed graph" if tevs is not None else
+                         "eager step with events" + (f" (graph events unavailable: {graph_event_error[0]})"
+                                                     if graph_event_error[0] else "")),
         "eager_ms_per_step": eager_ms,
         "kernels": kern,
         "step_frac_of_hbm": step_bytes / (ms_step * 1e-3) / 1e9 / peak,
