@@ -9,9 +9,9 @@ from __future__ import annotations
 
 import torch
 
-from . import FP32, SCALE_CURRENT, alloc_qtensor, desc, qta_sq_error, taco_compress, taco_decompress
+from . import BF16, FP16, FP32, SCALE_CURRENT, alloc_qtensor, desc, qta_sq_error, taco_compress, taco_decompress
 
-_DT = {torch.bfloat16: 0, torch.float16: 1, torch.float32: FP32}
+_DT = {torch.bfloat16: BF16, torch.float16: FP16, torch.float32: FP32}
 
 
 def block_errors(x: torch.Tensor, candidates=(64, 128, 256), mode: int = SCALE_CURRENT) -> dict:
