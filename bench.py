@@ -333,31 +333,33 @@ def run_qta(args, w):
         # each compress uses the per-tensor scale left by the previous step and
         # accumulates this step's amax; the receiving side dequantizes with the
         # same scale, so the states are updated once, at the end of the step
+        # events go on the current stream, which is the capture stream while
+        # a CUDA graph of the step is being recorded
         mode = qta.SCALE_CURRENT if first else qta.SCALE_DELAYED
         if ev:
-            ev[0].record(stream)
+            ev[0].record()
         qta.taco_compress(d_in, x, in_dt, q, mode)
         if ev:
-            ev[1].record(stream)
+            ev[1].record()
         if fused:
             qta.qar_reduce_requant(d_sh, shards, 0, R, d_g, g, mode)
             if ev:
-                ev[2].record(stream)
-                ev[3].record(stream)
+                ev[2].record()
+                ev[3].record()
         else:
             qta.qar_reduce(d_sh, shards, 0, R, ssum)
             if ev:
-                ev[2].record(stream)
+                ev[2].record()
             qta.qar_requant(d_g, ssum, g, mode)
             if ev:
-                ev[3].record(stream)
+                ev[3].record()
         qta.taco_decompress(d_g, g, y, in_dt)
         if ev:
-            ev[4].record(stream)
+            ev[4].record()
         if n_state:
             qta.taco_update_scale(states, n_state)
         if ev:
-            ev[5].record(stream)
+            ev[5].record()
         launches[0] += (3 if fused else 4) + int(n_state > 0)
 
     fused = args.path == "fused"

@@ -245,6 +245,16 @@ qta_status taco_update_scale(float* state, int64_t n_tensors, qta_stream_t strea
  * src, dst: device, 16-byte aligned, non-overlapping; bytes % 16 == 0. */
 qta_status qta_copy(const void* src, void* dst, size_t bytes, qta_stream_t stream);
 
+/* qta_wait_self_test -- exercises the failure path of the bounded pipeline
+ * waits: a one-warp kernel waits on a shared-memory mbarrier through the
+ * same wait routine every kernel uses.  complete != 0: one thread arrives
+ * first and the wait succeeds at once.  complete == 0: nothing ever arrives;
+ * after the wait's limit (about 2 s) the kernel records the timeout flag
+ * (qta_device_error bit 0) and returns -- no trap, the context stays usable.
+ * (Not an operation of the pages: a check of this library's failure
+ * detection.) */
+qta_status qta_wait_self_test(int32_t complete, qta_stream_t stream);
+
 /* qta_device_error -- synchronises the current device, returns the flags
  * kernels recorded (0 = none; bit 0: a pipeline wait timed out) in *flags,
  * and clears them when `clear` is non-zero. */

@@ -79,11 +79,13 @@ def lib():
         L.qar_dequant_add.argtypes = [PD, PQ, vp, i32, vp, vp]
         L.qar_dequant_add_requant.argtypes = [PD, PQ, vp, i32, PQ, i32, vp]
         L.qta_sq_error.argtypes = [vp, i32, vp, i64, vp, vp]
+        L.qta_wait_self_test.argtypes = [i32, vp]
         L.taco_update_scale.argtypes = [vp, i64, vp]
         L.qta_copy.argtypes = [vp, vp, sz, vp]
         L.qta_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
         for name in ("taco_compress", "taco_decompress", "qar_reduce", "qar_requant", "qar_reduce_requant",
-                     "qar_dequant_add", "qar_dequant_add_requant", "qta_sq_error", "taco_update_scale", "qta_copy",
+                     "qar_dequant_add", "qar_dequant_add_requant", "qta_sq_error", "qta_wait_self_test",
+                     "taco_update_scale", "qta_copy",
                      "qta_device_error"):
             getattr(L, name).restype = ctypes.c_int
         L.qta_status_string.argtypes = [ctypes.c_int]
@@ -237,6 +239,10 @@ def qar_dequant_add_requant(d: Desc, q_in: QTensor, x, x_dtype: int, out: QTenso
 def qta_sq_error(a, a_dtype: int, b, n: int, out, stream=None) -> None:
     """out (device float64 [1]) = sum of (a - b)^2 over n elements."""
     _check("qta_sq_error", lib().qta_sq_error(_ptr(a), a_dtype, _ptr(b), n, _ptr(out), _stream(stream)))
+
+
+def qta_wait_self_test(complete: bool, stream=None) -> None:
+    _check("qta_wait_self_test", lib().qta_wait_self_test(1 if complete else 0, _stream(stream)))
 
 
 def taco_update_scale(state, n_tensors: int, stream=None) -> None:

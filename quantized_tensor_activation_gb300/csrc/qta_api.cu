@@ -239,6 +239,24 @@ __global__ void __launch_bounds__(512) copy_kernel(const uint4* __restrict__ src
     for (; i < n16; i += stride) __stcs(dst + i, __ldcs(src + i));
 }
 
+// Self-test of the bounded pipeline wait: one warp waits on an mbarrier
+// through mbar_wait, the wait every kernel uses.  With `complete` set, one
+// thread arrives first and the wait succeeds at once; otherwise nothing ever
+// arrives, the wait gives up after its limit, records ERR_WAIT_TIMEOUT and
+// the kernel returns normally.
+__global__ void __launch_bounds__(32) wait_self_test_kernel(int complete, unsigned int* err)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    if (complete && threadIdx.x == 0) mbar_arrive(&bar);
+    __syncwarp();
+    mbar_wait(&bar, 0u, err);
+}
+
 cudaError_t launch_state(float* state, long long n, int op, cudaStream_t stream)
 {
     if (n <= 0) return cudaSuccess;
@@ -564,6 +582,15 @@ qta_status qta_sq_error(const void* a, int32_t a_dtype, const float* b, int64_t 
     const long long blocks = (n + 255) / 256;
     const int grid = static_cast<int>(blocks < 4LL * sms ? (blocks > 0 ? blocks : 1) : 4LL * sms);
     return cuda_status(launch_sq_error(a, a_dtype, b, n, out, grid, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+qta_status qta_wait_self_test(int32_t complete, qta_stream_t stream)
+{
+    int sms = 0, smem_sm = 0;
+    unsigned int* err = nullptr;
+    if (device_info(&sms, &smem_sm, &err) != cudaSuccess) return QTA_ERR_CUDA;
+    wait_self_test_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(complete ? 1 : 0, err);
+    return cuda_status(cudaGetLastError());
 }
 
 qta_status taco_update_scale(float* state, int64_t n_tensors, qta_stream_t stream)
