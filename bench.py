@@ -24,6 +24,7 @@ import hashlib
 import glob
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -173,6 +174,7 @@ def _cpu_oracle_path(w: workloads.Workload, rows: int, seed: int = 0):
     t0 = time.perf_counter()
     st = np.zeros(2 * N, dtype=np.float32) if s1 == orc.TACO_FP8 else None
     c, s, z = orc.compress(s1, B, xb, dt, N, rows, C, st, orc.CURRENT)
+    t1 = time.perf_counter()
     cb = E // 2 if s1 == orc.INT4_ASYM else E
     nb = E // B
     shards = [(c[r * cb:(r + 1) * cb], s[r * nb:(r + 1) * nb], None if z is None else z[r * nb:(r + 1) * nb],
@@ -180,9 +182,25 @@ def _cpu_oracle_path(w: workloads.Workload, rows: int, seed: int = 0):
     gr = max(1, rows // N)
     st2 = np.zeros(2 * N, dtype=np.float32) if s2 == orc.TACO_FP8 else None
     c2, sc2, z2 = orc.reduce_requant(s1, B, shards, rows, C, 0, N * gr, s2, gB, N, st2, orc.CURRENT)
+    t2 = time.perf_counter()
     orc.decompress(s2, gB, c2, sc2, z2, st2, N, gr, C, dt)
-    dt_s = time.perf_counter() - t0
-    return dt_s, 2 * E * N, 1
+    t3 = time.perf_counter()
+    _cpu_oracle_path.stages = {"compress_s": t1 - t0, "reduce_requant_s": t2 - t1, "decompress_s": t3 - t2}
+    return t3 - t0, 2 * E * N, 1
+
+
+def _host_cpu():
+    """The host's logical CPU count and model name (for the CPU-baseline report)."""
+    model = platform.processor() or platform.machine()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"nproc": os.cpu_count(), "cpu_model": model}
 
 
 def run_reference(args, w):
@@ -205,7 +223,8 @@ def run_reference(args, w):
         "config": _config(w),
         "cpu_baseline": {"value": val, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": f"{rows} of {w.rows} rows of each of the {w.ranks} ranks per step "
-                                   f"({w.ranks * rows * w.cols} elements), full path"},
+                                   f"({w.ranks * rows * w.cols} elements), full path",
+                         "stages": dict(_cpu_oracle_path.stages), "host": _host_cpu()},
         "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -664,7 +683,8 @@ def run_qta(args, w):
         dt_s, nbytes, threads = _cpu_oracle_path(w, rows, seed=args.seed)
         cpu = {"value": nbytes / dt_s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"{rows} of {w.rows} rows of each of the {w.ranks} ranks "
-                         f"({w.ranks * rows * w.cols} elements), full path, {dt_s:.1f} s"}
+                         f"({w.ranks * rows * w.cols} elements), full path, {dt_s:.1f} s",
+               "stages": dict(_cpu_oracle_path.stages), "host": _host_cpu()}
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
