@@ -1,16 +1,21 @@
 """Benchmark of the codec's hot path on one GB300 (or N independent replicas).
 
 One step = one pass of the whole path over one batch of synthetic input:
-  K1 taco_compress   all simulated TP ranks (one launch, DELAYED dual-scale)
-  K2 qar_reduce      dequantize the N code planes to FP32 and sum (all rows)
-  K3 qar_requant     requantize the FP32 sum for the gather stage
-  K4 taco_decompress the gathered codes back to the 16-bit dtype
-     taco_update_scale (both stages' per-tensor scales, one launch)
+  K1  taco_compress       all simulated TP ranks (one launch, DELAYED dual-scale)
+  K23 qar_reduce_requant  dequantize the N code planes, sum in FP32 and
+                          requantize for the gather stage (one kernel); with
+                          --path split: K2 qar_reduce + K3 qar_requant
+  K4  taco_decompress     the gathered codes back to the 16-bit dtype
+      taco_update_scale   both stages' per-tensor scales (one launch)
 Metric: GB/s of 16-bit input processed (2 bytes x elements x ranks / step
-time), with the fraction of the measured HBM bandwidth reached by the
-dominant kernel (K1) reported in "roofline".  The timed steps replay the step
-captured once as a CUDA graph (--no-graph: eager launches); per-kernel times
-come from the same step launched eagerly with CUDA events between the calls.
+time); "roofline" gives the fraction of the measured HBM bandwidth the
+dominant kernel (K1) reaches.  The timed steps replay the step captured once
+as a CUDA graph (--no-graph: eager launches).  Per-kernel times come from a
+graph of the same steps with a timing event between every two kernels,
+replayed after the timed region (eager launches if that is unavailable).
+The compress's SM cap is chosen per run from whole steps unless --k1-sms
+fixes it.  Optional reports: --ring (EQuARX adder chains), --sm-sweep,
+--choose-block.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl qta|reference]
 
