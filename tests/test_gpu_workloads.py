@@ -112,3 +112,61 @@ def test_workload_full_size(dev, name):
         assert_same("requant zeros", _rows_of(g.zeros, rows, gsb), np.concatenate([c[2] for c in gcodes]))
     yo = np.concatenate([orc.decompress(ORC_SCH[s2], gB, c, s, z, stj, 1, 1, C, o_dt) for c, s, z, stj in gcodes])
     assert_same("output rows", y[torch.as_tensor(rows, device=dev)], yo)
+
+
+@pytest.mark.parametrize("name", ["taco_tiny", "gpt_tp", "qwen_grad", "equarx_int8", "flash_int4"])
+def test_workload_full_size_fused_as_benched(dev, name):
+    """The timed step's own calls at full size: the compress on a capped SM
+    count (as the benchmark may choose), the fused reduce + requant with the
+    gather stage's per-shard DELAYED scales, the decompress; sampled rows
+    against the oracle's fused function, row by row."""
+    w = workloads.WORKLOADS[name]
+    N, R, C, B, gB = w.ranks, w.rows, w.cols, w.block, w.gather_block
+    s1, s2 = qta.SCHEMES[w.scheme], qta.SCHEMES[w.gather_scheme]
+    in_dt = qta.BF16 if w.dtype == "bf16" else qta.FP16
+    o_dt = orc.BF16 if w.dtype == "bf16" else orc.FP16
+    x = workloads.make_rank_inputs(w, device=dev, seed=11)
+
+    d_in = qta.desc(s1, B, R, C, batch=N, max_sms=144)
+    q = qta.alloc_qtensor(d_in, dev)
+    qta.taco_compress(d_in, x, in_dt, q, qta.SCALE_CURRENT if s1 == qta.TACO_FP8 else qta.SCALE_DELAYED)
+    gr = R // N
+    d_sh = qta.desc(s1, B, R, C)
+    d_g = qta.desc(s2, gB, gr, C, batch=N)
+    g = qta.alloc_qtensor(d_g, dev)
+    S2 = np.zeros(2 * N, dtype=np.float32)
+    S2[0::2] = [2.0 ** -7 * (1 + 0.25 * j) for j in range(N)]
+    if g.state is not None:
+        g.state.copy_(torch.from_numpy(S2))
+    qta.qar_reduce_requant(d_sh, [q.shard(r) for r in range(N)], 0, R, d_g, g, qta.SCALE_DELAYED)
+    y = torch.empty((R, C), dtype=w.torch_dtype, device=dev)
+    qta.taco_decompress(d_g, g, y, in_dt)
+    torch.cuda.synchronize()
+    assert qta.qta_device_error() == 0
+
+    rng = np.random.default_rng(hash(name) % 2 ** 31 + 1)
+    rows = np.unique(np.concatenate([[0, R - 1, gr - 1, gr], rng.choice(R, 8, replace=False)]))
+    k = len(rows)
+    xb = bits(x[:, torch.as_tensor(rows, device=dev)].contiguous().cpu())
+    st = None if s1 != qta.TACO_FP8 else bits(q.state).view(np.float32).copy()   # checked by the test above
+    shards = []
+    for r in range(N):
+        st_r = None if st is None else st[2 * r:2 * r + 2].copy()
+        c, s, z = orc.compress(ORC_SCH[s1], B, xb[r * k * C:(r + 1) * k * C], o_dt, 1, k, C, st_r, orc.DELAYED)
+        shards.append((c, s, z, st_r))
+    gcpr = C // 2 if s2 == qta.INT4_ASYM_G128 else C
+    gsb = {qta.TACO_FP8: 1, qta.INT8_SYM_B64: 4}.get(s2, 2) * (C // gB)
+    want_c, want_s, want_z, want_y = [], [], [], []
+    for i, row in enumerate(rows):
+        j = row // gr
+        stj = None if g.state is None else np.array([S2[2 * j], 0.0], dtype=np.float32)
+        c, s, z = orc.reduce_requant(ORC_SCH[s1], B, shards, k, C, i, i + 1, ORC_SCH[s2], gB, 1, stj, orc.DELAYED)
+        want_c.append(c)
+        want_s.append(s)
+        want_z.append(z)
+        want_y.append(orc.decompress(ORC_SCH[s2], gB, c, s, z, stj, 1, 1, C, o_dt))
+    assert_same("fused codes", _rows_of(g.codes, rows, gcpr), np.concatenate(want_c))
+    assert_same("fused scales", _rows_of(g.scales, rows, gsb), np.concatenate(want_s))
+    if want_z[0] is not None:
+        assert_same("fused zeros", _rows_of(g.zeros, rows, gsb), np.concatenate(want_z))
+    assert_same("output rows", y[torch.as_tensor(rows, device=dev)], np.concatenate(want_y))
