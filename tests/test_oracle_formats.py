@@ -1,9 +1,11 @@
 """Pins of the oracle's number formats against things other than itself.
 
 * E4M3 decode against torch's float8_e4m3fn (a library routine) on all codes.
-* E4M3 encode against an independent nearest-value table search, exhaustively
-  over every binary32 pattern whose magnitude lies in [2^-12, 2^10) and on
-  random patterns over the whole space; against torch's RNE cast in range.
+* E4M3 encode over all 2^32 binary32 patterns: against an independent
+  nearest-value table search for every pattern whose magnitude lies in
+  [2^-12, 2^10); against the constant each remaining pattern must give
+  (signed zero below, +-448 above and for +-Inf, 0x7F for NaN); on random
+  patterns; against torch's RNE cast in range.
 * TACO Fig. 6, Eq. (3): |x - FP8(x)| <= 2^(floor(log2|x|) - m), m = 3.
 * bf16 / fp16 rounding against torch's casts (round-to-nearest-even).
 """
@@ -62,6 +64,24 @@ def test_e4m3_encode_exhaustive_band(orc):
         for sgn in (0, 0x80000000):
             v = (u | np.uint32(sgn)).view(np.float32)
             assert np.array_equal(orc.e4m3_encode(v), _table_search_encode(v)), hex(start)
+
+
+def test_e4m3_encode_every_pattern_outside_the_band(orc):
+    # the remaining binary32 patterns, every one: below the band (|v| < 2^-12,
+    # under a quarter of the smallest subnormal step) the code is a signed zero;
+    # above it (|v| >= 2^10 > 464, and +-Inf) the code saturates to +-448; NaN
+    # gives 0x7F.  With the band test this covers all 2^32 patterns.
+    step = 1 << 24
+    for lo, hi, pos_code, neg_code in ((0, 115 << 23, 0x00, 0x80), (137 << 23, 255 << 23, 0x7E, 0xFE),
+                                       (255 << 23, (255 << 23) + 1, 0x7E, 0xFE)):
+        for start in range(lo, hi, step):
+            u = np.arange(start, min(start + step, hi), dtype=np.uint32)
+            for sgn, code in ((0, pos_code), (0x80000000, neg_code)):
+                got = orc.e4m3_encode((u | np.uint32(sgn)).view(np.float32))
+                assert np.all(got == code), hex(start)
+    nan = np.arange((255 << 23) + 1, 1 << 31, dtype=np.uint32)
+    for sgn in (0, 0x80000000):
+        assert np.all(orc.e4m3_encode((nan | np.uint32(sgn)).view(np.float32)) == 0x7F)
 
 
 def test_e4m3_encode_random_patterns(orc):
