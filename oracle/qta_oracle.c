@@ -8,8 +8,9 @@
  * The pages fix FP32 as the working precision of the method (EQuARX: shards
  * are dequantized to FP32 and summed in FP32; TACO: FP32 per-tensor scale),
  * so the oracle computes in binary32; every integer it produces (a code, a
- * scale byte) is decided in that precision.  Readings of passages the pages
- * leave open are marked R1..R12 and listed in the design notes.
+ * scale byte) is decided in that precision.  Where the pages leave a step
+ * open, the plainest reading that the rest supports is taken; each is stated
+ * where it is used, marked "Reading".
  */
 #include "qta_oracle.h"
 
@@ -22,7 +23,7 @@ static uint32_t f2u(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
 static float u2f(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
 
 /* Round the non-negative integer sig * 2^-shift to the nearest integer,
- * ties to even (R1: every rounding is round-to-nearest-even). */
+ * ties to even (reading: every rounding is round-to-nearest-even). */
 static uint32_t rne_shift(uint32_t sig, int shift)
 {
     if (shift <= 0) return sig << (-shift);
@@ -83,7 +84,7 @@ void orc_e4m3_encode_array(const float* v, uint8_t* out, int64_t n)
 
 /* ------------------------------------------------------------------------
  * bf16 / fp16 (IEEE binary16), round-to-nearest-even, overflow to +-Inf
- * (R11), NaN to a quiet NaN.
+ * (the standard conversion), NaN to a quiet NaN.
  * ---------------------------------------------------------------------- */
 float orc_bf16_to_f32(uint16_t h) { return u2f((uint32_t)h << 16); }
 
@@ -151,7 +152,7 @@ static void store_elem(void* y, int dtype, int64_t i, float v)
 
 /* ------------------------------------------------------------------------
  * Block Hadamard ([TACO] Core claim, Fig. 7, Fig. 8: the Hadamard rotation
- * of the Adaptive Scale-Hadamard transform).  R3: unnormalised Sylvester
+ * of the Adaptive Scale-Hadamard transform).  Reading: unnormalised Sylvester
  * matrix, H[i][j] = (-1)^popcount(i & j), applied as the in-place butterfly
  * with strides h = 1, 2, 4, ..., B/2 in that order; each pair (j, j+h) with
  * j & h == 0 becomes (a + b, a - b) in binary32.
@@ -175,7 +176,7 @@ void orc_fwht_rows(float* y, int64_t nblk, int B)
 /* ------------------------------------------------------------------------
  * Per-tensor FP32 scale of the dual-scale scheme ([TACO] Core claim:
  * dual-scale quantization keeps FP8 stable across training steps).
- * R5: S = amax / 448 from the latest amax (history length one); a zero,
+ * Reading: S = amax / 448 from the latest amax (history length one); a zero,
  * non-finite or sub-normal result falls back to S = 1.
  * ---------------------------------------------------------------------- */
 float orc_scale_from_amax(float amax)
@@ -194,15 +195,16 @@ void orc_taco_update_scale(float* state, int64_t batch)
 }
 
 /* ---- TACO FP8 compress of one tensor ([TACO] Core claim, Fig. 7) ----
- * R2: blocks are B contiguous elements along the hidden (last) axis.
- * R4: block scale r_b = E4M3(a_b / (448 S)) stored as one E4M3 byte relative
+ * Reading: blocks are B contiguous elements along the hidden (last) axis.
+ * Reading: block scale r_b = E4M3(a_b / (448 S)) stored as one E4M3 byte relative
  *     to the per-tensor FP32 scale S; s_b = S * r_b; codes E4M3(y * 1/s_b). */
-/* Dual-scale FP8 quantization of nblk transformed blocks y (R4, R5). */
+/* Dual-scale FP8 quantization of nblk transformed blocks y (block scale and
+ * per-tensor scale as read above). */
 /* mode: ORC_DELAYED or ORC_CURRENT, optionally OR'ed with ORC_ROUND_UP: the
  * block scale r_b is then the smallest E4M3 value not below a_b / (448 S)
  * instead of the nearest one, so that y / s_b stays within 448 whenever S
- * covers the tensor (no saturated codes; SURVEY's "round r_b up" variant of
- * [TACO] Fig. 7's dual scale). */
+ * covers the tensor (no saturated codes: the rounding alternative to the
+ * nearest block scale of [TACO] Fig. 7's dual scale). */
 static void taco_quantize_blocks(const float* y, int64_t nblk, int B, float* st, int mode,
                                  uint8_t* codes, uint8_t* scales)
 {
@@ -250,7 +252,7 @@ static int taco_compress_tensor(const void* x, int dtype, int64_t off, int64_t E
 
 /* ---- block-symmetric INT8, one FP32 scale per 64 ([EQuARX] What carries
  * the argument: Qp1 computes the absmax metadata, Qp2 scales the data).
- * R6: the 64 entries of one scale are 64 contiguous elements. */
+ * Reading: the 64 entries of one scale are 64 contiguous elements. */
 static void int8sym_compress_tensor(const void* x, int dtype, int64_t off, int64_t E,
                                     int8_t* codes, float* scales)
 {
@@ -272,9 +274,9 @@ static void int8sym_compress_tensor(const void* x, int dtype, int64_t off, int64
 
 /* ---- asymmetric group-128 INT4 / INT8 ([FLASH] What carries the argument,
  * Assumptions & free parameters: g = 128, fp16 scale + zero-point per group).
- * R7: min/max affine quantizer with a floating zero-point equal to the group
+ * Reading: min/max affine quantizer with a floating zero-point equal to the group
  * minimum: s = fp16((max-min)/Q), z = fp16(min), q = clamp(rint((x-z)/s)).
- * R8: INT4 codes, element 2k in the low nibble of byte k, 2k+1 in the high. */
+ * Reading: INT4 codes, element 2k in the low nibble of byte k, 2k+1 in the high. */
 static void asym_compress_tensor(const void* x, int dtype, int64_t off, int64_t E,
                                  int bits, uint8_t* codes, uint16_t* scales,
                                  uint16_t* zeros)
@@ -374,7 +376,7 @@ static void code_and_scale(int scheme, int B, const void* codes, const void* sca
 
 /* Dequantized value of element e (flat index within one tensor) in FP32.
  * TACO: E4M3 code times s_b = S * r_b, before the inverse transform.
- * INT8: q * s.  ASYM: fmaf(q, s, z) (one rounding, R7). */
+ * INT8: q * s.  ASYM: fmaf(q, s, z) (one rounding, the asymmetric reading above). */
 static float dequant(int scheme, int B, const void* codes, const void* scales,
                      const void* zeros, const float* st, int64_t e)
 {
@@ -438,7 +440,7 @@ int orc_decompress(int scheme, int B, const void* codes, const void* scales,
 /* Dequantize-reduce ([EQuARX] What carries the argument: each received shard
  * is converted to FP32 first and the partial sums are kept in FP32;
  * [FLASH] What carries the argument: local FP32 sum after the All2All).
- * R9: per element, in rank order r = 0 .. N-1, with the dequantized term in
+ * Reading: per element, in rank order r = 0 .. N-1, with the dequantized term in
  * FP32 arithmetic entering the FP32 partial sum:
  *   TACO, INT8:  acc = code_0 * s_0;  acc = fmaf(code_r, s_r, acc)
  *                (the product code * scale is exact inside the fused
@@ -447,7 +449,7 @@ int orc_decompress(int scheme, int B, const void* codes, const void* scales,
  * TACO sums in the Hadamard domain and applies the inverse transform once to
  * the sum (then 1/B). */
 /* The per-element sums of rows [row_begin, row_end) before any transform
- * (R9), written to acc. */
+ * (the rank-order reading above), written to acc. */
 static void reduce_sums(int scheme, int B, int n_ranks, const void* const* codes,
                         const void* const* scales, const void* const* zeros,
                         const float* const* states, int64_t cols, int64_t row_begin,
@@ -497,7 +499,7 @@ int orc_reduce(int scheme, int B, int n_ranks, const void* const* codes,
  * domain of the output blocks -- they are the transform of the reduced rows
  * -- so they are requantized there directly (the inverse and the forward
  * transform, which cancel, are not applied).  Every other pair: qar_reduce
- * then the compress of its FP32 rows (R10). */
+ * then the compress of its FP32 rows. */
 int orc_reduce_requant(int scheme, int B, int n_ranks, const void* const* codes,
                        const void* const* scales, const void* const* zeros,
                        const float* const* states, int64_t rows, int64_t cols,

@@ -337,7 +337,7 @@ def _round_f32(x):
 
 @pytest.mark.parametrize("scheme,B", [(0, 128), (1, 64)])
 def test_reduce_accumulates_with_one_rounding_per_rank(orc, scheme, B):
-    # R9: acc = RN(c0*s0), then acc = RN(c1*s1 + acc) with the product exact
+    # rank-order sum: acc = RN(c0*s0), then acc = RN(c1*s1 + acc) with the product exact
     # (a fused multiply-add); emulated here with exact rationals.
     from fractions import Fraction
     rows, cols = 2, 256
