@@ -104,6 +104,9 @@ struct AccumParams {
     int round_up;
 };
 
+// Per-tensor amax slots of a CTA's shared-memory table (see AMAX_SLOTS).
+constexpr int AMAX_SLOTS_CFG = 64;
+
 // ------------------------------------------------------------ configuration
 // Per kernel family: warps per CTA (one CTA per SM; __launch_bounds__ caps
 // the registers at 64K / threads), stages of the per-warp TMA ring, and
@@ -118,7 +121,8 @@ struct CompressCfg {
     static constexpr int OUT_BYTES = 32 * OUT_SEG;
     static constexpr int OUT_BUFS = (IN == IN_FP32) ? 1 : 2;
     static constexpr int WARP_SMEM = STAGES * IN_BYTES + OUT_BUFS * OUT_BYTES;
-    static constexpr int SMEM = WARPS * WARP_SMEM + WARPS * STAGES * 8 + 1024;
+    static constexpr int AMAX_BYTES = (SCH == S_TACO) ? 4 * AMAX_SLOTS_CFG : 0;
+    static constexpr int SMEM = WARPS * WARP_SMEM + WARPS * STAGES * 8 + AMAX_BYTES + 1024;
 };
 
 template <int SCH, int OUT>
@@ -153,7 +157,8 @@ struct ReduceCfg {
     static constexpr int OUT_BYTES = 32 * OUT_SEG;
     static constexpr int OUT_BUFS = 1;
     static constexpr int WARP_SMEM = STAGES * IN_BYTES + OUT_BUFS * OUT_BYTES;
-    static constexpr int SMEM = WARPS * WARP_SMEM + WARPS * STAGES * 8 + 1024;
+    static constexpr int AMAX_BYTES = (OSCH == S_TACO) ? 4 * AMAX_SLOTS_CFG : 0;
+    static constexpr int SMEM = WARPS * WARP_SMEM + WARPS * STAGES * 8 + AMAX_BYTES + 1024;
 };
 
 // Ring hop: a stage holds a warp tile of incoming codes (2 KB slot) and of
@@ -169,7 +174,8 @@ struct AccumCfg {
     static constexpr int STAGE_BYTES = IN_BYTES + X_BYTES;
     static constexpr int OUT_BYTES = 32 * (F32O ? 256 : 64);
     static constexpr int WARP_SMEM = STAGES * STAGE_BYTES + OUT_BYTES;
-    static constexpr int SMEM = WARPS * WARP_SMEM + WARPS * STAGES * 8 + 1024;
+    static constexpr int AMAX_BYTES = (OSCH == S_TACO) ? 4 * AMAX_SLOTS_CFG : 0;
+    static constexpr int SMEM = WARPS * WARP_SMEM + WARPS * STAGES * 8 + AMAX_BYTES + 1024;
 };
 
 __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw)
@@ -340,18 +346,71 @@ __device__ __forceinline__ void store_out16or32(const CUtensorMap* map, const ui
     }
 }
 
-// Per-tensor amax accumulation for the dual-scale state: a running max per
-// warp while consecutive warp tiles stay inside one tensor, flushed with one
-// atomicMax (non-negative floats order like their bit patterns).
+// ------------------------------------------------------------ quantizer
+// Per-tensor amax of the dual-scale state (non-negative floats order like
+// their bit patterns, so max is an unsigned atomicMax).  A CTA first gathers
+// the amax of the first AMAX_SLOTS tensors in a shared-memory table and adds
+// it to the global state once per tensor at its end: the warps of a fused
+// reduce switch output tensor almost every tile, and one global atomic per
+// tile on a handful of addresses serializes.
+constexpr int AMAX_SLOTS = AMAX_SLOTS_CFG;
+
+struct QuantOut {
+    void* scales;
+    void* zeros;
+    float* state;
+    int M;                  // segments of the quantized tensor (all batches)
+    int lanes_per_block;
+    int lanes_log2;
+    FastDiv seg_per_tensor;
+    int round_up;           // TACO block scales: smallest E4M3 value >= the ratio
+    unsigned int* cta_amax; // shared-memory amax table of the CTA (TACO)
+    int amax_slots;         // tensors [0, amax_slots) use the table
+};
+
+__device__ __forceinline__ void amax_add(const QuantOut& o, int tensor, uint32_t bits)
+{
+    if (tensor < o.amax_slots)
+        atomicMax(o.cta_amax + tensor, bits);
+    else
+        atomicMax(reinterpret_cast<unsigned int*>(o.state + 2 * tensor + 1), bits);
+}
+
+// Zero the CTA's table (every thread calls it once, before any tile).
+__device__ __forceinline__ void cta_amax_init(unsigned int* table)
+{
+    for (int i = threadIdx.x; i < AMAX_SLOTS; i += blockDim.x) table[i] = 0u;
+    __syncthreads();
+}
+
+// Number of table slots in use for a quantized tensor of M segments.
+__device__ __forceinline__ int cta_amax_slots(int M, const FastDiv& spt)
+{
+    const int n = static_cast<int>((static_cast<uint32_t>(M) + spt.d - 1u) / spt.d);
+    return n < AMAX_SLOTS ? n : AMAX_SLOTS;
+}
+
+// Add the CTA's table to the global state (every thread calls it once, after
+// its last tile and its warp's final flush).
+__device__ __forceinline__ void cta_amax_flush(const unsigned int* table, float* state, int slots)
+{
+    __syncthreads();
+    for (int i = threadIdx.x; i < slots; i += blockDim.x) {
+        const unsigned int v = table[i];
+        if (v != 0u) atomicMax(reinterpret_cast<unsigned int*>(state + 2 * i + 1), v);
+    }
+}
+
+// Running max per warp while consecutive warp tiles stay inside one tensor,
+// flushed into the table (or the global state) when the tensor changes.
 struct AmaxTracker {
     int tensor = -1;
     float m = 0.0f;
 
-    __device__ __forceinline__ void flush(float* state, int lane)
+    __device__ __forceinline__ void flush(const QuantOut& o, int lane)
     {
         const uint32_t w = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
-        if (lane == 0 && tensor >= 0 && w != 0u)
-            atomicMax(reinterpret_cast<unsigned int*>(state + 2 * tensor + 1), w);
+        if (lane == 0 && tensor >= 0 && w != 0u) amax_add(o, tensor, w);
         m = 0.0f;
     }
 };
@@ -369,18 +428,6 @@ __device__ __forceinline__ void drain_ring(uint64_t* bars, int stages, int stage
     }
 }
 
-// ------------------------------------------------------------ quantizer
-// Output side of a quantization: where the per-block metadata goes.
-struct QuantOut {
-    void* scales;
-    void* zeros;
-    float* state;
-    int M;                  // segments of the quantized tensor (all batches)
-    int lanes_per_block;
-    int lanes_log2;
-    FastDiv seg_per_tensor;
-    int round_up;           // TACO block scales: smallest E4M3 value >= the ratio
-};
 
 // Quantizes one warp tile (one 64-element segment per lane, values in the
 // original domain) into code words `ow`, writes the per-block metadata and
@@ -428,12 +475,12 @@ struct Quantizer {
             const float a = absmax64(v);
             if (uniform) {
                 if (tens != amax.tensor) {
-                    amax.flush(o.state, lane);
+                    amax.flush(o, lane);
                     amax.tensor = tens;
                 }
                 amax.m = fmaxf(amax.m, a);
             } else if (valid && a > 0.0f) {
-                atomicMax(reinterpret_cast<unsigned int*>(o.state + 2 * tens + 1), __float_as_uint(a));
+                amax_add(o, tens, __float_as_uint(a));
             }
             if constexpr (!AMAX_ONLY) {
                 if (!uniform || tens != cached_tensor) {
@@ -529,7 +576,7 @@ struct Quantizer {
 
     __device__ __forceinline__ void finish(const QuantOut& o, int lane)
     {
-        if constexpr (SCH == S_TACO) amax.flush(o.state, lane);
+        if constexpr (SCH == S_TACO) amax.flush(o, lane);
     }
 };
 
@@ -576,6 +623,7 @@ compress_kernel(const __grid_constant__ CompressParams p)
     uint8_t* wb = smem + warp * C::WARP_SMEM;
     uint8_t* outb = wb + C::STAGES * C::IN_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::WARPS * C::WARP_SMEM) + warp * C::STAGES;
+    unsigned int* amax_tab = reinterpret_cast<unsigned int*>(smem + C::WARPS * C::WARP_SMEM + C::WARPS * C::STAGES * 8);
 
     const int W = gridDim.x * C::WARPS;
     const int first = blockIdx.x * C::WARPS + warp;
@@ -583,6 +631,7 @@ compress_kernel(const __grid_constant__ CompressParams p)
         for (int s = 0; s < C::STAGES; ++s) mbar_init(&bars[s], 1);
         fence_barrier_init();
     }
+    if constexpr (SCH == S_TACO) cta_amax_init(amax_tab);
     pdl_wait();
     pdl_trigger();
     if (lane == 0) {
@@ -595,7 +644,7 @@ compress_kernel(const __grid_constant__ CompressParams p)
     __syncwarp();
 
     const QuantOut qo{p.scales, p.zeros, p.state, p.M, p.lanes_per_block, p.lanes_log2, p.seg_per_tensor,
-                      p.round_up};
+                      p.round_up, amax_tab, (SCH == S_TACO) ? cta_amax_slots(p.M, p.seg_per_tensor) : 0};
     Quantizer<SCH> quant;
     int stage = 0;
     uint32_t phase = 0;
@@ -633,6 +682,7 @@ compress_kernel(const __grid_constant__ CompressParams p)
         bulk_wait_all();
         if (aborted) drain_ring(bars, C::STAGES, stage, phase, p.err);
     }
+    if constexpr (SCH == S_TACO) cta_amax_flush(amax_tab, p.state, qo.amax_slots);
 }
 
 // ------------------------------------------------------------ decompress
@@ -838,6 +888,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
     uint8_t* wb = smem + warp * C::WARP_SMEM;
     uint8_t* outb = wb + C::STAGES * C::IN_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::WARPS * C::WARP_SMEM) + warp * C::STAGES;
+    unsigned int* amax_tab = reinterpret_cast<unsigned int*>(smem + C::WARPS * C::WARP_SMEM + C::WARPS * C::STAGES * 8);
     const int W = gridDim.x * C::WARPS;
     const int first = blockIdx.x * C::WARPS + warp;
     const int n = p.n_ranks;
@@ -848,6 +899,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
         for (int s = 0; s < C::STAGES; ++s) mbar_init(&bars[s], 1);
         fence_barrier_init();
     }
+    if constexpr (OSCH == S_TACO) cta_amax_init(amax_tab);
     pdl_wait();
     pdl_trigger();
     if (lane == 0) {
@@ -865,7 +917,8 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
     int unit = 0;
     bool aborted = false;
     const QuantOut qo{p.q_scales, p.q_zeros, p.q_state, p.M_out, p.q_lanes_per_block, p.q_lanes_log2,
-                      p.q_seg_per_tensor, p.q_round_up};
+                      p.q_seg_per_tensor, p.q_round_up, amax_tab,
+                      (OSCH == S_TACO) ? cta_amax_slots(p.M_out, p.q_seg_per_tensor) : 0};
     Quantizer<(OSCH == OUT_F32) ? S_TACO : OSCH> quant;
     SegMeta<SCH> nxt[RANK_CHUNK];
     if (my_tiles > 0) reduce_meta_load<SCH, RANK_CHUNK>(p, 0, 0, first, W, lane, nxt);
@@ -953,6 +1006,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
         bulk_wait_all();
         if (aborted) drain_ring(bars, C::STAGES, stage, phase, p.err);
     }
+    if constexpr (OSCH == S_TACO) cta_amax_flush(amax_tab, p.q_state, qo.amax_slots);
 }
 
 // ------------------------------------------------------------ ring hop
@@ -974,6 +1028,7 @@ accum_kernel(const __grid_constant__ AccumParams p)
     uint8_t* wb = smem + warp * C::WARP_SMEM;
     uint8_t* outb = wb + C::STAGES * C::STAGE_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::WARPS * C::WARP_SMEM) + warp * C::STAGES;
+    unsigned int* amax_tab = reinterpret_cast<unsigned int*>(smem + C::WARPS * C::WARP_SMEM + C::WARPS * C::STAGES * 8);
     const int W = gridDim.x * C::WARPS;
     const int first = blockIdx.x * C::WARPS + warp;
     auto issue = [&](int s, int wt) {
@@ -991,6 +1046,7 @@ accum_kernel(const __grid_constant__ AccumParams p)
         for (int s = 0; s < C::STAGES; ++s) mbar_init(&bars[s], 1);
         fence_barrier_init();
     }
+    if constexpr (OSCH == S_TACO) cta_amax_init(amax_tab);
     pdl_wait();
     pdl_trigger();
     if (lane == 0) {
@@ -1003,7 +1059,7 @@ accum_kernel(const __grid_constant__ AccumParams p)
     __syncwarp();
     const int L = p.lanes_per_block;
     const QuantOut qo{p.q_scales, p.q_zeros, p.q_state, p.M, p.lanes_per_block, p.lanes_log2, p.seg_per_tensor,
-                      p.round_up};
+                      p.round_up, amax_tab, (OSCH == S_TACO) ? cta_amax_slots(p.M, p.seg_per_tensor) : 0};
     Quantizer<(OSCH == OUT_F32) ? S_TACO : OSCH> quant;
     int stage = 0;
     uint32_t phase = 0;
@@ -1079,6 +1135,7 @@ accum_kernel(const __grid_constant__ AccumParams p)
         bulk_wait_all();
         if (aborted) drain_ring(bars, C::STAGES, stage, phase, p.err);
     }
+    if constexpr (OSCH == S_TACO) cta_amax_flush(amax_tab, p.q_state, qo.amax_slots);
 }
 
 // ------------------------------------------------------------ small kernels
