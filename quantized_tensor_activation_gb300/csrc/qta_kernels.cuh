@@ -150,13 +150,18 @@ struct ReduceCfg {
     static constexpr int WARPS = W16 ? 16 : 12;
     static constexpr int IN_SEG = (SCH == S_ASYM4) ? 32 : 64;
     static constexpr int OUT_SEG = (OSCH == OUT_F32) ? 256 : (OSCH == S_ASYM4) ? 32 : 64;
-    static constexpr int STAGES = (OSCH == OUT_F32) ? 4 : ((SCH == S_ASYM4) ? 12 : 8);
+    // ranks whose warp tiles share one stage (one load barrier, one wait):
+    // the 1 KB INT4 tiles of the fused kernel are loaded two ranks at a time
+    static constexpr int RPU = (SCH == S_ASYM4 && OSCH != OUT_F32) ? 2 : 1;
+    static constexpr int STAGES = (OSCH == OUT_F32) ? 4 : ((SCH == S_ASYM4) ? 12 / RPU : 8);
     // ranks whose scale metadata is fetched together, one chunk ahead
     static constexpr int RANK_CHUNK = W16 ? 8 : 4;
+    static_assert(RANK_CHUNK % RPU == 0, "a stage never spans two metadata chunks");
     static constexpr int IN_BYTES = 32 * IN_SEG;
+    static constexpr int STAGE_BYTES = RPU * IN_BYTES;
     static constexpr int OUT_BYTES = 32 * OUT_SEG;
     static constexpr int OUT_BUFS = 1;
-    static constexpr int WARP_SMEM = STAGES * IN_BYTES + OUT_BUFS * OUT_BYTES;
+    static constexpr int WARP_SMEM = STAGES * STAGE_BYTES + OUT_BUFS * OUT_BYTES;
     static constexpr int AMAX_BYTES = (OSCH == S_TACO) ? 4 * AMAX_SLOTS_CFG : 0;
     static constexpr int SMEM = WARPS * WARP_SMEM + WARPS * STAGES * 8 + AMAX_BYTES + 1024;
 };
@@ -734,7 +739,8 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
     uint8_t* outb = wb + C::STAGES * C::IN_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::WARPS * C::WARP_SMEM) + warp * C::STAGES;
     const int W = gridDim.x * C::WARPS;
-    const int first = blockIdx.x * C::WARPS + warp;
+    // warp-major: the tiles of the last, partial round spread over all CTAs
+    const int first = warp * gridDim.x + blockIdx.x;
     if (lane == 0) {
         for (int s = 0; s < C::STAGES; ++s) mbar_init(&bars[s], 1);
         fence_barrier_init();
@@ -822,9 +828,10 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
 // issuing lane walks them with a cursor (tile index t, rank r).
 struct UnitCursor {
     int t = 0, r = 0;
-    __device__ __forceinline__ void advance(int n_ranks)
+    __device__ __forceinline__ void advance(int n_ranks, int ranks_per_unit = 1)
     {
-        if (++r == n_ranks) {
+        r += ranks_per_unit;
+        if (r >= n_ranks) {
             r = 0;
             ++t;
         }
@@ -837,8 +844,13 @@ __device__ __forceinline__ void reduce_issue(const ReduceParams& p, uint8_t* wb,
 {
     using C = ReduceCfg<SCH, OSCH>;
     const int wt = first + u.t * W;
-    mbar_arrive_expect_tx(&bars[stage], C::IN_BYTES);
-    tma_load_2d(wb + stage * C::IN_BYTES, &p.in_map[u.r], 0, p.seg_begin + wt * 32, &bars[stage]);
+    const int nr = min(C::RPU, p.n_ranks - u.r);
+    mbar_arrive_expect_tx(&bars[stage], nr * C::IN_BYTES);
+#pragma unroll
+    for (int i = 0; i < C::RPU; ++i)
+        if (i < nr)
+            tma_load_2d(wb + stage * C::STAGE_BYTES + i * C::IN_BYTES, &p.in_map[u.r + i], 0,
+                        p.seg_begin + wt * 32, &bars[stage]);
 }
 
 // Ranks are processed in chunks of RANK_CHUNK; the scale metadata of the next
@@ -886,14 +898,15 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
     uint8_t* smem = aligned_smem(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t* wb = smem + warp * C::WARP_SMEM;
-    uint8_t* outb = wb + C::STAGES * C::IN_BYTES;
+    uint8_t* outb = wb + C::STAGES * C::STAGE_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::WARPS * C::WARP_SMEM) + warp * C::STAGES;
     unsigned int* amax_tab = reinterpret_cast<unsigned int*>(smem + C::WARPS * C::WARP_SMEM + C::WARPS * C::STAGES * 8);
     const int W = gridDim.x * C::WARPS;
-    const int first = blockIdx.x * C::WARPS + warp;
+    // warp-major: the tiles of the last, partial round spread over all CTAs
+    const int first = warp * gridDim.x + blockIdx.x;
     const int n = p.n_ranks;
     const int my_tiles = (first < p.n_warp_tiles) ? (p.n_warp_tiles - first + W - 1) / W : 0;
-    const int total_units = my_tiles * n;
+    const int total_units = my_tiles * ((n + C::RPU - 1) / C::RPU);
     UnitCursor next_unit;   // next unit to load (meaningful in lane 0)
     if (lane == 0) {
         for (int s = 0; s < C::STAGES; ++s) mbar_init(&bars[s], 1);
@@ -905,7 +918,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
     if (lane == 0) {
         for (int u = 0; u < C::STAGES && u < total_units; ++u) {
             reduce_issue<SCH, OSCH>(p, wb, bars, u, next_unit, first, W);
-            next_unit.advance(n);
+            next_unit.advance(n, C::RPU);
         }
     }
     __syncwarp();
@@ -938,28 +951,34 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
             for (int kk = 0; kk < RANK_CHUNK; ++kk) {
                 const int r = c * RANK_CHUNK + kk;
                 if (r >= n) break;
-                const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[stage], phase, p.err));
-                if (!ok) {
-                    aborted = true;
-                    break;
+                const int slot = kk % C::RPU;   // this rank's tile within the stage
+                if (slot == 0) {
+                    const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[stage], phase, p.err));
+                    if (!ok) {
+                        aborted = true;
+                        break;
+                    }
                 }
                 float s, z;
                 cur[kk].decode(s, z);
                 const uint16_t s16 = static_cast<uint16_t>(cur[kk].raw);
+                const uint8_t* tile = wb + stage * C::STAGE_BYTES + slot * C::IN_BYTES;
                 if (r == 0)
-                    dequant_segment<SCH, 0>(wb + stage * C::IN_BYTES, lane, s, z, acc, s16);
+                    dequant_segment<SCH, 0>(tile, lane, s, z, acc, s16);
                 else
-                    dequant_segment<SCH, 1>(wb + stage * C::IN_BYTES, lane, s, z, acc, s16);
-                __syncwarp();
-                if (lane == 0 && unit + C::STAGES < total_units) {
-                    fence_proxy_async_smem();
-                    reduce_issue<SCH, OSCH>(p, wb, bars, stage, next_unit, first, W);
-                    next_unit.advance(n);
-                }
-                ++unit;
-                if (++stage == C::STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
+                    dequant_segment<SCH, 1>(tile, lane, s, z, acc, s16);
+                if (slot == C::RPU - 1 || r == n - 1) {
+                    __syncwarp();
+                    if (lane == 0 && unit + C::STAGES < total_units) {
+                        fence_proxy_async_smem();
+                        reduce_issue<SCH, OSCH>(p, wb, bars, stage, next_unit, first, W);
+                        next_unit.advance(n, C::RPU);
+                    }
+                    ++unit;
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
             }
         }
