@@ -34,9 +34,10 @@ def _step(scheme, B, gscheme, gB, x, n, rows, cols, max_sms):
 
 @pytest.mark.parametrize("scheme,B,gscheme,gB", [("taco_fp8", 128, "taco_fp8", 128),
                                                   ("int4_asym", 128, "int8_asym", 128)])
-def test_same_bytes_with_fewer_sms(scheme, B, gscheme, gB):
+@pytest.mark.parametrize("n,rows", [(4, 96), (5, 120)])   # 5: a stage of the INT4 reduce holds a lone rank
+def test_same_bytes_with_fewer_sms(scheme, B, gscheme, gB, n, rows):
     dev = device()
-    n, rows, cols = 4, 96, 1024
+    cols = 1024
     x = to_dtype_cpu(random_values(np.random.default_rng(2), (n, rows, cols), "mixed"), qta.BF16).to(dev)
     ref = _step(scheme, B, gscheme, gB, x, n, rows, cols, 0)
     for m in (1, 7):
