@@ -436,6 +436,103 @@ __device__ __forceinline__ void fwht_cross(u64 (&v)[32], int lanes_per_block, in
     }
 }
 
+// Halved exchange ("exchange layout").  In the cross-lane stages above every
+// lane ships all 64 of its values to its partner.  Here each lane ships only
+// the half whose outputs it does not keep, so a stage costs 32 shuffles
+// instead of 64, and afterwards the lanes of a block own a block-wide strip
+// of positions in every row rather than a row each.  To let both partners ship
+// the same registers, lane c of a block keeps position j of its row in slot
+// j ^ xm(c), xm = 32 (c & 1) + 16 (c >> 1 & 1) (the second term only when
+// 4 lanes share a block).
+__device__ __forceinline__ uint32_t xl_mask(int lanes_per_block, int lane)
+{
+    return (lanes_per_block >= 2 ? (lane & 1) * 32u : 0u) | (lanes_per_block == 4 ? ((lane >> 1) & 1) * 16u : 0u);
+}
+
+// fwht64_local on the permuted slots: stages with stride 16 and 32 see the
+// lower and upper position of a pair swapped in the lanes whose mask has that
+// bit.  With A, B the slots of a pair and s = -1 in those lanes (else +1):
+// A' = fma(A, s, B), B' = fma(B, -s, A), which is (a+b, a-b) in position
+// order with one rounding each, identical to the add / subtract.
+__device__ __forceinline__ void fwht64_local_xl(u64 (&v)[32], uint32_t xm)
+{
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const float2 t = up2(v[j]);
+        v[j] = pk2(__fadd_rn(t.x, t.y), __fsub_rn(t.x, t.y));
+    }
+#pragma unroll
+    for (int hp = 1; hp < 8; hp <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 2 * hp) {
+#pragma unroll
+            for (int j = i; j < i + hp; ++j) {
+                const u64 a = v[j], b = v[j + hp];
+                v[j] = add2(a, b);
+                v[j + hp] = sub2(a, b);
+            }
+        }
+    }
+#pragma unroll
+    for (int hp = 8; hp < 32; hp <<= 1) {
+        const float s = (xm & (2u * hp)) ? -1.0f : 1.0f;
+        const u64 s2 = pk2(s, s), ns2 = pk2(-s, -s);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2 * hp) {
+#pragma unroll
+            for (int j = i; j < i + hp; ++j) {
+                const u64 a = v[j], b = v[j + hp];
+                v[j] = fma2(a, s2, b);
+                v[j + hp] = fma2(b, ns2, a);
+            }
+        }
+    }
+}
+
+// Strides 64 and 128 with the halved exchange, on the permuted slots.  Stage
+// d pairs lane c with c ^ d.  Each lane keeps the lower half of every group of
+// registers and ships the upper half, which holds the partner's kept
+// positions.  With a = the kept value, o = the partner's value there and
+// s = +1 in the upper lane (else -1): lower row a+o, upper row
+// fma(o, s, -s*a) = (lower - upper), both rounded once as in fwht_cross
+// (-s*a is exact).  A sign-bit XOR in place of the multiply measured slower.  Afterwards, with 4 lanes per block, registers 0-7, 8-15,
+// 16-23, 24-31 hold rows 0, 2, 1, 3 of the block.  With 2 lanes, registers
+// 0-15 and 16-31 hold rows 0 and 1.  Register 2i+t of a group holds position
+// xm + 2i + t.
+__device__ __forceinline__ void fwht_cross_xl(u64 (&v)[32], int lanes_per_block, int lane)
+{
+    if (lanes_per_block >= 2) {
+        const float s = (lane & 1) ? 1.0f : -1.0f;
+        const u64 s2 = pk2(s, s), ns2 = pk2(-s, -s);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const u64 o = __shfl_xor_sync(0xffffffffu, v[16 + j], 1);
+            const u64 a = v[j];
+            v[j] = add2(a, o);
+            v[16 + j] = fma2(o, s2, mul2(a, ns2));
+        }
+    }
+    if (lanes_per_block == 4) {
+        const float s = (lane & 2) ? 1.0f : -1.0f;
+        const u64 s2 = pk2(s, s), ns2 = pk2(-s, -s);
+#pragma unroll
+        for (int h = 0; h < 32; h += 16)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const u64 o = __shfl_xor_sync(0xffffffffu, v[h + 8 + j], 2);
+                const u64 a = v[h + j];
+                v[h + j] = add2(a, o);
+                v[h + 8 + j] = fma2(o, s2, mul2(a, ns2));
+            }
+    }
+}
+
+// Block row (0 .. lanes-1) held by register group g after fwht_cross_xl.
+__device__ __forceinline__ int xl_group_row(int g, int lanes_log2)
+{
+    return lanes_log2 == 2 ? (((g & 1) << 1) | (g >> 1)) : g;
+}
+
 __device__ __forceinline__ float group_max(float m, int lanes_per_block)
 {
     for (int d = 1; d < lanes_per_block; d <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));

@@ -190,25 +190,25 @@ __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw)
 
 // ------------------------------------------------------------ segment I/O
 // Read this lane's 64-element input segment (row `lane` of a stage) as 32
-// float pairs.
+// float pairs.  xm (a multiple of 16) permutes the slots: slot j receives
+// position j ^ xm (the exchange layout of fwht_cross_xl).
 template <int IN>
-__device__ __forceinline__ void load_segment(const uint8_t* st, int lane, u64 (&v)[32])
+__device__ __forceinline__ void load_segment(const uint8_t* st, int lane, u64 (&v)[32], uint32_t xm = 0)
 {
     if constexpr (IN == IN_FP32) {
+        const uint32_t cx = xm >> 2;   // 16-byte chunks of 4 values, 8 per box
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint8_t* box = st + h * 4096;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint4 w = lds128(box, sw128(lane, c));
-                v[h * 16 + c * 2 + 0] = pk2(__uint_as_float(w.x), __uint_as_float(w.y));
-                v[h * 16 + c * 2 + 1] = pk2(__uint_as_float(w.z), __uint_as_float(w.w));
-            }
+        for (int sc = 0; sc < 16; ++sc) {
+            const uint32_t pc = sc ^ cx;
+            const uint4 w = lds128(st + (pc >> 3) * 4096, sw128(lane, pc & 7u));
+            v[sc * 2 + 0] = pk2(__uint_as_float(w.x), __uint_as_float(w.y));
+            v[sc * 2 + 1] = pk2(__uint_as_float(w.z), __uint_as_float(w.w));
         }
     } else {
+        const uint32_t cx = xm >> 3;   // 16-byte chunks of 8 values
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-            const uint4 w = lds128(st, sw128(lane, c));
+            const uint4 w = lds128(st, sw128(lane, c ^ cx));
             const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k)
@@ -241,12 +241,47 @@ __device__ __forceinline__ void store_segment(uint8_t* ob, int lane, const u64 (
     }
 }
 
-// Byte codes of one segment from a stage (64 bytes, SW64) into 16 words.
-__device__ __forceinline__ void load_codes8(const uint8_t* st, int lane, uint32_t (&q)[16])
+// Output of fwht_cross_xl into the staging rows: register group g (32/L
+// pairs) goes to row (lane & ~(L-1)) + xl_group_row(g) of the warp tile,
+// positions xm .. xm + 64/L - 1.
+template <int OUT>
+__device__ __forceinline__ void store_segment_xl(uint8_t* ob, int lane, const u64 (&v)[32], int lanes_log2,
+                                                 uint32_t xm)
+{
+    const int base = lane & ~((1 << lanes_log2) - 1);
+    if constexpr (OUT == IN_FP32) {
+        const int kl = 4 - lanes_log2;   // log2 of the 16-byte chunks per group
+#pragma unroll
+        for (int sc = 0; sc < 16; ++sc) {
+            const int g = sc >> kl;
+            const uint32_t row = base + xl_group_row(g, lanes_log2);
+            const uint32_t pc = (xm >> 2) + (sc & ((1 << kl) - 1));
+            const u64 a = v[sc * 2], b = v[sc * 2 + 1];
+            sts128(ob + (pc >> 3) * 4096, sw128(row, pc & 7u), make_uint4(lo32(a), hi32(a), lo32(b), hi32(b)));
+        }
+    } else {
+        const int kl = 3 - lanes_log2;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const int g = c >> kl;
+            const uint32_t row = base + xl_group_row(g, lanes_log2);
+            const uint32_t pc = (xm >> 3) + (c & ((1 << kl) - 1));
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                w[k] = (OUT == IN_BF16) ? pair_to_bf16x2(v[c * 4 + k]) : pair_to_f16x2(v[c * 4 + k]);
+            sts128(ob, sw128(row, pc), make_uint4(w[0], w[1], w[2], w[3]));
+        }
+    }
+}
+
+// Byte codes of one segment from a stage (64 bytes, SW64) into 16 words;
+// word group c receives the 16 codes of chunk c ^ cx.
+__device__ __forceinline__ void load_codes8(const uint8_t* st, int lane, uint32_t (&q)[16], uint32_t cx = 0)
 {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        const uint4 w = lds128(st, sw64(lane, c));
+        const uint4 w = lds128(st, sw64(lane, c ^ cx));
         q[c * 4 + 0] = w.x;
         q[c * 4 + 1] = w.y;
         q[c * 4 + 2] = w.z;
@@ -280,7 +315,7 @@ __device__ __forceinline__ void load_codes4(const uint8_t* st, int lane, uint32_
 // own rounding as defined.
 template <int SCH, int MODE>
 __device__ __forceinline__ void dequant_segment(const uint8_t* st, int lane, float s, float z, u64 (&v)[32],
-                                                uint16_t s16)
+                                                uint16_t s16, uint32_t xm = 0)
 {
     const u64 s2 = pk2(s, s);
     const u64 z2 = pk2(z, z);
@@ -305,7 +340,7 @@ __device__ __forceinline__ void dequant_segment(const uint8_t* st, int lane, flo
         }
     } else {
         uint32_t q[16];
-        load_codes8(st, lane, q);
+        load_codes8(st, lane, q, xm >> 4);
 #pragma unroll
         for (int w = 0; w < 16; ++w) {
             if constexpr (SCH == S_TACO) {
@@ -465,15 +500,21 @@ struct Quantizer {
 
     // AMAX_ONLY: transform and record the amax, write nothing else.
     // transformed (TACO): v already holds the Hadamard-domain values.
-    template <bool AMAX_ONLY>
+    // XL (TACO): v holds the lane's row in the permuted slots of xl_mask, the
+    // transform runs with the halved exchange, and ow comes out in its
+    // layout (store_codes<..., true>).
+    template <bool AMAX_ONLY, bool XL = false>
     __device__ __forceinline__ void run(u64 (&v)[32], const QuantOut& o, int tile_first, int lane,
-                                        uint32_t (&ow)[16], bool transformed = false)
+                                        uint32_t (&ow)[16], bool transformed = false, uint32_t xm = 0)
     {
         const int g = tile_first + lane;
         const bool valid = g < o.M;
         const int L = o.lanes_per_block;
         if constexpr (SCH == S_TACO) {
-            if (!transformed) {
+            if constexpr (XL) {
+                fwht64_local_xl(v, xm);
+                fwht_cross_xl(v, L, lane);
+            } else if (!transformed) {
                 fwht64_local(v);
                 fwht_cross(v, L, lane);
             }
@@ -587,9 +628,11 @@ struct Quantizer {
 
 // Stage one warp tile of code words in shared memory and store it with one
 // TMA tensor store (8-bit codes: 64 B rows, SW64; 4-bit: 32 B rows, SW32).
-template <int SCH, int OUT_BUFS>
+// XL: ow is in the layout of fwht_cross_xl: word group g (16/L words) goes
+// to row (lane & ~(L-1)) + xl_group_row(g), codes xm .. xm + 64/L - 1.
+template <int SCH, int OUT_BUFS, bool XL = false>
 __device__ __forceinline__ void store_codes(uint8_t* ob, const CUtensorMap* map, int row, int lane,
-                                            const uint32_t (&ow)[16])
+                                            const uint32_t (&ow)[16], int lanes_log2 = 0, uint32_t xm = 0)
 {
     if (lane == 0) {
         if constexpr (OUT_BUFS == 1)
@@ -598,7 +641,16 @@ __device__ __forceinline__ void store_codes(uint8_t* ob, const CUtensorMap* map,
             bulk_wait_read<1>();
     }
     __syncwarp();
-    if constexpr (SCH == S_ASYM4) {
+    if constexpr (XL) {
+        const int base = lane & ~((1 << lanes_log2) - 1);
+        const int kl = 2 - lanes_log2;   // log2 of the 16-byte chunks per group
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t r = base + xl_group_row(c >> kl, lanes_log2);
+            const uint32_t pc = (xm >> 4) + (c & ((1 << kl) - 1));
+            sts128(ob, sw64(r, pc), make_uint4(ow[4 * c], ow[4 * c + 1], ow[4 * c + 2], ow[4 * c + 3]));
+        }
+    } else if constexpr (SCH == S_ASYM4) {
 #pragma unroll
         for (int c = 0; c < 2; ++c)
             sts128(ob, sw32(lane, c), make_uint4(ow[4 * c], ow[4 * c + 1], ow[4 * c + 2], ow[4 * c + 3]));
@@ -651,6 +703,10 @@ compress_kernel(const __grid_constant__ CompressParams p)
     const QuantOut qo{p.scales, p.zeros, p.state, p.M, p.lanes_per_block, p.lanes_log2, p.seg_per_tensor,
                       p.round_up, amax_tab, (SCH == S_TACO) ? cta_amax_slots(p.M, p.seg_per_tensor) : 0};
     Quantizer<SCH> quant;
+    // TACO: the rows are loaded into the permuted slots of the halved
+    // cross-lane exchange
+    constexpr bool XL = (SCH == S_TACO);
+    const uint32_t xm = XL ? xl_mask(p.lanes_per_block, lane) : 0u;
     int stage = 0;
     uint32_t phase = 0;
     int k = 0;
@@ -664,7 +720,7 @@ compress_kernel(const __grid_constant__ CompressParams p)
             break;
         }
         u64 v[32];
-        load_segment<IN>(wb + stage * C::IN_BYTES, lane, v);
+        load_segment<IN>(wb + stage * C::IN_BYTES, lane, v, xm);
         __syncwarp();
         {   // refill this stage with the tile STAGES ahead
             const int nwt = wt + C::STAGES * W;
@@ -678,9 +734,10 @@ compress_kernel(const __grid_constant__ CompressParams p)
             phase ^= 1u;
         }
         uint32_t ow[16];
-        quant.template run<AMAX_ONLY>(v, qo, wt * 32, lane, ow);
+        quant.template run<AMAX_ONLY, XL>(v, qo, wt * 32, lane, ow, false, xm);
         if constexpr (!AMAX_ONLY)
-            store_codes<SCH, C::OUT_BUFS>(outb + (k % C::OUT_BUFS) * C::OUT_BYTES, &p.out_map, wt * 32, lane, ow);
+            store_codes<SCH, C::OUT_BUFS, XL>(outb + (k % C::OUT_BUFS) * C::OUT_BYTES, &p.out_map, wt * 32, lane,
+                                              ow, p.lanes_log2, xm);
     }
     quant.finish(qo, lane);
     if (lane == 0) {
@@ -757,6 +814,9 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
     }
     __syncwarp();
     const int L = p.lanes_per_block;
+    // TACO: the codes are read into the permuted slots of the halved
+    // cross-lane exchange
+    const uint32_t xm = (SCH == S_TACO) ? xl_mask(L, lane) : 0u;
     int stage = 0;
     uint32_t phase = 0;
     int k = 0;
@@ -780,7 +840,7 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
         float s, z;
         cur.decode(s, z);
         u64 v[32];
-        dequant_segment<SCH, 0>(wb + stage * C::IN_BYTES, lane, s, z, v, static_cast<uint16_t>(cur.raw));
+        dequant_segment<SCH, 0>(wb + stage * C::IN_BYTES, lane, s, z, v, static_cast<uint16_t>(cur.raw), xm);
         __syncwarp();
         {
             const int nwt = wt + C::STAGES * W;
@@ -795,8 +855,8 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
             phase ^= 1u;
         }
         if constexpr (SCH == S_TACO) {
-            fwht64_local(v);
-            fwht_cross(v, L, lane);
+            fwht64_local_xl(v, xm);
+            fwht_cross_xl(v, L, lane);
             const u64 ib = pk2(p.inv_block, p.inv_block);
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = mul2(v[j], ib);
@@ -809,7 +869,10 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
                 bulk_wait_read<1>();
         }
         __syncwarp();
-        store_segment<OUT>(ob, lane, v);
+        if constexpr (SCH == S_TACO)
+            store_segment_xl<OUT>(ob, lane, v, p.lanes_log2, xm);
+        else
+            store_segment<OUT>(ob, lane, v);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {

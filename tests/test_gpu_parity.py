@@ -101,6 +101,73 @@ def test_zero_and_constant_tensors(dev):
             compare_qtensor(f"const {val}", q, ref)
 
 
+def _tie_blocks(rng, n_blocks, B):
+    """Blocks whose butterflies meet exact zeros of every sign: upper half a
+    copy of the lower half (the last stage subtracts equal values), every
+    stride-64 partner equal, blocks of random +0 / -0, and the rest mixed
+    values with signed zeros sprinkled in."""
+    x = random_values(rng, (n_blocks, B), "mixed")
+    kind = rng.integers(0, 4, n_blocks)
+    h = B // 2
+    x[kind == 1, h:] = x[kind == 1, :h]
+    if B >= 128:
+        for lo in range(0, B, 128):
+            x[kind == 2, lo + 64:lo + 128] = x[kind == 2, lo:lo + 64]
+    zeros = np.where(rng.random((n_blocks, B)) < 0.5, np.float32(-0.0), np.float32(0.0))
+    x[kind == 3] = zeros[kind == 3]
+    sprinkle = rng.random((n_blocks, B)) < 0.1
+    x[sprinkle & (kind == 0)[:, None]] = zeros[sprinkle & (kind == 0)[:, None]]
+    return x
+
+
+@pytest.mark.parametrize("B", [64, 128, 256])
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_taco_compress_signed_zeros_and_ties(dev, B, dtype):
+    # the cross-lane stages form (lower - upper) in whichever lane keeps the
+    # position; equal operands and signed zeros must give the oracle's zero
+    # signs, hence its codes (0x00 vs 0x80), bit for bit
+    batch, rows, cols = 3, 21, 1024
+    rng = np.random.default_rng(7 * B + dtype)
+    x = _tie_blocks(rng, batch * rows * cols // B, B).reshape(batch, rows, cols)
+    xt = to_dtype_cpu(x, dtype)
+    for mode in (qta.SCALE_CURRENT, qta.SCALE_DELAYED):
+        state = np.array([0.002, 0.0, 0.0, 0.0, 1e-5, 0.0], dtype=np.float32)
+        _, q = gpu_compress(qta.TACO_FP8, B, xt, dtype, batch, rows, cols, mode, state=state.copy(), dev=dev)
+        ref = oracle_compress(qta.TACO_FP8, B, xt, dtype, batch, rows, cols,
+                              orc.CURRENT if mode == qta.SCALE_CURRENT else orc.DELAYED, state=state.copy())
+        torch.cuda.synchronize()
+        compare_qtensor(f"ties mode {mode}", q, ref)
+
+
+@pytest.mark.parametrize("B", [64, 128, 256])
+@pytest.mark.parametrize("out_dtype", DTYPES)
+def test_taco_decompress_signed_zeros_and_ties(dev, B, out_dtype):
+    # codes drawn from few values with many +-0 (0x00 / 0x80) and with halves
+    # and stride-64 partners repeated, so the inverse butterflies meet equal
+    # operands and signed zeros
+    batch, rows, cols = 2, 19, 1024
+    n = batch * rows * cols
+    rng = np.random.default_rng(11 * B + out_dtype)
+    pool = np.array([0x00, 0x80, 0x00, 0x80, 0x38, 0xB8, 0x01, 0x81, 0x7E, 0xFE], dtype=np.uint8)
+    c = pool[rng.integers(0, pool.size, n)].reshape(-1, B)
+    kind = rng.integers(0, 3, c.shape[0])
+    c[kind == 1, B // 2:] = c[kind == 1, :B // 2]
+    if B >= 128:
+        for lo in range(0, B, 128):
+            c[kind == 2, lo + 64:lo + 128] = c[kind == 2, lo:lo + 64]
+    c = c.reshape(-1)
+    s = rng.integers(0x08, 0x7E, n // B).astype(np.uint8)
+    st = np.array([0.003, 0.0, 1.5, 0.0], dtype=np.float32)
+    d = qta.desc(qta.TACO_FP8, B, rows, cols, batch=batch)
+    q = qta.QTensor(d, torch.from_numpy(c).to(dev), torch.from_numpy(s).to(dev), None, torch.from_numpy(st).to(dev))
+    y = torch.empty((batch, rows, cols), dtype={0: torch.bfloat16, 1: torch.float16, 2: torch.float32}[out_dtype],
+                    device=dev)
+    qta.taco_decompress(d, q, y, out_dtype)
+    ref = orc.decompress(orc.TACO_FP8, B, c, s, None, st, batch, rows, cols, ORC_DT[out_dtype])
+    torch.cuda.synchronize()
+    assert_same("decompress ties", y, ref)
+
+
 @pytest.mark.parametrize("scheme,B", [(qta.TACO_FP8, 64), (qta.TACO_FP8, 128), (qta.TACO_FP8, 256),
                                       (qta.INT8_SYM_B64, 64), (qta.INT4_ASYM_G128, 128),
                                       (qta.INT8_ASYM_G128, 128)])
