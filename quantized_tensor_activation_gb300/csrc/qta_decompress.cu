@@ -17,24 +17,40 @@ int decompress_smem(int scheme, int out_kind)
 }
 
 
-template <int SCH, int OUT>
+template <int SCH, int OUT, int LG = -1>
 static cudaError_t launch_d(const DecompressParams& p, int grid, cudaStream_t stream)
 {
     using C = DecompressCfg<SCH, OUT>;
     static std::atomic<unsigned> done{0};
-    auto fn = decompress_kernel<SCH, OUT>;
+    auto fn = decompress_kernel<SCH, OUT, LG>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(fn), C::SMEM, &done);
     if (e != cudaSuccess) return e;
     return launch_pdl(fn, dim3(grid), dim3(C::WARPS * 32), C::SMEM, stream, p);
+}
+
+// TACO kernels are compiled per block size (1, 2 or 4 lanes per block).
+template <int SCH, int OUT>
+static cudaError_t launch_d_lanes(const DecompressParams& p, int grid, cudaStream_t s)
+{
+    if constexpr (SCH != S_TACO) {
+        return launch_d<SCH, OUT>(p, grid, s);
+    } else {
+        switch (p.lanes_log2) {
+        case 0: return launch_d<SCH, OUT, 0>(p, grid, s);
+        case 1: return launch_d<SCH, OUT, 1>(p, grid, s);
+        case 2: return launch_d<SCH, OUT, 2>(p, grid, s);
+        default: return cudaErrorInvalidValue;
+        }
+    }
 }
 
 template <int SCH>
 static cudaError_t launch_d_out(int out_kind, const DecompressParams& p, int grid, cudaStream_t s)
 {
     switch (out_kind) {
-    case IN_BF16: return launch_d<SCH, IN_BF16>(p, grid, s);
-    case IN_FP16: return launch_d<SCH, IN_FP16>(p, grid, s);
-    case IN_FP32: return launch_d<SCH, IN_FP32>(p, grid, s);
+    case IN_BF16: return launch_d_lanes<SCH, IN_BF16>(p, grid, s);
+    case IN_FP16: return launch_d_lanes<SCH, IN_FP16>(p, grid, s);
+    case IN_FP32: return launch_d_lanes<SCH, IN_FP32>(p, grid, s);
     default: return cudaErrorInvalidValue;
     }
 }

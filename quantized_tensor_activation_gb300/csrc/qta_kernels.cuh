@@ -669,7 +669,8 @@ __device__ __forceinline__ void store_codes(uint8_t* ob, const CUtensorMap* map,
 
 // ------------------------------------------------------------ compress
 // taco_compress / qar_requant / CURRENT-mode amax pre-pass (AMAX_ONLY).
-template <int IN, int SCH, bool AMAX_ONLY>
+// LG: log2 of the lanes per block when fixed at compile time (TACO), else -1.
+template <int IN, int SCH, bool AMAX_ONLY, int LG = -1>
 __global__ void __launch_bounds__(CompressCfg<IN, SCH>::WARPS * 32, 1)
 compress_kernel(const __grid_constant__ CompressParams p)
 {
@@ -700,13 +701,15 @@ compress_kernel(const __grid_constant__ CompressParams p)
     }
     __syncwarp();
 
-    const QuantOut qo{p.scales, p.zeros, p.state, p.M, p.lanes_per_block, p.lanes_log2, p.seg_per_tensor,
+    const int lg = (LG >= 0) ? LG : p.lanes_log2;
+    const int L = 1 << lg;
+    const QuantOut qo{p.scales, p.zeros, p.state, p.M, L, lg, p.seg_per_tensor,
                       p.round_up, amax_tab, (SCH == S_TACO) ? cta_amax_slots(p.M, p.seg_per_tensor) : 0};
     Quantizer<SCH> quant;
     // TACO: the rows are loaded into the permuted slots of the halved
     // cross-lane exchange
     constexpr bool XL = (SCH == S_TACO);
-    const uint32_t xm = XL ? xl_mask(p.lanes_per_block, lane) : 0u;
+    const uint32_t xm = XL ? xl_mask(L, lane) : 0u;
     int stage = 0;
     uint32_t phase = 0;
     int k = 0;
@@ -737,7 +740,7 @@ compress_kernel(const __grid_constant__ CompressParams p)
         quant.template run<AMAX_ONLY, XL>(v, qo, wt * 32, lane, ow, false, xm);
         if constexpr (!AMAX_ONLY)
             store_codes<SCH, C::OUT_BUFS, XL>(outb + (k % C::OUT_BUFS) * C::OUT_BYTES, &p.out_map, wt * 32, lane,
-                                              ow, p.lanes_log2, xm);
+                                              ow, lg, xm);
     }
     quant.finish(qo, lane);
     if (lane == 0) {
@@ -784,7 +787,8 @@ struct SegMeta {
     }
 };
 
-template <int SCH, int OUT>
+// LG: log2 of the lanes per block when fixed at compile time (TACO), else -1.
+template <int SCH, int OUT, int LG = -1>
 __global__ void __launch_bounds__(DecompressCfg<SCH, OUT>::WARPS * 32, 1)
 decompress_kernel(const __grid_constant__ DecompressParams p)
 {
@@ -813,7 +817,8 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
         }
     }
     __syncwarp();
-    const int L = p.lanes_per_block;
+    const int lg = (LG >= 0) ? LG : p.lanes_log2;
+    const int L = 1 << lg;
     // TACO: the codes are read into the permuted slots of the halved
     // cross-lane exchange
     const uint32_t xm = (SCH == S_TACO) ? xl_mask(L, lane) : 0u;
@@ -824,13 +829,13 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
     // metadata of the next warp tile is fetched one tile ahead
     SegMeta<SCH> meta;
     if (first < p.n_warp_tiles && first * 32 + lane < p.M)
-        meta.load(p.scales, p.zeros, p.state, first * 32 + lane, p.lanes_log2, p.seg_per_tensor);
+        meta.load(p.scales, p.zeros, p.state, first * 32 + lane, lg, p.seg_per_tensor);
     for (int wt = first; wt < p.n_warp_tiles; wt += W, ++k) {
         SegMeta<SCH> cur = meta;
         {
             const int gn = (wt + W) * 32 + lane;
             if (wt + W < p.n_warp_tiles && gn < p.M)
-                meta.load(p.scales, p.zeros, p.state, gn, p.lanes_log2, p.seg_per_tensor);
+                meta.load(p.scales, p.zeros, p.state, gn, lg, p.seg_per_tensor);
         }
         const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[stage], phase, p.err));
         if (!ok) {
@@ -870,7 +875,7 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
         }
         __syncwarp();
         if constexpr (SCH == S_TACO)
-            store_segment_xl<OUT>(ob, lane, v, p.lanes_log2, xm);
+            store_segment_xl<OUT>(ob, lane, v, lg, xm);
         else
             store_segment<OUT>(ob, lane, v);
         fence_proxy_async_smem();
