@@ -957,7 +957,9 @@ __device__ __forceinline__ void reduce_meta_load(const ReduceParams& p, int t, i
 // exactly as qar_requant quantizes an FP32 input -- bit-identical to the two
 // calls -- except for TACO -> TACO with equal blocks, where the Hadamard-
 // domain sum is requantized directly.
-template <int SCH, int OSCH, bool AMAX_ONLY>
+// LG: log2 of the shards' lanes per block when fixed at compile time (the
+// TACO FP32 sum, which inverts the transform with the halved exchange), else -1.
+template <int SCH, int OSCH, bool AMAX_ONLY, int LG = -1>
 __global__ void __launch_bounds__(ReduceCfg<SCH, OSCH>::WARPS * 32, 1)
 reduce_kernel(const __grid_constant__ ReduceParams p)
 {
@@ -990,7 +992,10 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
         }
     }
     __syncwarp();
-    const int L = p.lanes_per_block;
+    const int L = (LG >= 0) ? (1 << LG) : p.lanes_per_block;
+    // TACO FP32 sum: codes read into the permuted slots of the halved exchange
+    constexpr bool XL = (SCH == S_TACO) && (OSCH == OUT_F32);
+    const uint32_t xm = XL ? xl_mask(L, lane) : 0u;
     constexpr int RANK_CHUNK = C::RANK_CHUNK;
     const int n_chunks = (n + RANK_CHUNK - 1) / RANK_CHUNK;
     int stage = 0;
@@ -1032,9 +1037,9 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                 const uint16_t s16 = static_cast<uint16_t>(cur[kk].raw);
                 const uint8_t* tile = wb + stage * C::STAGE_BYTES + slot * C::IN_BYTES;
                 if (r == 0)
-                    dequant_segment<SCH, 0>(tile, lane, s, z, acc, s16);
+                    dequant_segment<SCH, 0>(tile, lane, s, z, acc, s16, xm);
                 else
-                    dequant_segment<SCH, 1>(tile, lane, s, z, acc, s16);
+                    dequant_segment<SCH, 1>(tile, lane, s, z, acc, s16, xm);
                 if (slot == C::RPU - 1 || r == n - 1) {
                     __syncwarp();
                     if (lane == 0 && unit + C::STAGES < total_units) {
@@ -1056,8 +1061,13 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
         // (the inverse and forward transforms cancel and are skipped).
         const bool direct = (SCH == S_TACO) && (OSCH == S_TACO) && (p.q_lanes_per_block == L);
         if (SCH == S_TACO && !direct) {
-            fwht64_local(acc);
-            fwht_cross(acc, L, lane);
+            if constexpr (XL) {
+                fwht64_local_xl(acc, xm);
+                fwht_cross_xl(acc, L, lane);
+            } else {
+                fwht64_local(acc);
+                fwht_cross(acc, L, lane);
+            }
             if constexpr (OSCH == OUT_F32) {
                 const u64 ib = pk2(p.inv_block, p.inv_block);
 #pragma unroll
@@ -1075,7 +1085,10 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
         if constexpr (OSCH == OUT_F32) {
             if (lane == 0) bulk_wait_read<0>();
             __syncwarp();
-            store_segment<IN_FP32>(outb, lane, acc);
+            if constexpr (XL)
+                store_segment_xl<IN_FP32>(outb, lane, acc, (LG >= 0) ? LG : p.lanes_log2, xm);
+            else
+                store_segment<IN_FP32>(outb, lane, acc);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {

@@ -20,12 +20,12 @@ int reduce_smem(int scheme, int out_scheme)
 
 bool reduce_requant_supported(int scheme, int out_scheme) { return reduce_smem(scheme, out_scheme) > 0 && out_scheme != OUT_F32; }
 
-template <int SCH, int OSCH, bool AMAX>
+template <int SCH, int OSCH, bool AMAX, int LG = -1>
 static cudaError_t launch_r(const ReduceParams& p, int grid, cudaStream_t stream)
 {
     using C = ReduceCfg<SCH, OSCH>;
     static std::atomic<unsigned> done{0};
-    auto fn = reduce_kernel<SCH, OSCH, AMAX>;
+    auto fn = reduce_kernel<SCH, OSCH, AMAX, LG>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(fn), C::SMEM, &done);
     if (e != cudaSuccess) return e;
     return launch_pdl(fn, dim3(grid), dim3(C::WARPS * 32), C::SMEM, stream, p);
@@ -34,7 +34,13 @@ static cudaError_t launch_r(const ReduceParams& p, int grid, cudaStream_t stream
 cudaError_t launch_reduce(int scheme, const ReduceParams& p, int grid, cudaStream_t stream)
 {
     switch (scheme) {
-    case S_TACO: return launch_r<S_TACO, OUT_F32, false>(p, grid, stream);
+    case S_TACO:   // compiled per block size: the inverse transform's strips are constants
+        switch (p.lanes_log2) {
+        case 0: return launch_r<S_TACO, OUT_F32, false, 0>(p, grid, stream);
+        case 1: return launch_r<S_TACO, OUT_F32, false, 1>(p, grid, stream);
+        case 2: return launch_r<S_TACO, OUT_F32, false, 2>(p, grid, stream);
+        default: return cudaErrorInvalidValue;
+        }
     case S_INT8SYM: return launch_r<S_INT8SYM, OUT_F32, false>(p, grid, stream);
     case S_ASYM4: return launch_r<S_ASYM4, OUT_F32, false>(p, grid, stream);
     case S_ASYM8: return launch_r<S_ASYM8, OUT_F32, false>(p, grid, stream);
