@@ -261,7 +261,7 @@ def algorithmic_bytes(w):
     return {"K1": k1, "K2": k2, "K3": k3, "K23": k23, "K4": k4}
 
 
-def ring_report(qta, w, x, steps: int):
+def ring_report(qta, w, x, steps: int, peak: float):
     """EQuARX full-loop and semi-loop adder chains (ring reduce-scatter with
     the partial sum requantized at every hop, then the quantized all-gather)
     over the workload's ranks: time of the reduce-scatter chains (CUDA events,
@@ -306,8 +306,56 @@ def ring_report(qta, w, x, steps: int):
         per_hop.append(err / (R * C))
     out["full_loop"]["mse_after_hop"] = per_hop
     del parts
+    out["hop_kernel"] = hop_kernel_report(qta, w, x, peak)
     assert qta.qta_device_error() == 0
     return out
+
+
+def hop_kernel_report(qta, w, x, peak: float, iters: int = 10):
+    """The ring's inner call on a whole rank tensor, for its roofline: rank
+    1's codes as the incoming partial sum, rank 0's tensor as the local
+    addend.  CUDA events around each call; a 256 MB write between calls
+    flushes L2.  Algorithmic bytes: the incoming codes and metadata, the local
+    tensor, and the output (codes and metadata, or the FP32 sum)."""
+    import torch
+
+    N, R, C = x.shape
+    dev = x.device
+    dt = {torch.bfloat16: qta.BF16, torch.float16: qta.FP16, torch.float32: qta.FP32}[x.dtype]
+    d = qta.desc(w.scheme, w.block, R, C)
+    qin = qta.alloc_qtensor(d, dev)
+    qta.taco_compress(d, x[1], dt, qin, qta.SCALE_CURRENT)
+    qout = qta.alloc_qtensor(d, dev)
+    qta.qar_dequant_add_requant(d, qin, x[0], dt, qout, qta.SCALE_CURRENT)
+    if qout.state is not None:
+        qta.taco_update_scale(qout.state, 1)        # S from this tensor: DELAYED from here on
+    s = torch.empty((R, C), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    E = R * C
+    q_bytes = qta.codes_bytes(d) + qta.scales_bytes(d) + qta.zeros_bytes(d)
+    x_bytes = E * x.element_size()
+    calls = {
+        "qar_dequant_add_requant": (lambda: qta.qar_dequant_add_requant(d, qin, x[0], dt, qout, qta.SCALE_DELAYED),
+                                    2 * q_bytes + x_bytes),
+        "qar_dequant_add": (lambda: qta.qar_dequant_add(d, qin, x[0], dt, s), q_bytes + x_bytes + 4 * E),
+    }
+    rep = {"shape": [R, C], "note": "one call over a whole rank tensor; L2 flushed between calls"}
+    for name, (fn, nbytes) in calls.items():
+        fn()
+        total = 0.0
+        for _ in range(iters):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            total += a.elapsed_time(b)
+        ms = total / iters
+        rep[name] = {"ms": ms, "gb_s": nbytes / (ms * 1e-3) / 1e9, "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / peak,
+                     "algorithmic_bytes": nbytes}
+    del flush, s, qin, qout
+    return rep
 
 
 def run_qta(args, w):
@@ -665,7 +713,7 @@ def run_qta(args, w):
                      "note": "output of the timed step vs the float64 sum of the 16-bit inputs"}
             del exact, err, e0, y0
 
-    ring_rep = ring_report(qta, w, x, 3) if args.ring else None
+    ring_rep = ring_report(qta, w, x, 3, peak) if args.ring else None
     block_choice = None
     if args.choose_block:
         from quantized_tensor_activation_gb300 import calib

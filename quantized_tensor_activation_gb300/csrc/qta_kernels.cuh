@@ -172,7 +172,9 @@ template <int XIN, int OSCH>
 struct AccumCfg {
     static constexpr bool F32X = XIN == IN_FP32;
     static constexpr bool F32O = OSCH == OUT_F32;
-    static constexpr int WARPS = (F32X && F32O) ? 6 : 8;
+    // 12 warps for the TACO and INT4 requantizing hops with a 16-bit local
+    // tensor (issue-bound; 166 and 158 registers), 8 for the others
+    static constexpr int WARPS = F32X ? (F32O ? 6 : 8) : ((OSCH == S_TACO || OSCH == S_ASYM4) ? 12 : 8);
     static constexpr int STAGES = 2;
     static constexpr int IN_BYTES = 32 * 64;
     static constexpr int X_BYTES = 32 * (F32X ? 256 : 128);
@@ -1110,6 +1112,40 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
 }
 
 // ------------------------------------------------------------ ring hop
+// v[j] = v[j] * (1/B) (TACO) + x[j], one scalar rounding each, with x read
+// chunk by chunk from this lane's row of the stage.
+template <int SCH, int XIN>
+__device__ __forceinline__ void add_local_segment(const uint8_t* st, int lane, u64 (&v)[32], float inv_block)
+{
+    auto add = [&](int j, float bx, float by) {
+        float2 a = up2(v[j]);
+        if constexpr (SCH == S_TACO) {
+            a.x = __fmul_rn(a.x, inv_block);
+            a.y = __fmul_rn(a.y, inv_block);
+        }
+        v[j] = pk2(__fadd_rn(a.x, bx), __fadd_rn(a.y, by));
+    };
+    if constexpr (XIN == IN_FP32) {
+#pragma unroll
+        for (int sc = 0; sc < 16; ++sc) {
+            const uint4 w = lds128(st + (sc >> 3) * 4096, sw128(lane, sc & 7));
+            add(sc * 2, __uint_as_float(w.x), __uint_as_float(w.y));
+            add(sc * 2 + 1, __uint_as_float(w.z), __uint_as_float(w.w));
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint4 w = lds128(st, sw128(lane, c));
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 b = up2((XIN == IN_BF16) ? bf16x2_to_pair(ws[k]) : f16x2_to_pair(ws[k]));
+                add(c * 4 + k, b.x, b.y);
+            }
+        }
+    }
+}
+
 // qar_dequant_add (OSCH = OUT_F32) and qar_dequant_add_requant (OSCH = SCH;
 // AMAX_ONLY = its CURRENT-mode pre-pass): the incoming codes are dequantized
 // exactly as taco_decompress dequantizes them to FP32 (TACO: inverse
@@ -1182,10 +1218,17 @@ accum_kernel(const __grid_constant__ AccumParams p)
         }
         float s, z;
         cur.decode(s, z);
-        u64 v[32], xv[32];
+        u64 v[32];
         const uint8_t* st = wb + stage * C::STAGE_BYTES;
         dequant_segment<SCH, 0>(st, lane, s, z, v, static_cast<uint16_t>(cur.raw));
-        load_segment<XIN>(st + C::IN_BYTES, lane, xv);
+        if constexpr (SCH == S_TACO) {
+            fwht64_local(v);
+            fwht_cross(v, L, lane);
+        }
+        // times 1/B (TACO), then the local tensor with one rounding per
+        // element: scalar rounded operations, which are never contracted.
+        // The local tensor is read from the stage a 16-byte chunk at a time.
+        add_local_segment<SCH, XIN>(st + C::IN_BYTES, lane, v, p.inv_block);
         __syncwarp();
         {
             const int nwt = wt + C::STAGES * W;
@@ -1197,22 +1240,6 @@ accum_kernel(const __grid_constant__ AccumParams p)
         if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
-        }
-        if constexpr (SCH == S_TACO) {
-            fwht64_local(v);
-            fwht_cross(v, L, lane);
-        }
-        // times 1/B (TACO), then the local tensor with one rounding per
-        // element: scalar rounded operations, which are never contracted
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            float2 a = up2(v[j]);
-            const float2 b = up2(xv[j]);
-            if constexpr (SCH == S_TACO) {
-                a.x = __fmul_rn(a.x, p.inv_block);
-                a.y = __fmul_rn(a.y, p.inv_block);
-            }
-            v[j] = pk2(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y));
         }
         if constexpr (OSCH == OUT_F32) {
             if (lane == 0) bulk_wait_read<0>();
