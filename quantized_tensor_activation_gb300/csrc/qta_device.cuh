@@ -495,10 +495,10 @@ __device__ __forceinline__ void fwht64_local_xl(u64 (&v)[32], uint32_t xm)
 // positions.  With a = the kept value, o = the partner's value there and
 // s = +1 in the upper lane (else -1): lower row a+o, upper row
 // fma(o, s, -s*a) = (lower - upper), both rounded once as in fwht_cross
-// (-s*a is exact).  A sign-bit XOR in place of the multiply measured slower.  Afterwards, with 4 lanes per block, registers 0-7, 8-15,
-// 16-23, 24-31 hold rows 0, 2, 1, 3 of the block.  With 2 lanes, registers
-// 0-15 and 16-31 hold rows 0 and 1.  Register 2i+t of a group holds position
-// xm + 2i + t.
+// (-s*a is exact; a sign-bit XOR in its place measured slower).  Afterwards,
+// with 4 lanes per block, registers 0-7, 8-15, 16-23, 24-31 hold rows 0, 2,
+// 1, 3 of the block; with 2 lanes, registers 0-15 and 16-31 hold rows 0 and
+// 1.  Register 2i+t of a group holds position xm + 2i + t.
 __device__ __forceinline__ void fwht_cross_xl(u64 (&v)[32], int lanes_per_block, int lane)
 {
     if (lanes_per_block >= 2) {

@@ -1112,17 +1112,15 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
 }
 
 // ------------------------------------------------------------ ring hop
-// v[j] = v[j] * (1/B) (TACO) + x[j], one scalar rounding each, with x read
-// chunk by chunk from this lane's row of the stage.
+// v[j] = v[j] * (1/B) (TACO) + x[j], one rounding each, with x read chunk
+// by chunk from this lane's row of the stage.  The multiply is packed and
+// the add scalar: ptxas contracts a packed multiply only into a packed add.
 template <int SCH, int XIN>
 __device__ __forceinline__ void add_local_segment(const uint8_t* st, int lane, u64 (&v)[32], float inv_block)
 {
+    const u64 ib2 = pk2(inv_block, inv_block);
     auto add = [&](int j, float bx, float by) {
-        float2 a = up2(v[j]);
-        if constexpr (SCH == S_TACO) {
-            a.x = __fmul_rn(a.x, inv_block);
-            a.y = __fmul_rn(a.y, inv_block);
-        }
+        const float2 a = up2((SCH == S_TACO) ? mul2(v[j], ib2) : v[j]);
         v[j] = pk2(__fadd_rn(a.x, bx), __fadd_rn(a.y, by));
     };
     if constexpr (XIN == IN_FP32) {
