@@ -4,27 +4,56 @@
 
 namespace qta {
 
-int accum_warps(int x_kind, bool requant)
+// Warps and shared memory of the kernel that launch_accum runs (the grid is
+// sized from them).
+template <int XIN>
+static void accum_cfg_x(int scheme, bool requant, int& warps, int& smem)
 {
-    return requant ? (x_kind == IN_FP32 ? AccumCfg<IN_FP32, S_TACO>::WARPS : AccumCfg<IN_BF16, S_TACO>::WARPS)
-                   : (x_kind == IN_FP32 ? AccumCfg<IN_FP32, OUT_F32>::WARPS : AccumCfg<IN_BF16, OUT_F32>::WARPS);
+    if (!requant) {
+        warps = AccumCfg<XIN, OUT_F32>::WARPS;
+        smem = AccumCfg<XIN, OUT_F32>::SMEM;
+        return;
+    }
+    switch (scheme) {
+    case S_TACO: warps = AccumCfg<XIN, S_TACO>::WARPS; smem = AccumCfg<XIN, S_TACO>::SMEM; break;
+    case S_INT8SYM: warps = AccumCfg<XIN, S_INT8SYM>::WARPS; smem = AccumCfg<XIN, S_INT8SYM>::SMEM; break;
+    case S_ASYM4: warps = AccumCfg<XIN, S_ASYM4>::WARPS; smem = AccumCfg<XIN, S_ASYM4>::SMEM; break;
+    default: warps = AccumCfg<XIN, S_ASYM8>::WARPS; smem = AccumCfg<XIN, S_ASYM8>::SMEM; break;
+    }
 }
 
-int accum_smem(int x_kind, bool requant)
+void accum_cfg(int scheme, int x_kind, bool requant, int& warps, int& smem)
 {
-    return requant ? (x_kind == IN_FP32 ? AccumCfg<IN_FP32, S_TACO>::SMEM : AccumCfg<IN_BF16, S_TACO>::SMEM)
-                   : (x_kind == IN_FP32 ? AccumCfg<IN_FP32, OUT_F32>::SMEM : AccumCfg<IN_BF16, OUT_F32>::SMEM);
+    if (x_kind == IN_FP32)
+        accum_cfg_x<IN_FP32>(scheme, requant, warps, smem);
+    else
+        accum_cfg_x<IN_BF16>(scheme, requant, warps, smem);
+}
+
+template <int SCH, int XIN, int OSCH, bool AMAX_ONLY, int LG = -1>
+static cudaError_t launch_a1(const AccumParams& p, int grid, cudaStream_t stream)
+{
+    using C = AccumCfg<XIN, OSCH>;
+    static std::atomic<unsigned> done{0};
+    auto fn = accum_kernel<SCH, XIN, OSCH, AMAX_ONLY, LG>;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(fn), C::SMEM, &done);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(fn, dim3(grid), dim3(C::WARPS * 32), C::SMEM, stream, p);
 }
 
 template <int SCH, int XIN, int OSCH, bool AMAX_ONLY>
 static cudaError_t launch_a(const AccumParams& p, int grid, cudaStream_t stream)
 {
-    using C = AccumCfg<XIN, OSCH>;
-    static std::atomic<unsigned> done{0};
-    auto fn = accum_kernel<SCH, XIN, OSCH, AMAX_ONLY>;
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(fn), C::SMEM, &done);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(fn, dim3(grid), dim3(C::WARPS * 32), C::SMEM, stream, p);
+    if constexpr (SCH == S_TACO) {
+        switch (p.lanes_log2) {
+        case 0: return launch_a1<SCH, XIN, OSCH, AMAX_ONLY, 0>(p, grid, stream);
+        case 1: return launch_a1<SCH, XIN, OSCH, AMAX_ONLY, 1>(p, grid, stream);
+        case 2: return launch_a1<SCH, XIN, OSCH, AMAX_ONLY, 2>(p, grid, stream);
+        default: return cudaErrorInvalidValue;
+        }
+    } else {
+        return launch_a1<SCH, XIN, OSCH, AMAX_ONLY>(p, grid, stream);
+    }
 }
 
 template <int SCH, int XIN>

@@ -544,8 +544,9 @@ static qta_status accum_impl(const qta_desc* d, const qta_qtensor* in, const voi
         p.q_state = out->state;
         p.round_up = (mode & QTA_SCALE_ROUND_UP) ? 1 : 0;
     }
-    const int grid = grid_for(p.n_warp_tiles, accum_warps(x_dtype, requant), accum_smem(x_dtype, requant), sms,
-                              smem_sm, d->max_sms);
+    int a_warps = 0, a_smem = 0;
+    accum_cfg(d->scheme, x_dtype, requant, a_warps, a_smem);
+    const int grid = grid_for(p.n_warp_tiles, a_warps, a_smem, sms, smem_sm, d->max_sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (requant && d->scheme == QTA_TACO_FP8 && base_mode == QTA_SCALE_CURRENT) {
         cudaError_t e = launch_state(out->state, d->batch, STATE_RESET_AMAX, s);

@@ -1149,8 +1149,9 @@ __device__ __forceinline__ void add_local_segment(const uint8_t* st, int lane, u
 // exactly as taco_decompress dequantizes them to FP32 (TACO: inverse
 // butterfly, then 1/B), the local tensor is added with one scalar FP32
 // rounding per element, and the sum is stored, or quantized exactly as
-// qar_requant quantizes an FP32 input.
-template <int SCH, int XIN, int OSCH, bool AMAX_ONLY>
+// qar_requant quantizes an FP32 input.  LG: log2 of the lanes per block when
+// fixed at compile time (TACO), else -1.
+template <int SCH, int XIN, int OSCH, bool AMAX_ONLY, int LG = -1>
 __global__ void __launch_bounds__(AccumCfg<XIN, OSCH>::WARPS * 32, 1)
 accum_kernel(const __grid_constant__ AccumParams p)
 {
@@ -1191,8 +1192,9 @@ accum_kernel(const __grid_constant__ AccumParams p)
         }
     }
     __syncwarp();
-    const int L = p.lanes_per_block;
-    const QuantOut qo{p.q_scales, p.q_zeros, p.q_state, p.M, p.lanes_per_block, p.lanes_log2, p.seg_per_tensor,
+    const int lg = (LG >= 0) ? LG : p.lanes_log2;
+    const int L = 1 << lg;
+    const QuantOut qo{p.q_scales, p.q_zeros, p.q_state, p.M, L, lg, p.seg_per_tensor,
                       p.round_up, amax_tab, (OSCH == S_TACO) ? cta_amax_slots(p.M, p.seg_per_tensor) : 0};
     Quantizer<(OSCH == OUT_F32) ? S_TACO : OSCH> quant;
     int stage = 0;

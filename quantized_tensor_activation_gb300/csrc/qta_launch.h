@@ -13,13 +13,12 @@ int compress_smem(int in_kind, int scheme);
 int decompress_smem(int scheme, int out_kind);
 int reduce_smem(int scheme, int out_scheme);   // out_scheme: OUT_F32 or the requant scheme
 bool reduce_requant_supported(int scheme, int out_scheme);
-int accum_smem(int x_kind, bool requant);
 
 // Warps per CTA of each kernel family.
 int compress_warps(int in_kind);
 int decompress_warps(int out_kind);
 int reduce_warps();
-int accum_warps(int x_kind, bool requant);
+void accum_cfg(int scheme, int x_kind, bool requant, int& warps, int& smem);
 
 cudaError_t launch_compress(int in_kind, int scheme, bool amax_only, const CompressParams& p, int grid,
                             cudaStream_t stream);
