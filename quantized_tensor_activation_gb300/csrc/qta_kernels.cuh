@@ -1004,8 +1004,10 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
     uint32_t phase = 0;
     int unit = 0;
     bool aborted = false;
-    const QuantOut qo{p.q_scales, p.q_zeros, p.q_state, p.M_out, p.q_lanes_per_block, p.q_lanes_log2,
-                      p.q_seg_per_tensor, p.q_round_up, amax_tab,
+    // TACO -> TACO compiled for one block size: the output's lanes equal the input's
+    constexpr bool SAME_LG = (LG >= 0) && (SCH == S_TACO) && (OSCH == S_TACO);
+    const QuantOut qo{p.q_scales, p.q_zeros, p.q_state, p.M_out, SAME_LG ? L : p.q_lanes_per_block,
+                      SAME_LG ? LG : p.q_lanes_log2, p.q_seg_per_tensor, p.q_round_up, amax_tab,
                       (OSCH == S_TACO) ? cta_amax_slots(p.M_out, p.q_seg_per_tensor) : 0};
     Quantizer<(OSCH == OUT_F32) ? S_TACO : OSCH> quant;
     SegMeta<SCH> nxt[RANK_CHUNK];
@@ -1061,7 +1063,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
         // TACO -> TACO with equal blocks: the sums already are the Hadamard
         // transform of the reduced rows, so they are requantized as they are
         // (the inverse and forward transforms cancel and are skipped).
-        const bool direct = (SCH == S_TACO) && (OSCH == S_TACO) && (p.q_lanes_per_block == L);
+        const bool direct = SAME_LG || ((SCH == S_TACO) && (OSCH == S_TACO) && (p.q_lanes_per_block == L));
         if (SCH == S_TACO && !direct) {
             if constexpr (XL) {
                 fwht64_local_xl(acc, xm);

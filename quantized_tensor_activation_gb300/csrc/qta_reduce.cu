@@ -53,6 +53,12 @@ cudaError_t launch_reduce_requant(int scheme, int out_scheme, bool amax_only, co
 {
     switch (scheme * 4 + out_scheme) {
     case S_TACO * 4 + S_TACO:
+        // equal blocks of 4 lanes (B = 256, no transform): compiled for that
+        // block size, 45.1 -> 43.6 us on 4 x 8192 x 5120; the same for
+        // 2 lanes measured slower (59.6 -> 60.7 us on 8 x 8192 x 4096)
+        if (p.q_lanes_log2 == 2 && p.lanes_log2 == 2)
+            return amax_only ? launch_r<S_TACO, S_TACO, true, 2>(p, grid, stream)
+                             : launch_r<S_TACO, S_TACO, false, 2>(p, grid, stream);
         return amax_only ? launch_r<S_TACO, S_TACO, true>(p, grid, stream)
                          : launch_r<S_TACO, S_TACO, false>(p, grid, stream);
     case S_INT8SYM * 4 + S_INT8SYM: return launch_r<S_INT8SYM, S_INT8SYM, false>(p, grid, stream);
