@@ -927,7 +927,7 @@ __device__ __forceinline__ void reduce_issue(const ReduceParams& p, uint8_t* wb,
 // chunk is fetched while the current one is accumulated.
 template <int SCH, int RANK_CHUNK>
 __device__ __forceinline__ void reduce_meta_load(const ReduceParams& p, int t, int c, int first, int W, int lane,
-                                                 SegMeta<SCH> (&m)[RANK_CHUNK])
+                                                 SegMeta<SCH> (&m)[RANK_CHUNK], const float* sS)
 {
     const int o = (first + t * W) * 32 + lane;
     const int g = p.seg_begin + o;
@@ -938,7 +938,7 @@ __device__ __forceinline__ void reduce_meta_load(const ReduceParams& p, int t, i
         if (valid && r < p.n_ranks) {
             if constexpr (SCH == S_TACO) {
                 m[k].raw = __ldg(static_cast<const uint8_t*>(p.scales[r]) + (g >> p.lanes_log2));
-                m[k].S = __ldg(p.state[r]);
+                m[k].S = sS[r];
             } else if constexpr (SCH == S_INT8SYM) {
                 m[k].raw = __float_as_uint(__ldg(static_cast<const float*>(p.scales[r]) + g));
             } else {
@@ -987,6 +987,12 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
     if constexpr (OSCH == S_TACO) cta_amax_init(amax_tab);
     pdl_wait();
     pdl_trigger();
+    // per-tensor scales of the shards, read once per CTA
+    __shared__ float sS[MAX_RANKS];
+    if constexpr (SCH == S_TACO) {
+        if (threadIdx.x < p.n_ranks) sS[threadIdx.x] = __ldg(p.state[threadIdx.x]);
+        __syncthreads();
+    }
     if (lane == 0) {
         for (int u = 0; u < C::STAGES && u < total_units; ++u) {
             reduce_issue<SCH, OSCH>(p, wb, bars, u, next_unit, first, W);
@@ -1011,7 +1017,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                       (OSCH == S_TACO) ? cta_amax_slots(p.M_out, p.q_seg_per_tensor) : 0};
     Quantizer<(OSCH == OUT_F32) ? S_TACO : OSCH> quant;
     SegMeta<SCH> nxt[RANK_CHUNK];
-    if (my_tiles > 0) reduce_meta_load<SCH, RANK_CHUNK>(p, 0, 0, first, W, lane, nxt);
+    if (my_tiles > 0) reduce_meta_load<SCH, RANK_CHUNK>(p, 0, 0, first, W, lane, nxt, sS);
     for (int t = 0; t < my_tiles && !aborted; ++t) {
         const int wt = first + t * W;
         if constexpr (OSCH != OUT_F32) quant.begin(qo, wt * 32, lane);
@@ -1021,9 +1027,9 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
 #pragma unroll
             for (int kk = 0; kk < RANK_CHUNK; ++kk) cur[kk] = nxt[kk];
             if (c + 1 < n_chunks)
-                reduce_meta_load<SCH, RANK_CHUNK>(p, t, c + 1, first, W, lane, nxt);
+                reduce_meta_load<SCH, RANK_CHUNK>(p, t, c + 1, first, W, lane, nxt, sS);
             else if (t + 1 < my_tiles)
-                reduce_meta_load<SCH, RANK_CHUNK>(p, t + 1, 0, first, W, lane, nxt);
+                reduce_meta_load<SCH, RANK_CHUNK>(p, t + 1, 0, first, W, lane, nxt, sS);
 #pragma unroll
             for (int kk = 0; kk < RANK_CHUNK; ++kk) {
                 const int r = c * RANK_CHUNK + kk;
