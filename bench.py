@@ -14,7 +14,8 @@ as a CUDA graph (--no-graph: eager launches).  Per-kernel times come from a
 graph of the same steps with a timing event between every two kernels,
 replayed after the timed region (eager launches if that is unavailable).
 The compress's SM cap is chosen per run from whole steps unless --k1-sms
-fixes it.  Optional reports: --ring (EQuARX adder chains), --sm-sweep,
+fixes it.  Optional reports: --ring (EQuARX adder chains and the hop kernels),
+--hop (the hop kernels alone), --sm-sweep,
 --choose-block.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl qta|reference]
@@ -714,6 +715,7 @@ def run_qta(args, w):
             del exact, err, e0, y0
 
     ring_rep = ring_report(qta, w, x, 3, peak) if args.ring else None
+    hop_rep = hop_kernel_report(qta, w, x, peak) if (args.hop and not args.ring) else None
     block_choice = None
     if args.choose_block:
         from quantized_tensor_activation_gb300 import calib
@@ -766,6 +768,7 @@ def run_qta(args, w):
                        "kernels": kernel_table(evs2, not fused)},
         "recon": recon,
         "ring": ring_rep,
+        "hop_kernel": hop_rep,
         "sm_sweep": sm_sweep,
         "block_choice": block_choice,
         "cpu_baseline": cpu,
@@ -799,6 +802,8 @@ def main(argv=None):
                     help="comma-separated SM counts: time the step with every call capped to that many SMs")
     ap.add_argument("--choose-block", action="store_true",
                     help="add the reconstruction error of rank 0's tensor for TACO blocks 64/128/256")
+    ap.add_argument("--hop", action="store_true",
+                    help="time the ring's hop kernels alone on a whole rank tensor (roofline; no adder chains)")
     ap.add_argument("--ring", action="store_true",
                     help="add the ring adder-chain report (full loop / semi loop) of the workload")
     ap.add_argument("--no-graph", action="store_true", help="launch the timed steps eagerly instead of as a CUDA graph")
