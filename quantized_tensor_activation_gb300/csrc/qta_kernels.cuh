@@ -144,18 +144,19 @@ constexpr int OUT_F32 = -1;
 
 template <int SCH, int OSCH = OUT_F32>
 struct ReduceCfg {
-    // the INT4 kernels fit 128 registers and gain from 16 warps (issue-bound
-    // decode); the others need more registers and run 12
-    static constexpr bool W16 = (SCH == S_ASYM4);
+    // the INT4 kernels and the fused TACO -> TACO reduce fit 128 registers
+    // and run 16 warps (the INT4 decode is issue-bound; the TACO one fits
+    // with 2-rank metadata chunks and 6 stages); the others run 12
+    static constexpr bool W16 = (SCH == S_ASYM4) || (SCH == S_TACO && OSCH == S_TACO);
     static constexpr int WARPS = W16 ? 16 : 12;
     static constexpr int IN_SEG = (SCH == S_ASYM4) ? 32 : 64;
     static constexpr int OUT_SEG = (OSCH == OUT_F32) ? 256 : (OSCH == S_ASYM4) ? 32 : 64;
     // ranks whose warp tiles share one stage (one load barrier, one wait):
     // the 1 KB INT4 tiles of the fused kernel are loaded two ranks at a time
     static constexpr int RPU = (SCH == S_ASYM4 && OSCH != OUT_F32) ? 2 : 1;
-    static constexpr int STAGES = (OSCH == OUT_F32) ? 4 : ((SCH == S_ASYM4) ? 12 / RPU : 8);
+    static constexpr int STAGES = (OSCH == OUT_F32) ? 4 : ((SCH == S_ASYM4) ? 12 / RPU : (W16 ? 6 : 8));
     // ranks whose scale metadata is fetched together, one chunk ahead
-    static constexpr int RANK_CHUNK = W16 ? 8 : 4;
+    static constexpr int RANK_CHUNK = (SCH == S_ASYM4) ? 8 : (W16 ? 2 : 4);
     static_assert(RANK_CHUNK % RPU == 0, "a stage never spans two metadata chunks");
     static constexpr int IN_BYTES = 32 * IN_SEG;
     static constexpr int STAGE_BYTES = RPU * IN_BYTES;
@@ -938,7 +939,7 @@ __device__ __forceinline__ void reduce_meta_load(const ReduceParams& p, int t, i
         if (valid && r < p.n_ranks) {
             if constexpr (SCH == S_TACO) {
                 m[k].raw = __ldg(static_cast<const uint8_t*>(p.scales[r]) + (g >> p.lanes_log2));
-                m[k].S = sS[r];
+                (void)sS;   // the shard's per-tensor scale is read at decode time
             } else if constexpr (SCH == S_INT8SYM) {
                 m[k].raw = __float_as_uint(__ldg(static_cast<const float*>(p.scales[r]) + g));
             } else {
@@ -1043,7 +1044,12 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                     }
                 }
                 float s, z;
-                cur[kk].decode(s, z);
+                if constexpr (SCH == S_TACO) {
+                    s = __fmul_rn(sS[r], e4m3_decode(cur[kk].raw));
+                    z = 0.0f;
+                } else {
+                    cur[kk].decode(s, z);
+                }
                 const uint16_t s16 = static_cast<uint16_t>(cur[kk].raw);
                 const uint8_t* tile = wb + stage * C::STAGE_BYTES + slot * C::IN_BYTES;
                 if (r == 0)
