@@ -334,6 +334,7 @@ def test_copy_kernel(dev):
 
 
 @pytest.mark.parametrize("scheme,B,gscheme,gB", [(qta.TACO_FP8, 128, qta.TACO_FP8, 128),
+                                                 (qta.TACO_FP8, 256, qta.TACO_FP8, 256),
                                                  (qta.TACO_FP8, 256, qta.TACO_FP8, 128),
                                                  (qta.TACO_FP8, 64, qta.TACO_FP8, 256),
                                                  (qta.INT8_SYM_B64, 64, qta.INT8_SYM_B64, 64),
