@@ -925,10 +925,12 @@ __device__ __forceinline__ void reduce_issue(const ReduceParams& p, uint8_t* wb,
 }
 
 // Ranks are processed in chunks of RANK_CHUNK; the scale metadata of the next
-// chunk is fetched while the current one is accumulated.
+// chunk is fetched while the current one is accumulated (TACO: the block
+// scale bytes; the shards' per-tensor scales are read from the CTA's shared
+// copy when a rank is decoded).
 template <int SCH, int RANK_CHUNK>
 __device__ __forceinline__ void reduce_meta_load(const ReduceParams& p, int t, int c, int first, int W, int lane,
-                                                 SegMeta<SCH> (&m)[RANK_CHUNK], const float* sS)
+                                                 SegMeta<SCH> (&m)[RANK_CHUNK])
 {
     const int o = (first + t * W) * 32 + lane;
     const int g = p.seg_begin + o;
@@ -939,7 +941,6 @@ __device__ __forceinline__ void reduce_meta_load(const ReduceParams& p, int t, i
         if (valid && r < p.n_ranks) {
             if constexpr (SCH == S_TACO) {
                 m[k].raw = __ldg(static_cast<const uint8_t*>(p.scales[r]) + (g >> p.lanes_log2));
-                (void)sS;   // the shard's per-tensor scale is read at decode time
             } else if constexpr (SCH == S_INT8SYM) {
                 m[k].raw = __float_as_uint(__ldg(static_cast<const float*>(p.scales[r]) + g));
             } else {
@@ -1018,7 +1019,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                       (OSCH == S_TACO) ? cta_amax_slots(p.M_out, p.q_seg_per_tensor) : 0};
     Quantizer<(OSCH == OUT_F32) ? S_TACO : OSCH> quant;
     SegMeta<SCH> nxt[RANK_CHUNK];
-    if (my_tiles > 0) reduce_meta_load<SCH, RANK_CHUNK>(p, 0, 0, first, W, lane, nxt, sS);
+    if (my_tiles > 0) reduce_meta_load<SCH, RANK_CHUNK>(p, 0, 0, first, W, lane, nxt);
     for (int t = 0; t < my_tiles && !aborted; ++t) {
         const int wt = first + t * W;
         if constexpr (OSCH != OUT_F32) quant.begin(qo, wt * 32, lane);
@@ -1028,9 +1029,9 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
 #pragma unroll
             for (int kk = 0; kk < RANK_CHUNK; ++kk) cur[kk] = nxt[kk];
             if (c + 1 < n_chunks)
-                reduce_meta_load<SCH, RANK_CHUNK>(p, t, c + 1, first, W, lane, nxt, sS);
+                reduce_meta_load<SCH, RANK_CHUNK>(p, t, c + 1, first, W, lane, nxt);
             else if (t + 1 < my_tiles)
-                reduce_meta_load<SCH, RANK_CHUNK>(p, t + 1, 0, first, W, lane, nxt, sS);
+                reduce_meta_load<SCH, RANK_CHUNK>(p, t + 1, 0, first, W, lane, nxt);
 #pragma unroll
             for (int kk = 0; kk < RANK_CHUNK; ++kk) {
                 const int r = c * RANK_CHUNK + kk;
