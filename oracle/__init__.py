@@ -52,10 +52,13 @@ def build(force: bool = False) -> str:
 
 
 def lib():
+    """The loaded oracle library.  QTA_ORACLE_LIB names another build of it
+    to load instead (the mutation tests load deliberately miswritten copies
+    to show that the pins fail on them)."""
     global _lib
     with _lock:
         if _lib is None:
-            L = ctypes.CDLL(build())
+            L = ctypes.CDLL(os.environ.get("QTA_ORACLE_LIB") or build())
             i64, i32, vp, fp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p
             L.orc_e4m3_encode.argtypes = [ctypes.c_float]
             L.orc_e4m3_encode.restype = ctypes.c_uint8
