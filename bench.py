@@ -9,17 +9,25 @@ One step = one pass of the whole path over one batch of synthetic input:
       taco_update_scale   both stages' per-tensor scales (one launch)
 Metric: GB/s of 16-bit input processed (2 bytes x elements x ranks / step
 time); "roofline" gives the fraction of the measured HBM bandwidth the
-dominant kernel (K1) reaches.  The timed steps replay the step captured once
-as a CUDA graph (--no-graph: eager launches).  Per-kernel times come from a
+dominant kernel (K1) reaches.  The timed steps replay the step captured as
+a CUDA graph (--no-graph: eager launches).  Per-kernel times come from a
 graph of the same steps with a timing event between every two kernels,
 replayed after the timed region (eager launches if that is unavailable).
-The compress's SM cap is chosen per run from whole steps unless --k1-sms
-fixes it.  Optional reports: --ring (EQuARX adder chains and the hop kernels),
---hop (the hop kernels alone), --sm-sweep,
---choose-block.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl qta|reference]
+The default run measures every target workload: the headline (--workload,
+default the largest: 8 x [16384 x 8192] bf16, block-symmetric INT8) with
+the end-to-end, CPU-baseline and roofline reports, then each other target
+workload as its own report under "per_config" (the Qwen-style gradient
+workload as 16 drifting per-step inputs resident in HBM and cycled), and
+the K0 copy kernel on 1 GiB beside the measured copy peak.  The compress's
+SM cap is chosen per workload from whole steps unless --k1-sms fixes it.
+Optional reports: --ring (EQuARX adder chains and the hop kernels), --hop
+(the hop kernels alone), --sm-sweep, --choose-block.
 
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--per-config auto|none|a,b] [--impl qta|reference]
+
+--gpus N without torchrun starts N local replica processes (one per GPU).
 --impl reference times the CPU oracle (the plain single-threaded reference
 implementation of the same path) on a bounded row sample of the workload.
 """
@@ -46,11 +54,10 @@ METRIC = "fused compress + dequant-reduce GB/s of bf16 input; % of GB300 HBM pea
 FALLBACK_HBM_GBS = 6800.0
 
 # Per-launch DRAM traffic (bytes read + written) of the dominant kernel from
-# one ncu capture, keyed by (kernel, workload) together with the digest of
-# the CUDA sources it was measured on; a changed source makes it stale (null).
+# one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), keyed by
+# (kernel, workload) together with the digest of the CUDA sources it was
+# measured on; a changed source makes it stale (null).
 NCU_TRAFFIC = {
-    # ncu dram__bytes_read.sum + dram__bytes_write.sum of one compress_kernel<bf16, TACO>
-    # launch on gpt_tp (profiles/gpt_tp_step.md), valid for the CUDA sources it was taken on
     ("taco_compress", "gpt_tp"): {"bytes": 536908032 + 236312320, "src": "7f3dcfb9a19b9fd0"},
 }
 
@@ -359,24 +366,40 @@ def hop_kernel_report(qta, w, x, peak: float, iters: int = 10):
     return rep
 
 
-def run_qta(args, w):
+def _cpu_rows(w, target_elems: int) -> int:
+    """Rows per rank of a bounded oracle sample of about target_elems
+    elements over all ranks (a multiple of the rank count, at least one row
+    per gather shard)."""
+    rows = max(w.ranks, int(target_elems // (w.ranks * w.cols)))
+    rows = min(w.rows, rows - rows % w.ranks)
+    return max(rows, w.ranks)
+
+
+def cpu_baseline(w, rows: int, seed: int):
+    dt_s, nbytes, threads = _cpu_oracle_path(w, rows, seed=seed)
+    return {"value": nbytes / dt_s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{rows} of {w.rows} rows of each of the {w.ranks} ranks "
+                      f"({w.ranks * rows * w.cols} elements), full path, {dt_s:.1f} s",
+            "stages": dict(_cpu_oracle_path.stages), "host": _host_cpu()}
+
+
+def measure_workload(qta, w, args, dev, ws: int, local: int, headline: bool) -> dict:
+    """Time the whole hot path on one workload: K1 taco_compress (all ranks),
+    K23 qar_reduce_requant (or K2 + K3), K4 taco_decompress and the state
+    update, as one captured CUDA graph per step.  A workload with a per-step
+    magnitude drift keeps one input per step resident in HBM and cycles
+    through them, so every timed step compresses a new tensor with the
+    per-tensor scales the previous step left.  Returns the per-workload
+    report (times are the max over ranks)."""
     import torch
 
-    import quantized_tensor_activation_gb300 as qta
-
-    ws, rank = _dist()
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    qta.build()
     sch = qta.SCHEMES
     N, R, C = w.ranks, w.rows, w.cols
     in_dt = qta.BF16 if w.dtype == "bf16" else qta.FP16
     tdt = w.torch_dtype
-    x = workloads.make_rank_inputs(w, device=dev, seed=args.seed)            # [N, R, C] resident in HBM
+    n_in = max(1, w.steps)
+    # inputs resident in HBM: [N, R, C] per step
+    xs = [workloads.make_rank_inputs(w, device=dev, seed=args.seed, step=k) for k in range(n_in)]
     d_in = qta.desc(sch[w.scheme], w.block, R, C, batch=N, max_sms=max(args.k1_sms, 0))
     d_sh = qta.desc(sch[w.scheme], w.block, R, C)
     d_g = qta.desc(sch[w.gather_scheme], w.gather_block, R // N, C, batch=N)
@@ -399,15 +422,19 @@ def run_qta(args, w):
     ssum = torch.empty((R, C), dtype=torch.float32, device=dev)
     y = torch.empty((R, C), dtype=tdt, device=dev)
     stream = torch.cuda.current_stream()
-
     launches = [0]
+    counter = [0]            # steps issued so far: step i compresses input i mod n_in
 
-    def step(first=False, ev=None, fused=True):
+    def step(first=False, ev=None, fused=True, i=None):
         # each compress uses the per-tensor scale left by the previous step and
         # accumulates this step's amax; the receiving side dequantizes with the
-        # same scale, so the states are updated once, at the end of the step
-        # events go on the current stream, which is the capture stream while
-        # a CUDA graph of the step is being recorded
+        # same scale, so the states are updated once, at the end of the step.
+        # Events go on the current stream (the capture stream while a CUDA
+        # graph of the step is recorded).
+        if i is None:
+            i = counter[0]
+            counter[0] += 1
+        x = xs[i % n_in]
         mode = qta.SCALE_CURRENT if first else qta.SCALE_DELAYED
         if ev:
             ev[0].record()
@@ -466,8 +493,8 @@ def run_qta(args, w):
         d_in.max_sms = min(k1_tune, key=lambda c: (k1_tune[c], c != 0))
     k1_cap = d_in.max_sms
 
-    # calibrate a load window of about 0.6 s on each side of the timed region,
-    # so that nvidia-smi samples the clocks under the same continuous load
+    # a load window of about 0.6 s on each side of the timed region, so that
+    # nvidia-smi samples the clocks under the same continuous load
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
     for _ in range(3):
@@ -487,42 +514,49 @@ def run_qta(args, w):
         t1.record(stream)
         return evs, t0, t1, launches[0]
 
-    # the step as a CUDA graph (kernel parameters, tensor maps included, are
-    # fixed at capture; every replay recomputes the whole step)
-    graph = None
+    # the step as CUDA graphs, one per resident input (kernel parameters,
+    # tensor maps included, are fixed at capture; every replay recomputes
+    # the whole step)
+    graphs = None
     if not args.no_graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            step(fused=fused)
-        graph.replay()
+        graphs = []
+        for k in range(n_in):
+            gr_ = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr_):
+                step(fused=fused, i=k)
+            graphs.append(gr_)
+        for gr_ in graphs:
+            gr_.replay()
         torch.cuda.synchronize()
+    replays = [0]
 
     def run_step():
-        if graph is not None:
-            graph.replay()
+        if graphs is not None:
+            graphs[replays[0] % n_in].replay()
+            replays[0] += 1
         else:
             step(fused=fused)
 
     # the timed steps as one CUDA graph with a timing event between every two
-    # kernels (event record nodes): the per-kernel times then come from the
-    # timed region itself, free of host launch gaps
+    # kernels (event record nodes): the per-kernel times then come from steps
+    # like the timed ones, free of host launch gaps
+    graph_event_error = [None]
+
     def graph_with_events(fused_path):
         try:
             evl = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)]
                    for _ in range(args.steps)]
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr):
+            gr_ = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr_):
                 for i in range(args.steps):
-                    step(ev=evl[i], fused=fused_path)
-            gr.replay()
+                    step(ev=evl[i], fused=fused_path, i=i)
+            gr_.replay()
             torch.cuda.synchronize()
             evl[0][0].elapsed_time(evl[0][1])
-            return gr, evl
+            return gr_, evl
         except (TypeError, RuntimeError) as e:
             graph_event_error[0] = f"{type(e).__name__}: {str(e).splitlines()[0][:160]}"
             return None, None
-
-    graph_event_error = [None]
 
     tgraph, tevs = (None, None) if args.no_graph else graph_with_events(fused)
 
@@ -553,10 +587,9 @@ def run_qta(args, w):
         torch.distributed.barrier()
     clk = clocks.stop()
     if clk is not None:
-        clk["window"] = f"sampled every 100 ms over {2 * pad + args.steps} back-to-back steps around and including the timed ones"
+        clk["window"] = (f"sampled every 100 ms over {2 * pad + args.steps} back-to-back steps around and "
+                         f"including the timed ones")
     ms_step = max_over_ranks(t_start.elapsed_time(t_end) / args.steps, dev)
-    # the same steps as one graph with the timing events (the event nodes
-    # cost a few microseconds each, so the headline above runs without them)
     events_ms = None
     if tgraph is not None:
         p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -566,8 +599,7 @@ def run_qta(args, w):
         torch.cuda.synchronize()
         events_ms = p0.elapsed_time(p1) / args.steps
 
-    # per-kernel times: from the timed graph's events, else from the step
-    # launched eagerly with events between the calls
+    # per-kernel times: from the event graph, else from eager steps with events
     evs, e0, e1, _ = timed(fused)
     torch.cuda.synchronize()
     eager_ms = e0.elapsed_time(e1) / args.steps
@@ -589,7 +621,7 @@ def run_qta(args, w):
 
     # the same step with every call capped to a number of SMs (eager launches)
     sweep_raw = []
-    if args.sm_sweep:
+    if headline and args.sm_sweep:
         for n_sms in [int(v) for v in args.sm_sweep.split(",")]:
             for dd in (d_in, d_sh, d_g):
                 dd.max_sms = n_sms
@@ -600,14 +632,14 @@ def run_qta(args, w):
         d_in.max_sms, d_sh.max_sms, d_g.max_sms = k1_cap, 0, 0
         assert qta.qta_device_error() == 0
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers (headline)
     e2e = None
-    if not args.no_e2e:
-        xh = x.cpu().pin_memory()
+    if headline and not args.no_e2e:
+        xh = [x.cpu().pin_memory() for x in xs]
         yh = [torch.empty((R, C), dtype=tdt).pin_memory() for _ in range(2)]
         # double-buffered: the upload of step i+1 runs on its own copy stream
         # while step i computes and downloads its result
-        xd = [torch.empty_like(x) for _ in range(2)]
+        xd = [torch.empty_like(xs[0]) for _ in range(2)]
         yd = [y, torch.empty_like(y)]
         h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
         x_free = [torch.cuda.Event() for _ in range(2)]    # the step that last read xd[b] has compressed it
@@ -620,7 +652,7 @@ def run_qta(args, w):
             bi = i % 2
             h2d.wait_event(x_free[bi])
             with torch.cuda.stream(h2d):
-                xd[bi].copy_(xh, non_blocking=True)
+                xd[bi].copy_(xh[i % n_in], non_blocking=True)
             arrived = torch.cuda.Event()
             arrived.record(h2d)
             stream.wait_event(arrived)
@@ -655,17 +687,13 @@ def run_qta(args, w):
             stream.wait_event(ev)
         b.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = a.elapsed_time(b) / k
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / k, dev)
         e2e = {"value": 2 * N * R * C / (e2e_ms * 1e-3) / 1e9 * ws, "unit": "GB/s",
-               "h2d_bytes_per_step": x.numel() * x.element_size(),
+               "h2d_bytes_per_step": xs[0].numel() * xs[0].element_size(),
                "d2h_bytes_per_step": y.numel() * y.element_size(), "ms_per_step": e2e_ms,
                "pipeline": "inputs and outputs double-buffered: the upload of step i+1 overlaps step i's "
                            "kernels and download; each step copies its own inputs in and its result out"}
-
-    if rank != 0:
-        if ws > 1:
-            torch.distributed.destroy_process_group()
-        return
+        del xh, yh, xd, yd
 
     in_bytes = 2 * N * R * C
     value = job_throughput(in_bytes, ms_step, ws)
@@ -692,28 +720,123 @@ def run_qta(args, w):
 
     kern = kernel_table(evs, fused)
     step_bytes = alg["K1"] + alg["K4"] + (alg["K23"] if fused else alg["K2"] + alg["K3"])
-    achieved = alg["K1"] / (kern["K1"]["ms"] * 1e-3) / 1e9
-    tr = NCU_TRAFFIC.get(("taco_compress", w.name))
-    traffic = tr["bytes"] if tr and tr.get("src") == _src_digest() else None
 
-    # reconstruction error of the step's output against the exact sum of the
+    # reconstruction error of one step's output against the exact sum of the
     # ranks' inputs (float64), and of one rank's compress -> decompress
     recon = None
     if not args.no_recon:
+        step(fused=fused, i=0)
         with torch.no_grad():
-            exact = x.double().sum(dim=0)
+            x0 = xs[0]
+            exact = x0.double().sum(dim=0)
             err = y.double() - exact
             mse = float((err * err).mean())
             d0 = qta.desc(sch[w.scheme], w.block, R, C)
             y0 = torch.empty((R, C), dtype=torch.float32, device=dev)
             qta.taco_decompress(d0, shards[0], y0, qta.FP32)
-            e0 = y0.double() - x[0].double()
+            e0 = y0.double() - x0[0].double()
             recon = {"allreduce_mse": mse, "allreduce_nmse": mse / float((exact * exact).mean()),
                      "stage1_mse_rank0": float((e0 * e0).mean()),
-                     "stage1_nmse_rank0": float((e0 * e0).mean()) / float((x[0].double() ** 2).mean()),
-                     "note": "output of the timed step vs the float64 sum of the 16-bit inputs"}
+                     "stage1_nmse_rank0": float((e0 * e0).mean()) / float((x0[0].double() ** 2).mean()),
+                     "note": "output of one step (input 0, DELAYED scales) vs the float64 sum of the 16-bit "
+                             "inputs"}
             del exact, err, e0, y0
+        torch.cuda.synchronize()
+        assert qta.qta_device_error() == 0
 
+    rep = {
+        "config": _config(w),
+        "ms_per_step": ms_step,
+        "value": value,
+        "unit": "GB/s",
+        "step_frac_of_hbm": step_bytes / (ms_step * 1e-3) / 1e9 / peak,
+        "kernels": kern,
+        "k1_sms": {"k1_max_sms": k1_cap or "all",
+                   "k1_sms_choice": ("fixed" if k1_tune is None else
+                                     "fastest eager step of " + ", ".join(
+                                         f"{c or 'all'}: {t * 1e3:.1f} us" for c, t in k1_tune.items()))},
+        "path": "fused reduce+requant (qar_reduce_requant)" if fused else "qar_reduce + qar_requant",
+        "launch": (f"CUDA graph of one step, replayed ({n_in} graphs, one per resident input)" if n_in > 1
+                   else "CUDA graph of one step, replayed") if graphs is not None else "eager",
+        "kernel_times": ("events between the kernels inside a CUDA graph of the same steps, replayed after "
+                         "the timed region" if tevs is not None else
+                         "eager step with events" + (f" (graph events unavailable: {graph_event_error[0]})"
+                                                     if graph_event_error[0] else "")),
+        "ms_per_step_graph_with_events": events_ms,
+        "eager_ms_per_step": eager_ms,
+        "other_path": {"path": "qar_reduce + qar_requant" if fused else "qar_reduce_requant",
+                       "ms_per_step": other_ms, "value": in_bytes / (other_ms * 1e-3) / 1e9 * ws,
+                       "kernels": kernel_table(evs2, not fused)},
+        "recon": recon,
+        "clocks": clk,
+        "gpu_launches": n_launch,
+        "inputs": (f"{n_in} per-step inputs resident in HBM ({n_in * in_bytes / 1e9:.2f} GB), cycled: step i "
+                   f"compresses input i mod {n_in}, each drawn with its own magnitude factor" if n_in > 1
+                   else f"one input resident in HBM ({in_bytes / 1e9:.2f} GB of 16-bit values)"),
+        "_alg": alg, "_peak": (peak, peak_kind), "_e2e": e2e, "_sweep": sweep_raw,
+        "_kernel_table": kernel_table, "_fused": fused,
+    }
+    if headline:
+        rep["_keep"] = (xs, shards, q)
+    else:
+        del xs, q, g, shards, ssum, y, states
+    del graphs, tgraph
+    return rep
+
+
+def copy_probe(qta, dev, nbytes: int = 1 << 30, iters: int = 10) -> dict:
+    """K0: the plain copy kernel (qta_copy) over nbytes (larger than L2),
+    mean of iters calls timed with CUDA events after warm-up."""
+    import torch
+    src = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    src.random_(0, 255)
+    dst = torch.empty_like(src)
+    for _ in range(3):
+        qta.qta_copy(src, dst, nbytes)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(iters):
+        qta.qta_copy(src, dst, nbytes)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / iters
+    ok = bool(torch.equal(src, dst))
+    del src, dst
+    peak, kind = _peaks()
+    gbs = 2 * nbytes / (ms * 1e-3) / 1e9
+    return {"kernel": "K0 qta_copy", "bytes_copied": nbytes, "ms": ms, "gb_s": gbs,
+            "frac_of_peak": gbs / peak, "peak": peak, "peak_source": f"{kind} hbm_gbs (a torch copy, driver-measured)",
+            "copy_correct": ok, "note": "read + write bytes per call / mean CUDA-event time of 10 calls"}
+
+
+def run_qta(args, w):
+    import torch
+
+    import quantized_tensor_activation_gb300 as qta
+
+    ws, rank = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    qta.build()
+
+    head = measure_workload(qta, w, args, dev, ws, local, headline=True)
+    xs, shards, q = head.pop("_keep")
+    alg, (peak, peak_kind) = head.pop("_alg"), head.pop("_peak")
+    e2e, sweep_raw = head.pop("_e2e"), head.pop("_sweep")
+    kernel_table, fused = head.pop("_kernel_table"), head.pop("_fused")
+    kern = head["kernels"]
+    achieved = alg["K1"] / (kern["K1"]["ms"] * 1e-3) / 1e9
+    tr = NCU_TRAFFIC.get(("taco_compress", w.name))
+    traffic = tr["bytes"] if tr and tr.get("src") == _src_digest() else None
+
+    N, R, C = w.ranks, w.rows, w.cols
+    in_bytes = 2 * N * R * C
+    x = xs[0]
     ring_rep = ring_report(qta, w, x, 3, peak) if args.ring else None
     hop_rep = hop_kernel_report(qta, w, x, peak) if (args.hop and not args.ring) else None
     block_choice = None
@@ -731,68 +854,113 @@ def run_qta(args, w):
                              "value": in_bytes / (ms * 1e-3) / 1e9 * ws,
                              "kernels_ms": {k: v["ms"] for k, v in t.items()},
                              "kernels_frac_of_hbm": {k: v["frac_of_hbm"] for k, v in t.items() if "frac_of_hbm" in v}})
+    del xs, shards, q, x
+    torch.cuda.empty_cache()
+
+    # the other target workloads, each measured the same way
+    per_config = {}
+    for name in args.per_config:
+        wc = workloads.WORKLOADS[name]
+        rep = measure_workload(qta, wc, args, dev, ws, local, headline=False)
+        for k in ("_alg", "_peak", "_e2e", "_sweep", "_kernel_table", "_fused"):
+            rep.pop(k)
+        per_config[name] = rep
+        torch.cuda.empty_cache()
+
+    k0 = None if args.no_k0 else copy_probe(qta, dev)
 
     cpu = None
-    if not args.no_cpu_baseline and ws == 1:
-        rows = args.cpu_rows or w.rows
-        dt_s, nbytes, threads = _cpu_oracle_path(w, rows, seed=args.seed)
-        cpu = {"value": nbytes / dt_s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"{rows} of {w.rows} rows of each of the {w.ranks} ranks "
-                         f"({w.ranks * rows * w.cols} elements), full path, {dt_s:.1f} s",
-               "stages": dict(_cpu_oracle_path.stages), "host": _host_cpu()}
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_rows or _cpu_rows(w, 4e8), args.seed)
+        for name, rep in per_config.items():
+            wc = workloads.WORKLOADS[name]
+            rep["cpu_baseline"] = cpu_baseline(wc, _cpu_rows(wc, 6e7), args.seed)
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
 
     line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": _config(w),
-        "k1_sms": {"k1_max_sms": k1_cap or "all",
-                   "k1_sms_choice": ("fixed" if k1_tune is None else
-                                     "fastest eager step of " + ", ".join(
-                                         f"{c or 'all'}: {t * 1e3:.1f} us" for c, t in k1_tune.items()))},
+        "metric": METRIC, "value": head["value"], "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": head["config"],
+        "k1_sms": head["k1_sms"],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "kernel": "K1 taco_compress",
                      "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes": alg["K1"]},
-        "path": "fused reduce+requant (qar_reduce_requant)" if fused else "qar_reduce + qar_requant",
-        "launch": "CUDA graph of one step, replayed" if graph is not None else "eager",
-        "kernel_times": ("events between the kernels inside a CUDA graph of the same steps, replayed after "
-                         "the timed region" if tevs is not None else
-                         "eager step with events" + (f" (graph events unavailable: {graph_event_error[0]})"
-                                                     if graph_event_error[0] else "")),
-        "ms_per_step_graph_with_events": events_ms,
-        "eager_ms_per_step": eager_ms,
+        "path": head["path"],
+        "launch": head["launch"],
+        "kernel_times": head["kernel_times"],
+        "ms_per_step_graph_with_events": head["ms_per_step_graph_with_events"],
+        "eager_ms_per_step": head["eager_ms_per_step"],
         "kernels": kern,
-        "step_frac_of_hbm": step_bytes / (ms_step * 1e-3) / 1e9 / peak,
-        "other_path": {"path": "qar_reduce + qar_requant" if fused else "qar_reduce_requant",
-                       "ms_per_step": other_ms, "value": in_bytes / (other_ms * 1e-3) / 1e9 * ws,
-                       "kernels": kernel_table(evs2, not fused)},
-        "recon": recon,
+        "step_frac_of_hbm": head["step_frac_of_hbm"],
+        "other_path": head["other_path"],
+        "recon": head["recon"],
+        "inputs": head["inputs"],
         "ring": ring_rep,
         "hop_kernel": hop_rep,
         "sm_sweep": sm_sweep,
         "block_choice": block_choice,
         "cpu_baseline": cpu,
-        "clocks": clk,
+        "clocks": head["clocks"],
         "e2e": e2e,
-        "gpu_launches": n_launch,
+        "gpu_launches": head["gpu_launches"],
+        "k0_copy": k0,
+        "per_config": per_config or None,
     }
     print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
 
 
+def _free_port() -> int:
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def launch_replicas(n: int, argv) -> int:
+    """--gpus N without torchrun: start N local processes, one per GPU, with
+    the rendezvous variables torchrun would set (127.0.0.1), and return the
+    worst exit code.  Rank 0 prints the JSON line."""
+    port = _free_port()
+    procs = []
+    for r in range(n):
+        env = dict(os.environ, RANK=str(r), LOCAL_RANK=str(r), WORLD_SIZE=str(n), LOCAL_WORLD_SIZE=str(n),
+                   MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        procs.append(subprocess.Popen([sys.executable, os.path.abspath(__file__), *argv], env=env))
+    rcs = [p.wait() for p in procs]
+    return max(rcs, key=abs)
+
+
+TARGET_CONFIGS = ["gpt_tp", "qwen_grad", "equarx_int8", "flash_int4"]
+
+
 def main(argv=None):
+    argv = sys.argv[1:] if argv is None else list(argv)
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="gpt_tp", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default="equarx_int8", choices=sorted(workloads.WORKLOADS),
+                    help="the headline workload (default: the largest, 8 x [16384 x 8192] bf16)")
+    ap.add_argument("--per-config", default="auto",
+                    help="comma-separated workloads measured after the headline, each as its own report under "
+                         "per_config ('auto': the other target workloads; 'none': no others)")
     ap.add_argument("--impl", default="qta", choices=["qta", "reference"])
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--cpu-rows", type=int, default=0, help="oracle row sample per rank (0: all rows)")
+    ap.add_argument("--cpu-rows", type=int, default=0,
+                    help="oracle row sample per rank of the headline's CPU baseline (0: about 4e8 elements)")
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-k0", action="store_true", help="skip the K0 copy-kernel probe")
     ap.add_argument("--no-clocks", action="store_true", help="skip the nvidia-smi clock window (profiling runs)")
     ap.add_argument("--no-recon", action="store_true", help="skip the reconstruction-error report")
     ap.add_argument("--k1-sms", type=int, default=-1,
@@ -810,12 +978,35 @@ def main(argv=None):
     ap.add_argument("--path", default="fused", choices=["fused", "split"],
                     help="fused: qar_reduce_requant; split: qar_reduce then qar_requant (FP32 sum in HBM)")
     args = ap.parse_args(argv)
+    if args.per_config == "auto":
+        args.per_config = [c for c in TARGET_CONFIGS if c != args.workload]
+    elif args.per_config in ("", "none"):
+        args.per_config = []
+    else:
+        args.per_config = [c.strip() for c in args.per_config.split(",") if c.strip()]
+        bad = [c for c in args.per_config if c not in workloads.WORKLOADS]
+        if bad:
+            ap.error(f"unknown workloads in --per-config: {bad}")
     w = workloads.WORKLOADS[args.workload]
+    ws, _ = _dist()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # N independent replicas, one process per GPU, as torchrun would start them
+        if args.impl == "qta":
+            import torch
+            have = torch.cuda.device_count()
+            if have < args.gpus:
+                print(f"bench.py: --gpus {args.gpus} asks for more GPUs than the {have} visible", file=sys.stderr)
+                return 2
+        return launch_replicas(args.gpus, argv)
+    if args.gpus > 1 and ws != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={ws}", file=sys.stderr)
+        return 2
     if args.impl == "reference":
         run_reference(args, w)
     else:
         run_qta(args, w)
+    return 0
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main())

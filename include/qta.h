@@ -42,10 +42,15 @@
  *    QTA_ERR_CUDA.  An empty tensor (batch*rows*cols == 0) is a no-op that
  *    returns QTA_OK.  Kernels never trap; a pipeline wait that exceeds its
  *    time limit (about 2 s) makes the kernel stop early and record a flag
- *    that qta_device_error() reports.
+ *    that qta_device_error() reports (the stopping warp then waits at most
+ *    about 2 s more for its own loads in flight, so such a kernel ends
+ *    within about 4 s).
  *  - Input values must be finite; non-finite inputs give unspecified (but
  *    memory-safe) codes.
- *  - Results are deterministic and bit-identical run to run.
+ *  - The codec calls (compress, decompress, reduce, requant, their fused
+ *    forms, the ring hops, the state update and the copy) are
+ *    deterministic: bit-identical results run to run.  qta_sq_error is
+ *    not: the order of its FP64 partial sums is not fixed.
  */
 #ifndef QTA_H
 #define QTA_H
@@ -94,10 +99,10 @@ typedef enum {
  *           that is zero, non-finite or below FLT_MIN), state[1] = amax,
  *           then compress with it (two passes over the input).
  * ROUND_UP: a flag OR'ed into either mode.  The block scale r_b becomes
- *           the smallest E4M3 value not below a_b/(448 S) instead of the
- *           nearest one, so y/s_b never exceeds 448 while S covers the tensor
- *           (no saturated codes, coarser steps) -- the rounding alternative
- *           to [TACO] Fig. 7's dual scale. */
+ *           the smallest E4M3 value not below a_b * t (t as in taco_compress)
+ *           instead of the nearest one, so y/s_b never exceeds 448 while S
+ *           covers the tensor (no saturated codes, coarser steps) -- the
+ *           rounding alternative to [TACO] Fig. 7's dual scale. */
 typedef enum { QTA_SCALE_DELAYED = 0, QTA_SCALE_CURRENT = 1, QTA_SCALE_ROUND_UP = 4 } qta_scale_mode;
 
 typedef struct {
@@ -138,9 +143,12 @@ size_t qta_state_bytes(const qta_desc* d);
  * for every scheme: one kernel reads x once and writes codes + scales.
  * QTA_TACO_FP8: per block of `block` along the hidden axis (the reshape),
  * y = H x (unnormalised Sylvester Hadamard, butterfly strides 1,2,..,B/2 in
- * FP32), a_b = max|y|, r_b = E4M3(a_b / (448 S)) (raised to 2^-9 if it
- * rounds to 0 while a_b > 0), s_b = S r_b, codes = E4M3_sat(y * (1/s_b));
- * amax of y goes to state[1] (max-accumulated) [TACO Core claim, Fig. 7].
+ * FP32), a_b = max|y|; with t = 1/(448 S) once per tensor (the product and
+ * the reciprocal each rounded to FP32),
+ * r_b = E4M3(a_b * t) (the product rounded to FP32, then to E4M3; raised to
+ * 2^-9 if it rounds to 0 while a_b > 0), s_b = S r_b (FP32),
+ * codes = E4M3_sat(y * inv) with inv = 1/s_b rounded to FP32; the amax of y
+ * goes to state[1] (max-accumulated) [TACO Core claim, Fig. 7].
  * QTA_INT8_SYM_B64: a = max|x| per 64, s = a/127, q = clamp(rint(x*127/a))
  * [EQuARX Qp1/Qp2].  ASYM: s = fp16((max-min)/Q), z = fp16(min),
  * q = clamp(rint((x-z)/s), 0, Q) [FLASH].
@@ -189,7 +197,8 @@ qta_status qar_reduce(const qta_desc* d, const qta_qtensor* shards, int32_t n_ra
  * pairs (shards -> output): TACO_FP8 -> TACO_FP8, INT8_SYM_B64 ->
  * INT8_SYM_B64, INT4_ASYM_G128 -> INT8_ASYM_G128, INT8_ASYM_G128 ->
  * INT8_ASYM_G128; other pairs return QTA_ERR_UNSUPPORTED (use the two
- * calls). */
+ * calls).  The grid is capped by d->max_sms; out_desc->max_sms is not
+ * used. */
 qta_status qar_reduce_requant(const qta_desc* d, const qta_qtensor* shards, int32_t n_ranks,
                               int64_t row_begin, int64_t row_end, const qta_desc* out_desc,
                               const qta_qtensor* out, int32_t mode, qta_stream_t stream);
@@ -210,8 +219,9 @@ qta_status qar_requant(const qta_desc* d, const float* sum, const qta_qtensor* o
  * 1/B), and the receiver's own tensor x is added, one FP32 rounding per
  * element.  x: device [batch, rows, cols] of x_dtype (bf16, fp16 or fp32),
  * 16-byte aligned; sum_out: device f32 of the same shape, 16-byte aligned,
- * not overlapping x or `in`.  Caller-owned buffers; errors as for the other
- * calls. */
+ * not overlapping x or any buffer of `in` (an overlap is detected on the
+ * host and returns QTA_ERR_INVALID_ARG before anything is enqueued).
+ * Caller-owned buffers; errors as for the other calls. */
 qta_status qar_dequant_add(const qta_desc* d, const qta_qtensor* in, const void* x,
                            int32_t x_dtype, float* sum_out, qta_stream_t stream);
 
@@ -219,7 +229,8 @@ qta_status qar_dequant_add(const qta_desc* d, const qta_qtensor* in, const void*
  * before it travels on, in one kernel: bit-identical to qar_dequant_add
  * followed by qar_requant with `d` (same scheme, block and shape as the
  * incoming tensor; `mode` is the scale mode of a TACO output, whose state is
- * out->state).  `out` must not overlap `in` or x. */
+ * out->state).  No buffer of `out` may overlap x or a buffer of `in`
+ * (checked on the host: QTA_ERR_INVALID_ARG). */
 qta_status qar_dequant_add_requant(const qta_desc* d, const qta_qtensor* in, const void* x,
                                    int32_t x_dtype, const qta_qtensor* out, int32_t mode,
                                    qta_stream_t stream);

@@ -127,6 +127,16 @@ int log2i(int v)
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// Whether the byte ranges [a, a + na) and [b, b + nb) share a byte.
+bool overlaps(const void* a, size_t na, const void* b, size_t nb)
+{
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+size_t dtype_bytes(int32_t dt) { return dt == QTA_FP32 ? 4 : 2; }
+
 // Scheme checks shared by every call: scheme / block combination and shape.
 qta_status check_desc(const qta_desc* d)
 {
@@ -516,6 +526,27 @@ static qta_status accum_impl(const qta_desc* d, const qta_qtensor* in, const voi
     if (!aligned(x, 16) || (!requant && !aligned(sum_out, 16))) return QTA_ERR_ALIGNMENT;
     if ((st = check_qtensor(d, in)) != QTA_OK) return st;
     if (requant && (st = check_qtensor(d, out)) != QTA_OK) return st;
+    {   // the output may not overlap an input: the kernel reads and writes in one pass
+        const size_t n = static_cast<size_t>(n_elems(d));
+        const void* ins[5] = {x, in->codes, in->scales, in->zeros, in->state};
+        const size_t in_n[5] = {n * dtype_bytes(x_dtype), qta_codes_bytes(d), qta_scales_bytes(d),
+                                qta_zeros_bytes(d), qta_state_bytes(d)};
+        const void* outs[4] = {sum_out, nullptr, nullptr, nullptr};
+        size_t out_n[4] = {requant ? 0 : n * 4, 0, 0, 0};
+        if (requant) {
+            outs[0] = out->codes;
+            outs[1] = out->scales;
+            outs[2] = out->zeros;
+            outs[3] = out->state;
+            out_n[0] = qta_codes_bytes(d);
+            out_n[1] = qta_scales_bytes(d);
+            out_n[2] = qta_zeros_bytes(d);
+            out_n[3] = qta_state_bytes(d);
+        }
+        for (int i = 0; i < 4; ++i)
+            for (int j = 0; j < 5; ++j)
+                if (overlaps(outs[i], out_n[i], ins[j], in_n[j])) return QTA_ERR_INVALID_ARG;
+    }
     if (!encoder_ready()) return QTA_ERR_CUDA;
     int sms = 0, smem_sm = 0;
     unsigned int* err = nullptr;

@@ -90,6 +90,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
     return mbar_wait_slow(bar, parity, err);
 }
 
+// Wait for the phase with the given parity to complete until the
+// %globaltimer value `deadline_ns`; false when the deadline passes first.
+static __device__ __noinline__ bool mbar_wait_until(uint64_t* bar, uint32_t parity, uint64_t deadline_ns)
+{
+    for (;;) {
+        for (int i = 0; i < 256; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() > deadline_ns) return false;
+    }
+}
+
 // ------------------------------------------- programmatic dependent launch
 // The kernels are launched with programmatic stream serialization: a kernel
 // may start while its predecessor on the stream drains.  Every thread waits

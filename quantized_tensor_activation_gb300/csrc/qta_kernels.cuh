@@ -458,17 +458,35 @@ struct AmaxTracker {
     }
 };
 
-// Drain path after a timed-out wait: let every load this warp issued land
-// before the CTA may exit (each wait is bounded as well).
-__device__ __forceinline__ void drain_ring(uint64_t* bars, int stages, int stage, uint32_t phase, unsigned int* err)
+// Drain path after a timed-out wait: let the `pending` loads this warp
+// issued and has not consumed (the stages from `stage` on, in ring order)
+// land before the CTA may exit.  All of them share one deadline of about
+// 2 s, so a warp that gives up returns within about twice the wait limit.
+__device__ __forceinline__ void drain_ring(uint64_t* bars, int stages, int stage, uint32_t phase, int pending,
+                                           unsigned int* err)
 {
-    for (int i = 0; i < stages; ++i) {
-        mbar_wait(&bars[stage], phase, err);
+    const uint64_t deadline = globaltimer_ns() + 2000000000ull;
+    for (int i = 0; i < pending && i < stages; ++i) {
+        if (!mbar_wait_until(&bars[stage], phase, deadline)) {
+            atomicOr(err, ERR_WAIT_TIMEOUT);
+            return;
+        }
         if (++stage == stages) {
             stage = 0;
             phase ^= 1u;
         }
     }
+}
+
+// Loads in flight for the tiles first, first + W, ... of a warp when it
+// stops at tile wt: the tiles wt, wt + W, ..., wt + (stages-1) W that exist
+// (each consumed tile t refilled its stage with t + stages W).
+__device__ __forceinline__ int pending_tiles(int wt, int W, int n_tiles, int stages)
+{
+    int n = 0;
+    for (int j = 0; j < stages; ++j)
+        if (wt + j * W < n_tiles) ++n;
+    return n;
 }
 
 
@@ -717,12 +735,13 @@ compress_kernel(const __grid_constant__ CompressParams p)
     uint32_t phase = 0;
     int k = 0;
     bool aborted = false;
-
+    int pending = 0;
     for (int wt = first; wt < p.n_warp_tiles; wt += W, ++k) {
         quant.begin(qo, wt * 32, lane);
         const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[stage], phase, p.err));
         if (!ok) {
             aborted = true;
+            pending = pending_tiles(wt, W, p.n_warp_tiles, C::STAGES);
             break;
         }
         u64 v[32];
@@ -748,7 +767,7 @@ compress_kernel(const __grid_constant__ CompressParams p)
     quant.finish(qo, lane);
     if (lane == 0) {
         bulk_wait_all();
-        if (aborted) drain_ring(bars, C::STAGES, stage, phase, p.err);
+        if (aborted) drain_ring(bars, C::STAGES, stage, phase, pending, p.err);
     }
     if constexpr (SCH == S_TACO) cta_amax_flush(amax_tab, p.state, qo.amax_slots);
 }
@@ -829,6 +848,7 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
     uint32_t phase = 0;
     int k = 0;
     bool aborted = false;
+    int pending = 0;
     // metadata of the next warp tile is fetched one tile ahead
     SegMeta<SCH> meta;
     if (first < p.n_warp_tiles && first * 32 + lane < p.M)
@@ -843,6 +863,7 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
         const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[stage], phase, p.err));
         if (!ok) {
             aborted = true;
+            pending = pending_tiles(wt, W, p.n_warp_tiles, C::STAGES);
             break;
         }
         float s, z;
@@ -890,7 +911,7 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
     }
     if (lane == 0) {
         bulk_wait_all();
-        if (aborted) drain_ring(bars, C::STAGES, stage, phase, p.err);
+        if (aborted) drain_ring(bars, C::STAGES, stage, phase, pending, p.err);
     }
 }
 
@@ -1121,7 +1142,8 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
     if constexpr (OSCH != OUT_F32) quant.finish(qo, lane);
     if (lane == 0) {
         bulk_wait_all();
-        if (aborted) drain_ring(bars, C::STAGES, stage, phase, p.err);
+        // units [unit, unit + STAGES) that exist were issued and not consumed
+        if (aborted) drain_ring(bars, C::STAGES, stage, phase, min(C::STAGES, total_units - unit), p.err);
     }
     if constexpr (OSCH == S_TACO) cta_amax_flush(amax_tab, p.q_state, qo.amax_slots);
 }
@@ -1215,6 +1237,7 @@ accum_kernel(const __grid_constant__ AccumParams p)
     int stage = 0;
     uint32_t phase = 0;
     bool aborted = false;
+    int pending = 0;
     SegMeta<SCH> meta;   // metadata of the next warp tile, fetched one tile ahead
     if (first < p.n_warp_tiles && first * 32 + lane < p.M)
         meta.load(p.scales, p.zeros, p.state, first * 32 + lane, p.lanes_log2, p.seg_per_tensor);
@@ -1229,6 +1252,7 @@ accum_kernel(const __grid_constant__ AccumParams p)
         const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[stage], phase, p.err));
         if (!ok) {
             aborted = true;
+            pending = pending_tiles(wt, W, p.n_warp_tiles, C::STAGES);
             break;
         }
         float s, z;
@@ -1275,7 +1299,7 @@ accum_kernel(const __grid_constant__ AccumParams p)
     if constexpr (OSCH != OUT_F32) quant.finish(qo, lane);
     if (lane == 0) {
         bulk_wait_all();
-        if (aborted) drain_ring(bars, C::STAGES, stage, phase, p.err);
+        if (aborted) drain_ring(bars, C::STAGES, stage, phase, pending, p.err);
     }
     if constexpr (OSCH == S_TACO) cta_amax_flush(amax_tab, p.q_state, qo.amax_slots);
 }

@@ -37,7 +37,15 @@ def chunk_orders(n: int, j: int, semi: bool):
     return chains
 
 
+def _alloc_stream(stream, dev):
+    """The stream the ring's work runs on, as a torch stream (a raw handle
+    or None means the current stream)."""
+    return stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.current_stream(dev)
+
+
 def _chunk_desc(d: Desc, n: int) -> Desc:
+    if n < 2:
+        raise ValueError("a ring needs at least two ranks")
     if d.batch != 1 or d.rows % n:
         raise ValueError("the ring takes one [rows, cols] tensor per rank with rows divisible by the ranks")
     return desc(d.scheme, d.block, d.rows // n, d.cols, max_sms=d.max_sms)
@@ -55,9 +63,12 @@ def reduce_scatter(d: Desc, xs: torch.Tensor, semi: bool = False, hop_partials: 
     rc = dc.rows
     dt = _DT[xs.dtype]
     dev = xs.device
-    out = torch.empty((d.rows, d.cols), dtype=torch.float32, device=dev)
-    tmp = torch.empty((rc, d.cols), dtype=torch.float32, device=dev)
-    bufs = [[alloc_qtensor(dc, dev), alloc_qtensor(dc, dev)] for _ in range(2)]
+    # the buffers are allocated on the stream that uses them, so that the
+    # caching allocator orders their reuse after this work
+    with torch.cuda.stream(_alloc_stream(stream, dev)):
+        out = torch.empty((d.rows, d.cols), dtype=torch.float32, device=dev)
+        tmp = torch.empty((rc, d.cols), dtype=torch.float32, device=dev)
+        bufs = [[alloc_qtensor(dc, dev), alloc_qtensor(dc, dev)] for _ in range(2)]
 
     def chunk(r, j):
         return xs[r, j * rc:(j + 1) * rc]
@@ -96,8 +107,9 @@ def allreduce(d: Desc, xs: torch.Tensor, semi: bool = False, out_dtype=torch.flo
     s = reduce_scatter(d, xs, semi, stream=stream)
     dc = _chunk_desc(d, n)
     rc = dc.rows
-    g = alloc_qtensor(dc, xs.device)
-    y = torch.empty((d.rows, d.cols), dtype=out_dtype, device=xs.device)
+    with torch.cuda.stream(_alloc_stream(stream, xs.device)):
+        g = alloc_qtensor(dc, xs.device)
+        y = torch.empty((d.rows, d.cols), dtype=out_dtype, device=xs.device)
     for j in range(n):
         qar_requant(dc, s[j * rc:(j + 1) * rc], g, SCALE_CURRENT, stream)
         taco_decompress(dc, g, y[j * rc:(j + 1) * rc], _DT[out_dtype], stream)

@@ -170,3 +170,29 @@ def test_sq_error_argument_checks(L):
     assert f(None, 0, 16, 4, 16, None) == INV
     assert f(16, 0, 18, 4, 16, None) == ALN
     assert f(16, 0, 16, 4, 20, None) == ALN
+
+
+def test_ring_hop_rejects_overlapping_outputs(L):
+    # an output that overlaps the local tensor x or a buffer of the incoming
+    # tensor is refused on the host, before anything is enqueued (the
+    # addresses below are never dereferenced)
+    INV = qta.QTA_ERR_INVALID_ARG
+    d = ctypes.byref(qta.desc(0, 128, 4, 128))                  # TACO, 512 elements
+    qin = qta.QTensorC(0x100000, 0x200000, 0x300000, 0x400000)
+    x = 0x500000                                                # bf16: 1024 bytes
+    f, g = L.qar_dequant_add, L.qar_dequant_add_requant
+    assert f(d, ctypes.byref(qin), x, 0, x + 512, None) == INV            # sum_out inside x
+    assert f(d, ctypes.byref(qin), x, 0, x - 2032, None) == INV           # sum_out's end inside x
+    assert f(d, ctypes.byref(qin), x, 0, 0x100000 - 16, None) == INV      # over the incoming codes
+    assert f(d, ctypes.byref(qin), x, 0, 0x400000, None) == INV           # over the incoming state
+    out = qta.QTensorC(0x600000, 0x700000, 0x800000, 0x200000)            # out state = in scales
+    assert g(d, ctypes.byref(qin), x, 0, ctypes.byref(out), 0, None) == INV
+    out = qta.QTensorC(x, 0x700000, 0x800000, 0x900000)                   # out codes = x
+    assert g(d, ctypes.byref(qin), x, 0, ctypes.byref(out), 0, None) == INV
+
+
+def test_ring_rejects_fewer_than_two_ranks():
+    from quantized_tensor_activation_gb300 import ring
+    with pytest.raises(ValueError):
+        ring._chunk_desc(qta.desc("taco_fp8", 128, 4, 256), 1)
+    assert ring._chunk_desc(qta.desc("taco_fp8", 128, 4, 256), 2).rows == 2

@@ -47,3 +47,21 @@ def test_single_process_passthrough():
     import bench
     assert bench.max_over_ranks(3.25) == 3.25
     assert bench.job_throughput(1e9, 2.0, 1) == pytest.approx(500.0)
+
+
+def test_gpus_flag_without_torchrun_starts_replicas():
+    # --gpus 2 outside torchrun starts two local replica processes with the
+    # rendezvous variables set; only rank 0 prints, and the line reports both
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1",
+                        "--warmup", "0", "--workload", "taco_tiny", "--ref-rows", "8"],
+                       cwd=root, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2

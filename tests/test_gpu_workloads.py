@@ -7,11 +7,15 @@ Step checked: compress all ranks (CURRENT mode for TACO, so the per-tensor
 scale is a function of the data) -> dequantize-reduce all rows -> requantize
 the sum for the gather stage (DELAYED, with a per-shard scale fixed by the
 test) -> decompress."""
+import multiprocessing as mp
+import os
+
 import numpy as np
 import pytest
 import torch
 
 import oracle as orc
+import oracle_pool
 import quantized_tensor_activation_gb300 as qta
 import workloads
 from gpu_util import ORC_SCH, assert_close_f32, assert_same, bits, device
@@ -26,6 +30,39 @@ def dev():
     return device()
 
 
+@pytest.fixture(scope="module")
+def pool():
+    ctx = mp.get_context("spawn")
+    p = ctx.Pool(max(1, min(8, (os.cpu_count() or 2) - 1)))
+    yield p
+    p.close()
+    p.join()
+
+
+def _oracle_k1_state(pool, xb, N, R, C, B):
+    """The oracle's CURRENT-mode per-tensor state {S, amax} of every rank,
+    over whole rank tensors (max |H x| gathered shard by shard)."""
+    gr = R // N
+    parts = pool.map(oracle_pool.rows_amax, [(np.ascontiguousarray(xb[:, j * gr:(j + 1) * gr]).reshape(-1),
+                                              orc.BF16, N, gr, C, B) for j in range(N)])
+    amax = np.max(np.array(parts, dtype=np.float32), axis=0)
+    st = np.zeros(2 * N, dtype=np.float32)
+    st[0::2] = [orc.scale_from_amax(a) for a in amax]
+    st[1::2] = amax
+    return st
+
+
+def _oracle_gather_state(pool, xb, N, R, C, B, gB, st1, S2, fused):
+    """The oracle's gather-stage state of every output shard (DELAYED, scale
+    S2[j], amax over the whole shard), computed shard by shard."""
+    gr = R // N
+    tasks = [(np.ascontiguousarray(xb[:, j * gr:(j + 1) * gr]).reshape(-1), orc.BF16, N, gr, C, orc.TACO_FP8, B,
+              list(st1[0::2]), orc.TACO_FP8, gB, [S2[2 * j], 0.0], orc.DELAYED, fused, [0], orc.BF16)
+             for j in range(N)]
+    res = pool.map(oracle_pool.shard_chain, tasks)
+    return np.array([v for r in res for v in r["g_state"]], dtype=np.float32)
+
+
 def _rows_of(buf: torch.Tensor, rows_idx, per_row: int) -> np.ndarray:
     """Bytes of the given rows of a flat byte buffer with per_row bytes/row."""
     b = buf.view(-1, per_row)[torch.as_tensor(rows_idx, device=buf.device)]
@@ -33,7 +70,7 @@ def _rows_of(buf: torch.Tensor, rows_idx, per_row: int) -> np.ndarray:
 
 
 @pytest.mark.parametrize("name", ["taco_tiny", "gpt_tp", "qwen_grad", "equarx_int8", "flash_int4"])
-def test_workload_full_size(dev, name):
+def test_workload_full_size(dev, pool, name):
     w = workloads.WORKLOADS[name]
     N, R, C, B, gB = w.ranks, w.rows, w.cols, w.block, w.gather_block
     s1, s2 = qta.SCHEMES[w.scheme], qta.SCHEMES[w.gather_scheme]
@@ -62,16 +99,19 @@ def test_workload_full_size(dev, name):
     torch.cuda.synchronize()
     assert qta.qta_device_error() == 0
 
-    # ---- per-tensor scale (TACO, CURRENT mode): oracle over whole tensors
+    # ---- per-tensor scales (TACO): the compress's in CURRENT mode and the
+    # gather stage's (DELAYED with S2, amax over each whole output shard),
+    # both from the oracle over whole tensors
     st = None
     if s1 == qta.TACO_FP8:
-        st = np.zeros(2 * N, dtype=np.float32)
-        for r in range(N):
-            xr = x[r].float().cpu().numpy().reshape(-1)
-            amax = np.float32(np.abs(orc.fwht(xr, B)).max())
-            st[2 * r] = orc.scale_from_amax(amax)
-            st[2 * r + 1] = amax
+        xall = bits(x).reshape(N, R, C)
+        st = _oracle_k1_state(pool, xall, N, R, C, B)
         assert_same("per-tensor state", q.state, st)
+        if s2 == qta.TACO_FP8:
+            assert in_dt == qta.BF16
+            gst = _oracle_gather_state(pool, xall, N, R, C, B, gB, st, S2, fused=False)
+            assert_same("gather-stage state", g.state, gst)
+        del xall
 
     # ---- sampled rows
     rng = np.random.default_rng(hash(name) % 2 ** 32)
@@ -115,7 +155,7 @@ def test_workload_full_size(dev, name):
 
 
 @pytest.mark.parametrize("name", ["taco_tiny", "gpt_tp", "qwen_grad", "equarx_int8", "flash_int4"])
-def test_workload_full_size_fused_as_benched(dev, name):
+def test_workload_full_size_fused_as_benched(dev, pool, name):
     """The timed step's own calls at full size: the compress on a capped SM
     count (as the benchmark may choose), the fused reduce + requant with the
     gather stage's per-shard DELAYED scales, the decompress; sampled rows
@@ -148,7 +188,15 @@ def test_workload_full_size_fused_as_benched(dev, name):
     rows = np.unique(np.concatenate([[0, R - 1, gr - 1, gr], rng.choice(R, 8, replace=False)]))
     k = len(rows)
     xb = bits(x[:, torch.as_tensor(rows, device=dev)].contiguous().cpu())
-    st = None if s1 != qta.TACO_FP8 else bits(q.state).view(np.float32).copy()   # checked by the test above
+    st = None
+    if s1 == qta.TACO_FP8:
+        xall = bits(x).reshape(N, R, C)
+        st = _oracle_k1_state(pool, xall, N, R, C, B)
+        assert_same("per-tensor state", q.state, st)
+        if s2 == qta.TACO_FP8:
+            gst = _oracle_gather_state(pool, xall, N, R, C, B, gB, st, S2, fused=True)
+            assert_same("gather-stage state", g.state, gst)
+        del xall
     shards = []
     for r in range(N):
         st_r = None if st is None else st[2 * r:2 * r + 2].copy()
