@@ -34,6 +34,7 @@ implementation of the same path) on a bounded row sample of the workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import glob
 import json
@@ -460,6 +461,7 @@ def measure_workload(qta, w, args, dev, ws: int, local: int, headline: bool) -> 
             qta.taco_update_scale(states, n_state)
         if ev:
             ev[5].record()
+            ev[6].record()          # an interval with no kernel: the cost of the event nodes themselves
         launches[0] += (3 if fused else 4) + int(n_state > 0)
 
     fused = args.path == "fused"
@@ -504,7 +506,7 @@ def measure_workload(qta, w, args, dev, ws: int, local: int, headline: bool) -> 
     pad = 0 if args.no_clocks else max(1, int(600.0 / max(a.elapsed_time(b) / 3, 1e-3)))
 
     def timed(fused_path):
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         launches[0] = 0
@@ -544,7 +546,7 @@ def measure_workload(qta, w, args, dev, ws: int, local: int, headline: bool) -> 
 
     def graph_with_events(fused_path):
         try:
-            evl = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)]
+            evl = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(7)]
                    for _ in range(args.steps)]
             gr_ = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gr_):
@@ -701,10 +703,11 @@ def measure_workload(qta, w, args, dev, ws: int, local: int, headline: bool) -> 
     alg = algorithmic_bytes(w)
 
     def kernel_table(ev_list, fused_path):
-        per_k = {k: [] for k in ("K1", "K2", "K3", "K4", "U")}
+        per_k = {k: [] for k in ("K1", "K2", "K3", "K4", "U", "E")}
         for e in ev_list:
             for j, k in enumerate(per_k):
                 per_k[k].append(e[j].elapsed_time(e[j + 1]))
+        ev_ms = statistics.mean(per_k["E"])
         names = {"K1": "taco_compress", "K2": "qar_reduce_requant" if fused_path else "qar_reduce",
                  "K3": None if fused_path else "qar_requant", "K4": "taco_decompress"}
         table = {}
@@ -713,9 +716,14 @@ def measure_workload(qta, w, args, dev, ws: int, local: int, headline: bool) -> 
                 continue
             ms = statistics.mean(per_k[k])
             nbytes = alg["K23"] if (k == "K2" and fused_path) else alg[k]
+            net = max(ms - ev_ms, 1e-6)
             table[k] = {"call": names[k], "ms": ms, "gb_s": nbytes / (ms * 1e-3) / 1e9,
-                        "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / peak, "algorithmic_bytes": nbytes}
-        table["U"] = {"call": "taco_update_scale", "ms": statistics.mean(per_k["U"])}
+                        "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / peak, "algorithmic_bytes": nbytes,
+                        "frac_of_hbm_net": nbytes / (net * 1e-3) / 1e9 / peak}
+        table["U"] = {"call": "taco_update_scale" if n_state else None, "ms": statistics.mean(per_k["U"])}
+        table["event_interval_ms"] = ev_ms
+        table["note"] = ("ms: between the kernel's two event nodes; event_interval_ms: two consecutive event "
+                         "nodes with no kernel between them, in the same graph; frac_of_hbm_net uses ms minus it")
         return table
 
     kern = kernel_table(evs, fused)
@@ -782,6 +790,63 @@ def measure_workload(qta, w, args, dev, ws: int, local: int, headline: bool) -> 
         del xs, q, g, shards, ssum, y, states
     del graphs, tgraph
     return rep
+
+
+def ash_report(qta, dev, names=("gpt_tp", "flash_int4"), iters: int = 10) -> dict:
+    """The adaptive rescaling of the ASH transform against the plain one: on
+    each workload's full-size rank tensors, compressed with TACO FP8 (B = 128,
+    CURRENT scale), the per-channel factors from the channel amax over all
+    ranks; MSE of one rank's round trip and of the all-reduce (compress all
+    ranks, fused reduce + requant into the gather stage, decompress) against
+    the float64 inputs / sum, with and without the factors, and the compress
+    time with and without them (CUDA events, 10 calls)."""
+    import torch
+
+    out = {"note": "TACO FP8 B128 on the workload's tensors (whatever its own scheme); factors from "
+                   "taco_channel_amax over all ranks + taco_ash_update"}
+    for name in names:
+        w = workloads.WORKLOADS[name]
+        N, R, C = w.ranks, w.rows, w.cols
+        dt = qta.BF16 if w.dtype == "bf16" else qta.FP16
+        x = workloads.make_rank_inputs(w, device=dev, seed=3)
+        d = qta.desc(qta.TACO_FP8, 128, R, C, batch=N)
+        chan = qta.alloc_chan(C, dev)
+        qta.taco_channel_amax(d, x, dt, chan)
+        qta.taco_ash_update(chan, C)
+        e = torch.log2(chan[C:2 * C]).round().to(torch.int64).cpu()
+        rep = {"channels_rescaled": int((e > 0).sum()), "factor_histogram": torch.bincount(e, minlength=4).tolist()}
+        exact = x.double().sum(dim=0)
+        for tag, ch in (("plain", None), ("rescaled", chan)):
+            q = qta.alloc_qtensor(d, dev)
+            q.chan = ch
+            qta.taco_compress(d, x, dt, q, qta.SCALE_CURRENT)
+            y0 = torch.empty((R, C), dtype=torch.float32, device=dev)
+            qta.taco_decompress(qta.desc(qta.TACO_FP8, 128, R, C), q.shard(0), y0, qta.FP32)
+            dg = qta.desc(qta.TACO_FP8, 128, R // N, C, batch=N)
+            g = qta.alloc_qtensor(dg, dev)
+            g.chan = ch
+            qta.qar_reduce_requant(qta.desc(qta.TACO_FP8, 128, R, C), [q.shard(r) for r in range(N)], 0, R, dg, g,
+                                   qta.SCALE_CURRENT)
+            y = torch.empty((R, C), dtype=torch.float32, device=dev)
+            qta.taco_decompress(dg, g, y, qta.FP32)
+            e0 = y0.double() - x[0].double()
+            ea = y.double() - exact
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(iters):
+                qta.taco_compress(d, x, dt, q, qta.SCALE_DELAYED)
+            b.record()
+            torch.cuda.synchronize()
+            rep[tag] = {"round_trip_mse_rank0": float((e0 * e0).mean()), "allreduce_mse": float((ea * ea).mean()),
+                        "compress_ms": a.elapsed_time(b) / iters}
+            del q, g, y0, y, e0, ea
+        rep["round_trip_mse_ratio"] = rep["rescaled"]["round_trip_mse_rank0"] / rep["plain"]["round_trip_mse_rank0"]
+        rep["allreduce_mse_ratio"] = rep["rescaled"]["allreduce_mse"] / rep["plain"]["allreduce_mse"]
+        out[name] = rep
+        del x, exact, chan
+        torch.cuda.empty_cache()
+    assert qta.qta_device_error() == 0
+    return out
 
 
 def copy_probe(qta, dev, nbytes: int = 1 << 30, iters: int = 10) -> dict:
@@ -852,8 +917,9 @@ def run_qta(args, w):
             t = kernel_table(evs3, fused)
             sm_sweep.append({"max_sms": n_sms, "eager_ms_per_step": ms,
                              "value": in_bytes / (ms * 1e-3) / 1e9 * ws,
-                             "kernels_ms": {k: v["ms"] for k, v in t.items()},
-                             "kernels_frac_of_hbm": {k: v["frac_of_hbm"] for k, v in t.items() if "frac_of_hbm" in v}})
+                             "kernels_ms": {k: v["ms"] for k, v in t.items() if isinstance(v, dict)},
+                             "kernels_frac_of_hbm": {k: v["frac_of_hbm"] for k, v in t.items()
+                                                     if isinstance(v, dict) and "frac_of_hbm" in v}})
     del xs, shards, q, x
     torch.cuda.empty_cache()
 
@@ -868,6 +934,7 @@ def run_qta(args, w):
         torch.cuda.empty_cache()
 
     k0 = None if args.no_k0 else copy_probe(qta, dev)
+    ash = None if args.no_ash else ash_report(qta, dev)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -909,6 +976,7 @@ def run_qta(args, w):
         "e2e": e2e,
         "gpu_launches": head["gpu_launches"],
         "k0_copy": k0,
+        "ash_rescaling": ash,
         "per_config": per_config or None,
     }
     print(json.dumps(line), flush=True)
@@ -958,9 +1026,14 @@ def main(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=0,
                     help="oracle row sample per rank of the headline's CPU baseline (0: about 4e8 elements)")
     ap.add_argument("--ref-rows", type=int, default=256)
+    ap.add_argument("--rows", type=int, default=0,
+                    help="rows per rank of the headline workload (0: the workload's own; profiling captures of a "
+                         "smaller case)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-k0", action="store_true", help="skip the K0 copy-kernel probe")
+    ap.add_argument("--no-ash", action="store_true",
+                    help="skip the adaptive-rescaling report (TACO with per-channel factors vs plain)")
     ap.add_argument("--no-clocks", action="store_true", help="skip the nvidia-smi clock window (profiling runs)")
     ap.add_argument("--no-recon", action="store_true", help="skip the reconstruction-error report")
     ap.add_argument("--k1-sms", type=int, default=-1,
@@ -988,6 +1061,11 @@ def main(argv=None):
         if bad:
             ap.error(f"unknown workloads in --per-config: {bad}")
     w = workloads.WORKLOADS[args.workload]
+    if args.rows:
+        # a smaller case of the same workload (profiling captures): rows per rank
+        if args.rows % w.ranks:
+            ap.error("--rows must be a multiple of the workload's rank count")
+        w = dataclasses.replace(w, rows=args.rows)
     ws, _ = _dist()
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
         # N independent replicas, one process per GPU, as torchrun would start them

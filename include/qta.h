@@ -124,12 +124,22 @@ typedef struct {
  *  scales: u8 [n_blocks] E4M3 bits (TACO), f32 [n_blocks] (INT8 sym),
  *          fp16 bits [n_blocks] (asym)
  *  zeros : fp16 bits [n_blocks] (asym only, else unused)
- *  state : f32 [batch][2] = {S, amax} (TACO only, else unused) */
+ *  state : f32 [batch][2] = {S, amax} (TACO only, else unused)
+ *  chan  : NULL, or (TACO only) the adaptive rescaling of the Adaptive
+ *          Scale-Hadamard transform [TACO Core claim; Fig. 7: adaptive
+ *          rescaling before the ASH transform]: f32 [3][cols] = down, up,
+ *          amax, 16-byte aligned, shared by every tensor of a batch and by
+ *          every rank of a reduction.  The compress multiplies element
+ *          (row, c) by down[c] = 2^-e[c] before the transform; the decompress
+ *          and the FP32 reduce multiply by up[c] = 2^e[c] after the inverse
+ *          (both exact for powers of two barring underflow).  The factors
+ *          come from taco_channel_amax + taco_ash_update. */
 typedef struct {
     void* codes;
     void* scales;
     void* zeros;
     float* state;
+    float* chan;
 } qta_qtensor;
 
 /* Byte sizes of the buffers of a quantized tensor described by `d`
@@ -174,7 +184,9 @@ qta_status taco_decompress(const qta_desc* d, const qta_qtensor* in, void* y,
  * then acc = fmaf(code_r, s_r, acc) (one FP32 rounding per rank); asym
  * acc = fmaf(q_0, s_0, z_0), then acc += fmaf(q_r, s_r, z_r).  For
  * QTA_TACO_FP8 the sum is formed in the Hadamard domain and the inverse
- * transform (butterfly, then 1/B) is applied once to it.
+ * transform (butterfly, then 1/B) is applied once to it, then the channel
+ * factors up[c] when the shards carry the adaptive rescaling (every shard
+ * must carry the same chan pointer, else QTA_ERR_INVALID_ARG).
  * sum_out: device f32 [row_end-row_begin, cols], 16-byte aligned. */
 qta_status qar_reduce(const qta_desc* d, const qta_qtensor* shards, int32_t n_ranks,
                       int64_t row_begin, int64_t row_end, float* sum_out,
@@ -198,7 +210,9 @@ qta_status qar_reduce(const qta_desc* d, const qta_qtensor* shards, int32_t n_ra
  * INT8_SYM_B64, INT4_ASYM_G128 -> INT8_ASYM_G128, INT8_ASYM_G128 ->
  * INT8_ASYM_G128; other pairs return QTA_ERR_UNSUPPORTED (use the two
  * calls).  The grid is capped by d->max_sms; out_desc->max_sms is not
- * used. */
+ * used.  With the adaptive rescaling, out->chan must be the shards' chan
+ * (the factors then cancel between the reduce and the requant), else
+ * QTA_ERR_UNSUPPORTED. */
 qta_status qar_reduce_requant(const qta_desc* d, const qta_qtensor* shards, int32_t n_ranks,
                               int64_t row_begin, int64_t row_end, const qta_desc* out_desc,
                               const qta_qtensor* out, int32_t mode, qta_stream_t stream);
@@ -221,7 +235,9 @@ qta_status qar_requant(const qta_desc* d, const float* sum, const qta_qtensor* o
  * 16-byte aligned; sum_out: device f32 of the same shape, 16-byte aligned,
  * not overlapping x or any buffer of `in` (an overlap is detected on the
  * host and returns QTA_ERR_INVALID_ARG before anything is enqueued).
- * Caller-owned buffers; errors as for the other calls. */
+ * The ring hops take no adaptive rescaling (a chan returns
+ * QTA_ERR_UNSUPPORTED).  Caller-owned buffers; errors as for the other
+ * calls. */
 qta_status qar_dequant_add(const qta_desc* d, const qta_qtensor* in, const void* x,
                            int32_t x_dtype, float* sum_out, qta_stream_t stream);
 
@@ -245,6 +261,31 @@ qta_status qar_dequant_add_requant(const qta_desc* d, const qta_qtensor* in, con
  * the last bits between calls). */
 qta_status qta_sq_error(const void* a, int32_t a_dtype, const float* b, int64_t n, double* out,
                         qta_stream_t stream);
+
+/* Adaptive rescaling state: bytes of the chan buffer for `cols` channels
+ * (3 * cols floats; 0 for cols <= 0).  A fresh state holds down = up = 1 and
+ * amax = 0 (no rescaling). */
+size_t qta_chan_bytes(int64_t cols);
+
+/* taco_channel_amax -- per-channel statistics of the adaptive rescaling
+ * [TACO Core claim: data-driven reshaping with an Adaptive Scale-Hadamard
+ * transform]: chan[2*cols + c] = max(chan[2*cols + c], max over every row of
+ * every tensor of |x[.., c]|).  x: device [batch, rows, cols] of x_dtype
+ * (bf16, fp16, fp32), 16-byte aligned; chan: device f32 [3*cols], 16-byte
+ * aligned, not overlapping x.  d gives the shape only (any valid scheme).
+ * Run on the data of earlier steps (or a calibration batch); the codec calls
+ * use the factors the last taco_ash_update wrote. */
+qta_status taco_channel_amax(const qta_desc* d, const void* x, int32_t x_dtype, float* chan,
+                             qta_stream_t stream);
+
+/* taco_ash_update -- the channel factors from the accumulated amax, then
+ * amax = 0.  Rule (the pages give none): with E(v) the binary exponent of v
+ * (floor(log2 v); -127 for subnormals) and E_ref the lower median of
+ * E(amax[c]) over the channels with amax[c] > 0, e[c] = min(3, max(0,
+ * E(amax[c]) - E_ref - 2)) (0 for amax[c] == 0): channels at least a factor
+ * 8 above the typical range are divided by up to 8.  down[c] = 2^-e[c],
+ * up[c] = 2^e[c].  chan: device f32 [3*cols], 16-byte aligned.  One CTA. */
+qta_status taco_ash_update(float* chan, int64_t cols, qta_stream_t stream);
 
 /* taco_update_scale -- end-of-step update of the dual-scale state of
  * n_tensors tensors [TACO Core claim: stability across training steps]:

@@ -91,6 +91,18 @@ def lib():
             L.orc_reduce_requant.restype = i32
             L.orc_dequant_add.argtypes = [i32, i32, vp, vp, vp, fp, i64, i64, i64, vp, i32, fp]
             L.orc_dequant_add.restype = i32
+            L.orc_compress_chan.argtypes = L.orc_compress.argtypes + [fp]
+            L.orc_compress_chan.restype = i32
+            L.orc_decompress_chan.argtypes = L.orc_decompress.argtypes + [fp]
+            L.orc_decompress_chan.restype = i32
+            L.orc_reduce_chan.argtypes = L.orc_reduce.argtypes + [fp]
+            L.orc_reduce_chan.restype = i32
+            L.orc_reduce_requant_chan.argtypes = L.orc_reduce_requant.argtypes + [fp]
+            L.orc_reduce_requant_chan.restype = i32
+            L.orc_channel_amax.argtypes = [vp, i32, i64, i64, i64, fp]
+            L.orc_channel_amax.restype = i32
+            L.orc_ash_update.argtypes = [fp, i64]
+            L.orc_ash_update.restype = i32
             _lib = L
     return _lib
 
@@ -168,9 +180,18 @@ def codes_nbytes(scheme: int, n_elems: int) -> int:
     return n_elems // 2 if scheme == INT4_ASYM else n_elems
 
 
+def _chan(chan, cols):
+    if chan is None:
+        return None
+    assert chan.dtype == np.float32 and chan.flags.c_contiguous and chan.size == 3 * cols
+    return chan
+
+
 def compress(scheme: int, B: int, x: np.ndarray, in_dtype: int, batch: int, rows: int,
-             cols: int, state: np.ndarray | None = None, mode: int = DELAYED):
-    """Returns (codes, scales, zeros); updates ``state`` in place for TACO."""
+             cols: int, state: np.ndarray | None = None, mode: int = DELAYED, chan=None):
+    """Returns (codes, scales, zeros); updates ``state`` in place for TACO.
+    chan: the adaptive rescaling's per-channel state, float32 [3 * cols] =
+    down, up, amax (TACO only; None: no rescaling)."""
     E = batch * rows * cols
     x = np.ascontiguousarray(x)
     assert x.size == E
@@ -184,29 +205,30 @@ def compress(scheme: int, B: int, x: np.ndarray, in_dtype: int, batch: int, rows
     else:
         scales = np.zeros(E // 128, dtype=np.uint16)
         zeros = np.zeros(E // 128, dtype=np.uint16)
-    rc = lib().orc_compress(scheme, B, _ptr(x), in_dtype, batch, rows, cols,
-                            _ptr(state), mode, _ptr(codes), _ptr(scales), _ptr(zeros))
+    rc = lib().orc_compress_chan(scheme, B, _ptr(x), in_dtype, batch, rows, cols,
+                                 _ptr(state), mode, _ptr(codes), _ptr(scales), _ptr(zeros),
+                                 _ptr(_chan(chan, cols)))
     if rc:
         raise ValueError(f"oracle compress rejected the arguments ({rc})")
     return codes, scales, zeros
 
 
 def decompress(scheme: int, B: int, codes, scales, zeros, state, batch: int, rows: int,
-               cols: int, out_dtype: int) -> np.ndarray:
+               cols: int, out_dtype: int, chan=None) -> np.ndarray:
     E = batch * rows * cols
     out = np.zeros(E, dtype=np.float32 if out_dtype == FP32 else np.uint16)
     st = None if state is None else np.ascontiguousarray(state, dtype=np.float32)
-    rc = lib().orc_decompress(scheme, B, _ptr(np.ascontiguousarray(codes)),
-                              _ptr(np.ascontiguousarray(scales)),
-                              _ptr(None if zeros is None else np.ascontiguousarray(zeros)),
-                              _ptr(st), batch, rows, cols, _ptr(out), out_dtype)
+    rc = lib().orc_decompress_chan(scheme, B, _ptr(np.ascontiguousarray(codes)),
+                                   _ptr(np.ascontiguousarray(scales)),
+                                   _ptr(None if zeros is None else np.ascontiguousarray(zeros)),
+                                   _ptr(st), batch, rows, cols, _ptr(out), out_dtype, _ptr(_chan(chan, cols)))
     if rc:
         raise ValueError(f"oracle decompress rejected the arguments ({rc})")
     return out
 
 
 def reduce(scheme: int, B: int, shards, rows: int, cols: int, row_begin: int = 0,
-           row_end: int | None = None) -> np.ndarray:
+           row_end: int | None = None, chan=None) -> np.ndarray:
     """shards: list of (codes, scales, zeros, state) per rank, one tensor each."""
     if row_end is None:
         row_end = rows
@@ -219,8 +241,8 @@ def reduce(scheme: int, B: int, shards, rows: int, cols: int, row_begin: int = 0
     st_keep = [None if s[3] is None else np.ascontiguousarray(s[3], dtype=np.float32) for s in keep]
     states = VP(*[_ptr(a) for a in st_keep]) if st_keep[0] is not None else None
     out = np.zeros((row_end - row_begin) * cols, dtype=np.float32)
-    rc = lib().orc_reduce(scheme, B, n, codes, scales, zeros, states, rows, cols,
-                          row_begin, row_end, _ptr(out))
+    rc = lib().orc_reduce_chan(scheme, B, n, codes, scales, zeros, states, rows, cols,
+                               row_begin, row_end, _ptr(out), _ptr(_chan(chan, cols)))
     if rc:
         raise ValueError(f"oracle reduce rejected the arguments ({rc})")
     return out
@@ -239,7 +261,8 @@ def _shard_arrays(shards):
 
 
 def reduce_requant(scheme: int, B: int, shards, rows: int, cols: int, row_begin: int, row_end: int,
-                   out_scheme: int, out_B: int, out_batch: int, out_state=None, mode: int = DELAYED):
+                   out_scheme: int, out_B: int, out_batch: int, out_state=None, mode: int = DELAYED,
+                   chan=None):
     """Fused dequantize-reduce + requantize; returns (codes, scales, zeros) of
     the output tensors and updates ``out_state`` in place (TACO output)."""
     keep, st_keep, codes, scales, zeros, states = _shard_arrays(shards)
@@ -254,9 +277,9 @@ def reduce_requant(scheme: int, B: int, shards, rows: int, cols: int, row_begin:
     else:
         os_ = np.zeros(E // 128, dtype=np.uint16)
         oz = np.zeros(E // 128, dtype=np.uint16)
-    rc = lib().orc_reduce_requant(scheme, B, len(shards), codes, scales, zeros, states, rows, cols,
-                                  row_begin, row_end, out_scheme, out_B, out_batch, _ptr(out_state), mode,
-                                  _ptr(oc), _ptr(os_), _ptr(oz))
+    rc = lib().orc_reduce_requant_chan(scheme, B, len(shards), codes, scales, zeros, states, rows, cols,
+                                       row_begin, row_end, out_scheme, out_B, out_batch, _ptr(out_state), mode,
+                                       _ptr(oc), _ptr(os_), _ptr(oz), _ptr(_chan(chan, cols)))
     if rc:
         raise ValueError(f"oracle reduce_requant rejected the arguments ({rc})")
     return oc, os_, oz
@@ -382,3 +405,28 @@ def choose_block(x, x_dtype: int, batch: int, rows: int, cols: int, candidates=(
     errs = block_errors(x, x_dtype, batch, rows, cols, candidates)
     best = min(sorted(errs), key=lambda b: errs[b])
     return best, errs
+
+
+# ---------------------------------------------------------------- adaptive rescaling
+def new_chan_state(cols: int) -> np.ndarray:
+    """Per-channel state of the adaptive rescaling: float32 [3 * cols] =
+    down (all 1), up (all 1), amax (all 0)."""
+    c = np.zeros(3 * cols, dtype=np.float32)
+    c[:2 * cols] = 1.0
+    return c
+
+
+def channel_amax(x, dtype: int, batch: int, rows: int, cols: int, chan: np.ndarray) -> None:
+    """Max-accumulate |x| per channel (column) into chan's amax part."""
+    x = np.ascontiguousarray(x)
+    assert x.size == batch * rows * cols
+    rc = lib().orc_channel_amax(_ptr(x), dtype, batch, rows, cols, _ptr(_chan(chan, cols)))
+    if rc:
+        raise ValueError(f"oracle channel_amax rejected the arguments ({rc})")
+
+
+def ash_update(chan: np.ndarray, cols: int) -> None:
+    """Per-channel powers of two from the accumulated amax (median rule), amax reset."""
+    rc = lib().orc_ash_update(_ptr(_chan(chan, cols)), cols)
+    if rc:
+        raise ValueError(f"oracle ash_update rejected the arguments ({rc})")

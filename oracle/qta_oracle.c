@@ -237,13 +237,18 @@ static void taco_quantize_blocks(const float* y, int64_t nblk, int B, float* st,
 }
 
 /* ---- TACO FP8 compress of one tensor ([TACO] Core claim, Fig. 7):
- * the block Hadamard of every block, then the dual-scale quantization. */
-static int taco_compress_tensor(const void* x, int dtype, int64_t off, int64_t E, int B, float* st,
-                                int mode, uint8_t* codes, uint8_t* scales)
+ * the adaptive rescaling (when `down` is given: element i of a row, channel
+ * c = i mod cols, is multiplied by the power of two down[c] in FP32), the
+ * block Hadamard of every block, then the dual-scale quantization. */
+static int taco_compress_tensor(const void* x, int dtype, int64_t off, int64_t E, int64_t cols, int B,
+                                const float* down, float* st, int mode, uint8_t* codes, uint8_t* scales)
 {
     float* y = (float*)malloc(sizeof(float) * (size_t)(E > 0 ? E : 1));
     if (!y) return -2;
-    for (int64_t i = 0; i < E; ++i) y[i] = load_elem(x, dtype, off + i);
+    for (int64_t i = 0; i < E; ++i) {
+        y[i] = load_elem(x, dtype, off + i);
+        if (down) y[i] = y[i] * down[i % cols];
+    }
     orc_fwht_rows(y, E / B, B);
     taco_quantize_blocks(y, E / B, B, st, mode, codes, scales);
     free(y);
@@ -335,15 +340,16 @@ static int check_shape(int scheme, int B, int64_t batch, int64_t rows, int64_t c
     return 0;
 }
 
-int orc_compress(int scheme, int B, const void* x, int in_dtype, int64_t batch,
-                 int64_t rows, int64_t cols, float* state, int mode,
-                 void* codes, void* scales, void* zeros)
+int orc_compress_chan(int scheme, int B, const void* x, int in_dtype, int64_t batch,
+                      int64_t rows, int64_t cols, float* state, int mode,
+                      void* codes, void* scales, void* zeros, const float* chan)
 {
     if (check_shape(scheme, B, batch, rows, cols)) return -1;
+    if (chan && scheme != ORC_TACO_FP8) return -1;
     int64_t E = rows * cols;
     if (scheme == ORC_TACO_FP8) {
         for (int64_t t = 0; t < batch; ++t)
-            if (taco_compress_tensor(x, in_dtype, t * E, E, B, state + 2 * t, mode,
+            if (taco_compress_tensor(x, in_dtype, t * E, E, cols, B, chan, state + 2 * t, mode,
                                      (uint8_t*)codes + t * E, (uint8_t*)scales + t * (E / B)))
                 return -2;
     } else if (scheme == ORC_INT8_SYM) {
@@ -358,6 +364,13 @@ int orc_compress(int scheme, int B, const void* x, int in_dtype, int64_t batch,
                                  (uint16_t*)scales + t * (E / 128), (uint16_t*)zeros + t * (E / 128));
     }
     return 0;
+}
+
+int orc_compress(int scheme, int B, const void* x, int in_dtype, int64_t batch,
+                 int64_t rows, int64_t cols, float* state, int mode,
+                 void* codes, void* scales, void* zeros)
+{
+    return orc_compress_chan(scheme, B, x, in_dtype, batch, rows, cols, state, mode, codes, scales, zeros, 0);
 }
 
 /* The decoded code (exact) and the FP32 dequantization scale of element e
@@ -397,12 +410,16 @@ static float dequant(int scheme, int B, const void* codes, const void* scales,
 }
 
 /* Decompress: dequantize; for TACO apply the inverse Hadamard (the same
- * butterfly, then times 1/B, an exact power of two); round to out dtype. */
-int orc_decompress(int scheme, int B, const void* codes, const void* scales,
-                   const void* zeros, const float* state, int64_t batch,
-                   int64_t rows, int64_t cols, void* y, int out_dtype)
+ * butterfly, then times 1/B, an exact power of two), then, with the
+ * adaptive rescaling, times the channel's power of two up[c] (the inverse of
+ * the compress's down[c]); round to out dtype. */
+int orc_decompress_chan(int scheme, int B, const void* codes, const void* scales,
+                        const void* zeros, const float* state, int64_t batch,
+                        int64_t rows, int64_t cols, void* y, int out_dtype, const float* chan)
 {
     if (check_shape(scheme, B, batch, rows, cols)) return -1;
+    if (chan && scheme != ORC_TACO_FP8) return -1;
+    const float* up = chan ? chan + cols : 0;
     int64_t E = rows * cols;
     float* v = (float*)malloc(sizeof(float) * (size_t)B);
     if (!v) return -2;
@@ -429,12 +446,21 @@ int orc_decompress(int scheme, int B, const void* codes, const void* scales,
             if (scheme == ORC_TACO_FP8) {
                 orc_fwht(v, B);
                 for (int i = 0; i < B; ++i) v[i] = v[i] * (1.0f / (float)B);
+                if (up)
+                    for (int i = 0; i < B; ++i) v[i] = v[i] * up[(b * B + i) % cols];
             }
             for (int i = 0; i < B; ++i) store_elem(y, out_dtype, t * E + b * B + i, v[i]);
         }
     }
     free(v);
     return 0;
+}
+
+int orc_decompress(int scheme, int B, const void* codes, const void* scales,
+                   const void* zeros, const float* state, int64_t batch,
+                   int64_t rows, int64_t cols, void* y, int out_dtype)
+{
+    return orc_decompress_chan(scheme, B, codes, scales, zeros, state, batch, rows, cols, y, out_dtype, 0);
 }
 
 /* Dequantize-reduce ([EQuARX] What carries the argument: each received shard
@@ -475,22 +501,38 @@ static void reduce_sums(int scheme, int B, int n_ranks, const void* const* codes
     }
 }
 
-int orc_reduce(int scheme, int B, int n_ranks, const void* const* codes,
-               const void* const* scales, const void* const* zeros,
-               const float* const* states, int64_t rows, int64_t cols,
-               int64_t row_begin, int64_t row_end, float* sum_out)
+/* With the adaptive rescaling (chan given, the same for every rank: the
+ * ranks' pre-scaled tensors then sum to the pre-scaled sum, whose transform
+ * is the sum of their transforms), the sum is multiplied by up[c] after the
+ * inverse transform, as the decompress does. */
+int orc_reduce_chan(int scheme, int B, int n_ranks, const void* const* codes,
+                    const void* const* scales, const void* const* zeros,
+                    const float* const* states, int64_t rows, int64_t cols,
+                    int64_t row_begin, int64_t row_end, float* sum_out, const float* chan)
 {
     if (check_shape(scheme, B, 1, rows, cols)) return -1;
     if (n_ranks < 1 || row_begin < 0 || row_end < row_begin || row_end > rows) return -1;
+    if (chan && scheme != ORC_TACO_FP8) return -1;
     reduce_sums(scheme, B, n_ranks, codes, scales, zeros, states, cols, row_begin, row_end, sum_out);
     if (scheme == ORC_TACO_FP8) {
         int64_t n = (row_end - row_begin) * cols;
         for (int64_t b0 = 0; b0 < n; b0 += B) {
             orc_fwht(sum_out + b0, B);
             for (int i = 0; i < B; ++i) sum_out[b0 + i] = sum_out[b0 + i] * (1.0f / (float)B);
+            if (chan)
+                for (int i = 0; i < B; ++i) sum_out[b0 + i] = sum_out[b0 + i] * chan[cols + (b0 + i) % cols];
         }
     }
     return 0;
+}
+
+int orc_reduce(int scheme, int B, int n_ranks, const void* const* codes,
+               const void* const* scales, const void* const* zeros,
+               const float* const* states, int64_t rows, int64_t cols,
+               int64_t row_begin, int64_t row_end, float* sum_out)
+{
+    return orc_reduce_chan(scheme, B, n_ranks, codes, scales, zeros, states, rows, cols, row_begin, row_end,
+                           sum_out, 0);
 }
 
 /* Fused dequantize-reduce + requantize of rows [row_begin, row_end) into
@@ -500,14 +542,20 @@ int orc_reduce(int scheme, int B, int n_ranks, const void* const* codes,
  * -- so they are requantized there directly (the inverse and the forward
  * transform, which cancel, are not applied).  Every other pair: qar_reduce
  * then the compress of its FP32 rows. */
-int orc_reduce_requant(int scheme, int B, int n_ranks, const void* const* codes,
-                       const void* const* scales, const void* const* zeros,
-                       const float* const* states, int64_t rows, int64_t cols,
-                       int64_t row_begin, int64_t row_end, int out_scheme, int out_B,
-                       int64_t out_batch, float* out_state, int mode, void* out_codes,
-                       void* out_scales, void* out_zeros)
+/* chan (adaptive rescaling, TACO -> TACO only): the shards' and the
+ * output's channel factors, one set.  Equal blocks: the Hadamard-domain
+ * sums are the transform of the pre-scaled reduced rows and are requantized
+ * as they are; otherwise the reduce (times up[c]) then the compress (times
+ * down[c]). */
+int orc_reduce_requant_chan(int scheme, int B, int n_ranks, const void* const* codes,
+                            const void* const* scales, const void* const* zeros,
+                            const float* const* states, int64_t rows, int64_t cols,
+                            int64_t row_begin, int64_t row_end, int out_scheme, int out_B,
+                            int64_t out_batch, float* out_state, int mode, void* out_codes,
+                            void* out_scales, void* out_zeros, const float* chan)
 {
     if (check_shape(scheme, B, 1, rows, cols)) return -1;
+    if (chan && (scheme != ORC_TACO_FP8 || out_scheme != ORC_TACO_FP8)) return -1;
     if (n_ranks < 1 || row_begin < 0 || row_end < row_begin || row_end > rows) return -1;
     int64_t nrows = row_end - row_begin;
     if (out_batch < 1 || nrows % out_batch) return -1;
@@ -522,14 +570,26 @@ int orc_reduce_requant(int scheme, int B, int n_ranks, const void* const* codes,
             taco_quantize_blocks(acc + t * Et, Et / B, B, out_state + 2 * t, mode,
                                  (uint8_t*)out_codes + t * Et, (uint8_t*)out_scales + t * (Et / B));
     } else {
-        rc = orc_reduce(scheme, B, n_ranks, codes, scales, zeros, states, rows, cols, row_begin,
-                        row_end, acc);
+        rc = orc_reduce_chan(scheme, B, n_ranks, codes, scales, zeros, states, rows, cols, row_begin,
+                             row_end, acc, chan);
         if (!rc)
-            rc = orc_compress(out_scheme, out_B, acc, ORC_FP32, out_batch, nrows / out_batch, cols,
-                              out_state, mode, out_codes, out_scales, out_zeros);
+            rc = orc_compress_chan(out_scheme, out_B, acc, ORC_FP32, out_batch, nrows / out_batch, cols,
+                                   out_state, mode, out_codes, out_scales, out_zeros, chan);
     }
     free(acc);
     return rc;
+}
+
+int orc_reduce_requant(int scheme, int B, int n_ranks, const void* const* codes,
+                       const void* const* scales, const void* const* zeros,
+                       const float* const* states, int64_t rows, int64_t cols,
+                       int64_t row_begin, int64_t row_end, int out_scheme, int out_B,
+                       int64_t out_batch, float* out_state, int mode, void* out_codes,
+                       void* out_scales, void* out_zeros)
+{
+    return orc_reduce_requant_chan(scheme, B, n_ranks, codes, scales, zeros, states, rows, cols, row_begin,
+                                   row_end, out_scheme, out_B, out_batch, out_state, mode, out_codes,
+                                   out_scales, out_zeros, 0);
 }
 
 /* One hop of a ring reduce-scatter [EQuARX] What carries the argument (each
@@ -547,5 +607,78 @@ int orc_dequant_add(int scheme, int B, const void* codes, const void* scales, co
     if (rc) return rc;
     int64_t n = batch * rows * cols;
     for (int64_t e = 0; e < n; ++e) sum_out[e] = sum_out[e] + load_elem(x, x_dtype, e);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * Adaptive rescaling of the Adaptive Scale-Hadamard transform ([TACO] Core
+ * claim: data-driven reshaping together with an Adaptive Scale-Hadamard
+ * transform; Fig. 7: tensors are compressed via adaptive rescaling, the ASH
+ * transform and dual-scale quantization).  The pages give no rule.
+ * Reading: every hidden channel c gets a power of two down[c] = 2^-e[c]
+ * that multiplies the channel before the block Hadamard (and up[c] = 2^e[c]
+ * after the inverse), shared by all ranks of a reduction, so that channels
+ * far above the typical channel range no longer dominate the Hadamard
+ * blocks they fall in.  The exponents come from the per-channel amax of
+ * earlier data (caller-owned state, like the per-tensor scale):
+ *   E(v)  = floor(log2 v) for a normal v > 0 (its binary exponent), -127 for
+ *           a subnormal v;
+ *   E_ref = the lower median of E(amax[c]) over the channels with amax > 0;
+ *   e[c]  = min(3, max(0, E(amax[c]) - E_ref - 2)), 0 when amax[c] == 0:
+ *           channels less than a factor 8 above the typical range keep
+ *           factor 1; larger ones are divided by up to 8, which leaves
+ *           them at about four times the typical range.  (On the outlier-
+ *           channel workloads this rule lowered the round-trip error most
+ *           robustly among the thresholds and caps tried; a larger cap
+ *           amplifies the error of rare extreme channels.)
+ * chan = float[3 * cols]: down[cols], up[cols], amax[cols].
+ * ---------------------------------------------------------------------- */
+int orc_channel_amax(const void* x, int dtype, int64_t batch, int64_t rows, int64_t cols, float* chan)
+{
+    if (batch < 0 || rows < 0 || cols <= 0) return -1;
+    float* amax = chan + 2 * cols;
+    for (int64_t r = 0; r < batch * rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) amax[c] = fmaxf(amax[c], fabsf(load_elem(x, dtype, r * cols + c)));
+    return 0;
+}
+
+static int binary_exponent(float v)
+{
+    uint32_t u = f2u(v) & 0x7fffffffu;
+    int ef = (int)(u >> 23);
+    return ef == 0 ? -127 : ef - 127;
+}
+
+static int cmp_int(const void* a, const void* b)
+{
+    int x = *(const int*)a, y = *(const int*)b;
+    return (x > y) - (x < y);
+}
+
+int orc_ash_update(float* chan, int64_t cols)
+{
+    if (cols <= 0) return -1;
+    float* down = chan;
+    float* up = chan + cols;
+    float* amax = chan + 2 * cols;
+    int* ex = (int*)malloc(sizeof(int) * (size_t)cols);
+    if (!ex) return -2;
+    int64_t n = 0;
+    for (int64_t c = 0; c < cols; ++c)
+        if (amax[c] > 0.0f) ex[n++] = binary_exponent(amax[c]);
+    qsort(ex, (size_t)n, sizeof(int), cmp_int);
+    int e_ref = n > 0 ? ex[(n - 1) / 2] : 0;
+    free(ex);
+    for (int64_t c = 0; c < cols; ++c) {
+        int e = 0;
+        if (amax[c] > 0.0f) {
+            e = binary_exponent(amax[c]) - e_ref - 2;
+            if (e < 0) e = 0;
+            if (e > 3) e = 3;
+        }
+        down[c] = ldexpf(1.0f, -e);
+        up[c] = ldexpf(1.0f, e);
+        amax[c] = 0.0f;
+    }
     return 0;
 }

@@ -88,6 +88,27 @@ int orc_dequant_add(int scheme, int B, const void* codes, const void* scales, co
                     const float* state, int64_t batch, int64_t rows, int64_t cols, const void* x,
                     int x_dtype, float* sum_out);
 
+/* ---- adaptive rescaling (per-channel powers of two); chan = float[3*cols]:
+ *      down[cols], up[cols], amax[cols] ---- */
+int orc_channel_amax(const void* x, int dtype, int64_t batch, int64_t rows, int64_t cols, float* chan);
+int orc_ash_update(float* chan, int64_t cols);
+int orc_compress_chan(int scheme, int B, const void* x, int in_dtype, int64_t batch,
+                      int64_t rows, int64_t cols, float* state, int mode,
+                      void* codes, void* scales, void* zeros, const float* chan);
+int orc_decompress_chan(int scheme, int B, const void* codes, const void* scales,
+                        const void* zeros, const float* state, int64_t batch,
+                        int64_t rows, int64_t cols, void* y, int out_dtype, const float* chan);
+int orc_reduce_chan(int scheme, int B, int n_ranks, const void* const* codes,
+                    const void* const* scales, const void* const* zeros,
+                    const float* const* states, int64_t rows, int64_t cols,
+                    int64_t row_begin, int64_t row_end, float* sum_out, const float* chan);
+int orc_reduce_requant_chan(int scheme, int B, int n_ranks, const void* const* codes,
+                            const void* const* scales, const void* const* zeros,
+                            const float* const* states, int64_t rows, int64_t cols,
+                            int64_t row_begin, int64_t row_end, int out_scheme, int out_B,
+                            int64_t out_batch, float* out_state, int mode, void* out_codes,
+                            void* out_scales, void* out_zeros, const float* chan);
+
 #ifdef __cplusplus
 }
 #endif

@@ -43,7 +43,7 @@ class Desc(ctypes.Structure):
 
 class QTensorC(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("zeros", ctypes.c_void_p),
-                ("state", ctypes.c_void_p)]
+                ("state", ctypes.c_void_p), ("chan", ctypes.c_void_p)]
 
 
 _lib = None
@@ -82,10 +82,14 @@ def lib():
         L.qta_wait_self_test.argtypes = [i32, vp]
         L.taco_update_scale.argtypes = [vp, i64, vp]
         L.qta_copy.argtypes = [vp, vp, sz, vp]
+        L.qta_chan_bytes.argtypes = [i64]
+        L.qta_chan_bytes.restype = sz
+        L.taco_channel_amax.argtypes = [PD, vp, i32, vp, vp]
+        L.taco_ash_update.argtypes = [vp, i64, vp]
         L.qta_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
         for name in ("taco_compress", "taco_decompress", "qar_reduce", "qar_requant", "qar_reduce_requant",
                      "qar_dequant_add", "qar_dequant_add_requant", "qta_sq_error", "qta_wait_self_test",
-                     "taco_update_scale", "qta_copy",
+                     "taco_update_scale", "qta_copy", "taco_channel_amax", "taco_ash_update",
                      "qta_device_error"):
             getattr(L, name).restype = ctypes.c_int
         L.qta_status_string.argtypes = [ctypes.c_int]
@@ -132,15 +136,19 @@ def desc(scheme, block: int, rows: int, cols: int, batch: int = 1, max_sms: int 
 
 @dataclass
 class QTensor:
-    """Device buffers of one quantized tensor (torch uint8/float32 tensors)."""
+    """Device buffers of one quantized tensor (torch uint8/float32 tensors).
+    chan: the adaptive rescaling state (float32 [3 * cols], see alloc_chan)
+    or None."""
     desc: Desc
     codes: object
     scales: object
     zeros: object = None
     state: object = None
+    chan: object = None
 
     def c(self) -> QTensorC:
-        return QTensorC(_ptr(self.codes), _ptr(self.scales), _ptr(self.zeros), _ptr(self.state))
+        return QTensorC(_ptr(self.codes), _ptr(self.scales), _ptr(self.zeros), _ptr(self.state),
+                        _ptr(self.chan))
 
     def shard(self, i: int) -> "QTensor":
         """View of tensor i of a batch as a batch-1 quantized tensor."""
@@ -150,7 +158,7 @@ class QTensor:
         cb, sb, zb = codes_bytes(sub), scales_bytes(sub), zeros_bytes(sub)
         return QTensor(sub, self.codes[i * cb:(i + 1) * cb], self.scales[i * sb:(i + 1) * sb],
                        None if self.zeros is None else self.zeros[i * zb:(i + 1) * zb],
-                       None if self.state is None else self.state[2 * i:2 * i + 2])
+                       None if self.state is None else self.state[2 * i:2 * i + 2], self.chan)
 
 
 def codes_bytes(d: Desc) -> int:
@@ -257,3 +265,23 @@ def qta_device_error(clear: bool = True) -> int:
     flags = ctypes.c_uint32(0)
     _check("qta_device_error", lib().qta_device_error(ctypes.byref(flags), 1 if clear else 0))
     return flags.value
+
+
+# ---------------------------------------------------------------- adaptive rescaling
+def alloc_chan(cols: int, device="cuda"):
+    """Adaptive rescaling state of `cols` channels: float32 [3 * cols] =
+    down (1), up (1), amax (0), i.e. no rescaling until taco_ash_update."""
+    import torch
+    n = lib().qta_chan_bytes(int(cols)) // 4
+    c = torch.zeros(n, dtype=torch.float32, device=device)
+    c[:2 * cols] = 1.0
+    return c
+
+
+def taco_channel_amax(d: Desc, x, x_dtype: int, chan, stream=None) -> None:
+    _check("taco_channel_amax", lib().taco_channel_amax(ctypes.byref(d), _ptr(x), x_dtype, _ptr(chan),
+                                                        _stream(stream)))
+
+
+def taco_ash_update(chan, cols: int, stream=None) -> None:
+    _check("taco_ash_update", lib().taco_ash_update(_ptr(chan), cols, _stream(stream)))

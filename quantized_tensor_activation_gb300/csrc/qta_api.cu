@@ -185,6 +185,10 @@ qta_status check_qtensor(const qta_desc* d, const qta_qtensor* q)
         if (!q->state) return QTA_ERR_INVALID_ARG;
         if (!aligned(q->state, 4)) return QTA_ERR_ALIGNMENT;
     }
+    if (q->chan) {   // the adaptive rescaling goes with the Hadamard scheme only
+        if (d->scheme != QTA_TACO_FP8) return QTA_ERR_UNSUPPORTED;
+        if (!aligned(q->chan, 16)) return QTA_ERR_ALIGNMENT;
+    }
     return QTA_OK;
 }
 
@@ -247,6 +251,117 @@ __global__ void __launch_bounds__(512) copy_kernel(const uint4* __restrict__ src
         __stcs(dst + i + 3 * stride, d);
     }
     for (; i < n16; i += stride) __stcs(dst + i, __ldcs(src + i));
+}
+
+// Per-channel amax of the adaptive rescaling: thread t of grid column block
+// owns one 16-byte vector of columns (8 16-bit or 4 fp32 values) and walks
+// the rows of its row chunk, then max-accumulates into amax[] (non-negative
+// floats order like their bit patterns, so max is an unsigned atomicMax).
+template <int KIND>
+__global__ void __launch_bounds__(256) channel_amax_kernel(const uint8_t* __restrict__ x, long long n_rows,
+                                                           long long cols, long long rows_per_chunk,
+                                                           float* __restrict__ amax)
+{
+    pdl_wait();
+    pdl_trigger();
+    constexpr int PER = (KIND == IN_FP32) ? 4 : 8;
+    constexpr int ES = (KIND == IN_FP32) ? 4 : 2;
+    const long long cv = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    if (cv * PER >= cols) return;
+    const long long r0 = blockIdx.y * rows_per_chunk;
+    const long long r1 = (r0 + rows_per_chunk < n_rows) ? r0 + rows_per_chunk : n_rows;
+    float m[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) m[i] = 0.0f;
+    for (long long r = r0; r < r1; ++r) {
+        const uint4 w = __ldcs(reinterpret_cast<const uint4*>(x + (r * cols + cv * PER) * ES));
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if constexpr (KIND == IN_FP32) {
+                m[k] = fmaxf(m[k], fabsf(__uint_as_float(ws[k])));
+            } else {
+                const float2 f = up2((KIND == IN_BF16) ? bf16x2_to_pair(ws[k]) : f16x2_to_pair(ws[k]));
+                m[2 * k] = fmaxf(m[2 * k], fabsf(f.x));
+                m[2 * k + 1] = fmaxf(m[2 * k + 1], fabsf(f.y));
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+        if (m[i] > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(amax + cv * PER + i), __float_as_uint(m[i]));
+}
+
+// Update of the adaptive rescaling (one CTA): E(v) = exponent field of v
+// minus 127 (-127 for subnormals); E_ref = the lower median of E over the
+// channels with amax > 0, found from a histogram of the 255 exponent values;
+// e = min(3, max(0, E - E_ref - 2)); down = 2^-e, up = 2^e, amax = 0.
+__global__ void __launch_bounds__(1024) ash_update_kernel(float* __restrict__ chan, long long cols)
+{
+    pdl_wait();
+    pdl_trigger();
+    __shared__ unsigned int hist[256];
+    __shared__ int e_ref;
+    float* amax = chan + 2 * cols;
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0u;
+    __syncthreads();
+    for (long long c = threadIdx.x; c < cols; c += blockDim.x) {
+        const float v = amax[c];
+        if (v > 0.0f) atomicAdd(&hist[__float_as_uint(v) >> 23], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned int n = 0;
+        for (int i = 0; i < 256; ++i) n += hist[i];
+        int ref = 0;
+        if (n > 0) {
+            const unsigned int k = (n - 1) / 2;   // index of the lower median in sorted order
+            unsigned int cum = 0;
+            for (int i = 0; i < 256; ++i) {
+                cum += hist[i];
+                if (cum > k) {
+                    ref = i - 127;
+                    break;
+                }
+            }
+        }
+        e_ref = ref;
+    }
+    __syncthreads();
+    const int ref = e_ref;
+    for (long long c = threadIdx.x; c < cols; c += blockDim.x) {
+        const float v = amax[c];
+        int e = 0;
+        if (v > 0.0f) {
+            e = static_cast<int>(__float_as_uint(v) >> 23) - 127 - ref - 2;
+            e = e < 0 ? 0 : (e > 3 ? 3 : e);
+        }
+        chan[c] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+        chan[cols + c] = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+        amax[c] = 0.0f;
+    }
+}
+
+cudaError_t launch_channel_amax(const void* x, int kind, long long n_rows, long long cols, float* amax,
+                                cudaStream_t stream)
+{
+    const int per = kind == IN_FP32 ? 4 : 8;
+    const long long ncv = cols / per;
+    long long rpc = (n_rows + 65534) / 65535;   // grid.y stays within its limit
+    if (rpc < 64) rpc = 64;
+    const dim3 grid(static_cast<unsigned>((ncv + 255) / 256), static_cast<unsigned>((n_rows + rpc - 1) / rpc));
+    const uint8_t* xb = static_cast<const uint8_t*>(x);
+    switch (kind) {
+    case IN_BF16: return launch_pdl(channel_amax_kernel<IN_BF16>, grid, dim3(256), 0, stream, xb, n_rows, cols, rpc, amax);
+    case IN_FP16: return launch_pdl(channel_amax_kernel<IN_FP16>, grid, dim3(256), 0, stream, xb, n_rows, cols, rpc, amax);
+    case IN_FP32: return launch_pdl(channel_amax_kernel<IN_FP32>, grid, dim3(256), 0, stream, xb, n_rows, cols, rpc, amax);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_ash_update(float* chan, long long cols, cudaStream_t stream)
+{
+    return launch_pdl(ash_update_kernel, dim3(1), dim3(1024), 0, stream, chan, cols);
 }
 
 // Self-test of the bounded pipeline wait: one warp waits on an mbarrier
@@ -350,6 +465,8 @@ static qta_status compress_impl(const qta_desc* d, const void* x, int32_t x_dtyp
     p.lanes_log2 = log2i(p.lanes_per_block);
     p.seg_per_tensor = make_fastdiv(static_cast<uint32_t>(d->rows * d->cols / 64));
     p.round_up = (mode & QTA_SCALE_ROUND_UP) ? 1 : 0;
+    p.chan = out->chan;
+    p.seg_per_row = make_fastdiv(static_cast<uint32_t>(d->cols / 64));
     const int sch = d->scheme;  // qta_scheme values equal the kernel scheme kinds
     const int grid =
         grid_for(p.n_warp_tiles, compress_warps(x_dtype), compress_smem(x_dtype, sch), sms, smem_sm, d->max_sms);
@@ -404,6 +521,8 @@ qta_status taco_decompress(const qta_desc* d, const qta_qtensor* in, void* y, in
     p.lanes_log2 = log2i(p.lanes_per_block);
     p.inv_block = 1.0f / static_cast<float>(d->block);
     p.seg_per_tensor = make_fastdiv(static_cast<uint32_t>(d->rows * d->cols / 64));
+    p.chan_up = in->chan ? in->chan + d->cols : nullptr;
+    p.seg_per_row = make_fastdiv(static_cast<uint32_t>(d->cols / 64));
     const int grid = grid_for(p.n_warp_tiles, decompress_warps(y_dtype), decompress_smem(d->scheme, y_dtype), sms,
                               smem_sm, d->max_sms);
     return cuda_status(launch_decompress(d->scheme, y_dtype, p, grid, reinterpret_cast<cudaStream_t>(stream)));
@@ -422,8 +541,12 @@ static qta_status reduce_params(const qta_desc* d, const qta_qtensor* shards, in
     if (!shards) return QTA_ERR_INVALID_ARG;
     *empty = (row_end == row_begin || d->cols == 0);
     if (*empty) return QTA_OK;
-    for (int r = 0; r < n_ranks; ++r)
+    for (int r = 0; r < n_ranks; ++r) {
         if ((st = check_qtensor(d, &shards[r])) != QTA_OK) return st;
+        // one set of channel factors for every rank (the transform of the sum
+        // is then the sum of the transforms)
+        if (shards[r].chan != shards[0].chan) return QTA_ERR_INVALID_ARG;
+    }
     return QTA_OK;
 }
 
@@ -451,6 +574,8 @@ static qta_status reduce_fill(const qta_desc* d, const qta_qtensor* shards, int3
     p->lanes_per_block = lanes_of(d);
     p->lanes_log2 = log2i(p->lanes_per_block);
     p->inv_block = 1.0f / static_cast<float>(d->block);
+    p->chan_up = shards[0].chan ? shards[0].chan + d->cols : nullptr;
+    p->seg_per_row = make_fastdiv(static_cast<uint32_t>(d->cols / 64));
     return QTA_OK;
 }
 
@@ -471,7 +596,11 @@ qta_status qar_reduce_requant(const qta_desc* d, const qta_qtensor* shards, int3
     if (!reduce_requant_supported(d->scheme, od->scheme)) return QTA_ERR_UNSUPPORTED;
     if (empty) return QTA_OK;
     if ((st = check_qtensor(od, out)) != QTA_OK) return st;
+    // the requantized sum keeps the shards' channel factors: with one set on
+    // both sides the rescaling cancels between the reduce and the requant
+    if (out->chan != shards[0].chan) return QTA_ERR_UNSUPPORTED;
     if ((st = reduce_fill(d, shards, n_ranks, row_begin, row_end, &p, &sms, &smem_sm)) != QTA_OK) return st;
+    p.chan_up = nullptr;
     if (!map_codes(&p.out_map, od->scheme, out->codes, static_cast<uint64_t>(p.M_out))) return QTA_ERR_CUDA;
     p.q_scales = out->scales;
     p.q_zeros = out->zeros;
@@ -526,6 +655,7 @@ static qta_status accum_impl(const qta_desc* d, const qta_qtensor* in, const voi
     if (!aligned(x, 16) || (!requant && !aligned(sum_out, 16))) return QTA_ERR_ALIGNMENT;
     if ((st = check_qtensor(d, in)) != QTA_OK) return st;
     if (requant && (st = check_qtensor(d, out)) != QTA_OK) return st;
+    if (in->chan || (requant && out->chan)) return QTA_ERR_UNSUPPORTED;   // ring hops: no rescaling
     {   // the output may not overlap an input: the kernel reads and writes in one pass
         const size_t n = static_cast<size_t>(n_elems(d));
         const void* ins[5] = {x, in->codes, in->scales, in->zeros, in->state};
@@ -599,6 +729,30 @@ qta_status qar_dequant_add_requant(const qta_desc* d, const qta_qtensor* in, con
 {
     if (!out) return QTA_ERR_INVALID_ARG;
     return accum_impl(d, in, x, x_dtype, nullptr, out, mode, stream);
+}
+
+size_t qta_chan_bytes(int64_t cols) { return cols > 0 ? static_cast<size_t>(cols) * 3 * sizeof(float) : 0; }
+
+qta_status taco_channel_amax(const qta_desc* d, const void* x, int32_t x_dtype, float* chan, qta_stream_t stream)
+{
+    qta_status st = check_desc(d);
+    if (st != QTA_OK) return st;
+    if (x_dtype != QTA_BF16 && x_dtype != QTA_FP16 && x_dtype != QTA_FP32) return QTA_ERR_UNSUPPORTED;
+    if (n_elems(d) == 0) return QTA_OK;
+    if (!x || !chan) return QTA_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(chan, 16)) return QTA_ERR_ALIGNMENT;
+    if (overlaps(x, static_cast<size_t>(n_elems(d)) * dtype_bytes(x_dtype), chan, qta_chan_bytes(d->cols)))
+        return QTA_ERR_INVALID_ARG;
+    return cuda_status(launch_channel_amax(x, x_dtype, d->batch * d->rows, d->cols, chan + 2 * d->cols,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+qta_status taco_ash_update(float* chan, int64_t cols, qta_stream_t stream)
+{
+    if (cols <= 0) return cols == 0 ? QTA_OK : QTA_ERR_INVALID_ARG;
+    if (!chan) return QTA_ERR_INVALID_ARG;
+    if (!aligned(chan, 16)) return QTA_ERR_ALIGNMENT;
+    return cuda_status(launch_ash_update(chan, cols, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 qta_status qta_sq_error(const void* a, int32_t a_dtype, const float* b, int64_t n, double* out,

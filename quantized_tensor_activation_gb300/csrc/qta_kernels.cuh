@@ -41,6 +41,8 @@ struct CompressParams {
     int lanes_log2;
     FastDiv seg_per_tensor;
     int round_up;         // TACO: block scales rounded up (QTA_SCALE_ROUND_UP)
+    const float* chan;    // TACO adaptive rescaling: per-channel factors down[cols] (NULL: none)
+    FastDiv seg_per_row;  // cols / 64
 };
 
 struct DecompressParams {
@@ -56,6 +58,8 @@ struct DecompressParams {
     int lanes_log2;
     float inv_block;      // 1/B (TACO)
     FastDiv seg_per_tensor;
+    const float* chan_up; // TACO adaptive rescaling: per-channel factors up[cols] (NULL: none)
+    FastDiv seg_per_row;  // cols / 64
 };
 
 struct ReduceParams {
@@ -80,6 +84,8 @@ struct ReduceParams {
     int q_lanes_log2;
     FastDiv q_seg_per_tensor;
     int q_round_up;
+    const float* chan_up; // TACO FP32 sum: per-channel factors up[cols] (NULL: none)
+    FastDiv seg_per_row;  // cols / 64
 };
 
 // One ring hop: the incoming quantized partial sum plus the local tensor x,
@@ -386,6 +392,54 @@ __device__ __forceinline__ void store_out16or32(const CUtensorMap* map, const ui
         tma_store_3d(map, 0, 1, row, ob + 4096);
     } else {
         tma_store_2d(map, 0, row, ob);
+    }
+}
+
+// ------------------------------------------------------------ 1/B folded into the scale
+// The inverse transform ends with a multiply by 1/B (a power of two).  When
+// every per-tensor scale S of the values involved is at least 2^-71, every
+// block scale s_b = S r_b with r_b >= 2^-9 is at least 2^-80 and every
+// nonzero value the butterfly forms is a multiple of 2^-23 s_b 2^-9 >= 2^-112;
+// scaled by 1/B >= 2^-8 it stays a normal float.  In that range multiplying
+// by a power of two commutes with every rounding, so s_b / B in place of s_b,
+// and no multiply at the end, gives the same bits.
+constexpr float FOLD_MIN_S = 0x1p-71f;
+
+// ------------------------------------------------------------ adaptive rescaling
+// Column of the first element of segment g (cols = 64 * spr.d per row).
+__device__ __forceinline__ int seg_col0(int g, const FastDiv& spr)
+{
+    const uint32_t u = static_cast<uint32_t>(g);
+    return static_cast<int>(u - fdiv(u, spr) * spr.d) * SEG;
+}
+
+// Multiply a lane's segment, loaded into the permuted slots of xl_mask
+// (slot j holds position j ^ xm), by the per-channel factors f[col0 + position]
+// (powers of two, so every product is exact barring underflow).  The products
+// are consumed by scalar adds or multiplies only.
+__device__ __forceinline__ void scale_slots(u64 (&v)[32], const float* __restrict__ f, int col0, uint32_t xm)
+{
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        const float4 c = __ldg(reinterpret_cast<const float4*>(f + col0 + ((4u * q) ^ xm)));
+        v[2 * q] = mul2(v[2 * q], pk2(c.x, c.y));
+        v[2 * q + 1] = mul2(v[2 * q + 1], pk2(c.z, c.w));
+    }
+}
+
+// The same for values in the layout fwht_cross_xl leaves: pair j holds row
+// group g = j >> (5 - lg) of the block (segment base + xl_group_row(g)) at
+// positions xm + 2 (j mod 2^(5-lg)); colb is the column of the block's first
+// element.
+__device__ __forceinline__ void scale_xl(u64 (&v)[32], const float* __restrict__ f, int colb, int lg, uint32_t xm)
+{
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        const int g = j >> (5 - lg);
+        const int pos = static_cast<int>(xm) + 2 * (j & ((1 << (5 - lg)) - 1));
+        const float4 c = __ldg(reinterpret_cast<const float4*>(f + colb + SEG * xl_group_row(g, lg) + pos));
+        v[j] = mul2(v[j], pk2(c.x, c.y));
+        v[j + 1] = mul2(v[j + 1], pk2(c.z, c.w));
     }
 }
 
@@ -758,6 +812,9 @@ compress_kernel(const __grid_constant__ CompressParams p)
             stage = 0;
             phase ^= 1u;
         }
+        // adaptive rescaling: the channel factors before the transform
+        if constexpr (SCH == S_TACO)
+            if (p.chan) scale_slots(v, p.chan, seg_col0(wt * 32 + lane, p.seg_per_row), xm);
         uint32_t ow[16];
         quant.template run<AMAX_ONLY, XL>(v, qo, wt * 32, lane, ow, false, xm);
         if constexpr (!AMAX_ONLY)
@@ -868,6 +925,12 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
         }
         float s, z;
         cur.decode(s, z);
+        // TACO: 1/B folded into the block scale when every lane's S allows it
+        bool fold = false;
+        if constexpr (SCH == S_TACO) {
+            fold = __all_sync(0xffffffffu, cur.S >= FOLD_MIN_S);
+            if (fold) s = __fmul_rn(s, p.inv_block);
+        }
         u64 v[32];
         dequant_segment<SCH, 0>(wb + stage * C::IN_BYTES, lane, s, z, v, static_cast<uint16_t>(cur.raw), xm);
         __syncwarp();
@@ -886,9 +949,13 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
         if constexpr (SCH == S_TACO) {
             fwht64_local_xl(v, xm);
             fwht_cross_xl(v, L, lane);
-            const u64 ib = pk2(p.inv_block, p.inv_block);
+            if (!fold) {
+                const u64 ib = pk2(p.inv_block, p.inv_block);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = mul2(v[j], ib);
+                for (int j = 0; j < 32; ++j) v[j] = mul2(v[j], ib);
+            }
+            if (p.chan_up)
+                scale_xl(v, p.chan_up, seg_col0(wt * 32 + (lane & ~(L - 1)), p.seg_per_row), lg, xm);
         }
         uint8_t* ob = outb + (k % C::OUT_BUFS) * C::OUT_BYTES;
         if (lane == 0) {
@@ -1016,6 +1083,12 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
         if (threadIdx.x < p.n_ranks) sS[threadIdx.x] = __ldg(p.state[threadIdx.x]);
         __syncthreads();
     }
+    // TACO FP32 sum: 1/B folded into the shards' block scales (FOLD_MIN_S)
+    bool fold = false;
+    if constexpr (SCH == S_TACO && OSCH == OUT_F32) {
+        fold = true;
+        for (int r = 0; r < n; ++r) fold = fold && (sS[r] >= FOLD_MIN_S);
+    }
     if (lane == 0) {
         for (int u = 0; u < C::STAGES && u < total_units; ++u) {
             reduce_issue<SCH, OSCH>(p, wb, bars, u, next_unit, first, W);
@@ -1068,6 +1141,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                 float s, z;
                 if constexpr (SCH == S_TACO) {
                     s = __fmul_rn(sS[r], e4m3_decode(cur[kk].raw));
+                    if (fold) s = __fmul_rn(s, p.inv_block);
                     z = 0.0f;
                 } else {
                     cur[kk].decode(s, z);
@@ -1107,9 +1181,16 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                 fwht_cross(acc, L, lane);
             }
             if constexpr (OSCH == OUT_F32) {
-                const u64 ib = pk2(p.inv_block, p.inv_block);
+                if (!fold) {
+                    const u64 ib = pk2(p.inv_block, p.inv_block);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) acc[j] = mul2(acc[j], ib);
+                    for (int j = 0; j < 32; ++j) acc[j] = mul2(acc[j], ib);
+                }
+                if constexpr (XL)
+                    if (p.chan_up)
+                        scale_xl(acc, p.chan_up,
+                                 seg_col0(p.seg_begin + wt * 32 + (lane & ~(L - 1)), p.seg_per_row),
+                                 (LG >= 0) ? LG : p.lanes_log2, xm);
             } else {
                 // scalar rounded multiplies: the requantizer's butterfly adds
                 // follow, and a packed multiply would be contracted into them
@@ -1309,5 +1390,8 @@ enum StateOp : int { STATE_UPDATE = 0, STATE_RESET_AMAX = 1, STATE_SET_SCALE = 2
 
 __global__ void state_kernel(float* state, long long n, int op);
 __global__ void copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, long long n16);
+cudaError_t launch_channel_amax(const void* x, int kind, long long n_rows, long long cols, float* amax,
+                                cudaStream_t stream);
+cudaError_t launch_ash_update(float* chan, long long cols, cudaStream_t stream);
 
 }  // namespace qta

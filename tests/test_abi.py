@@ -196,3 +196,29 @@ def test_ring_rejects_fewer_than_two_ranks():
     with pytest.raises(ValueError):
         ring._chunk_desc(qta.desc("taco_fp8", 128, 4, 256), 1)
     assert ring._chunk_desc(qta.desc("taco_fp8", 128, 4, 256), 2).rows == 2
+
+
+def test_rescaling_argument_checks(L):
+    OK, INV, ALN, UNS = qta.QTA_OK, qta.QTA_ERR_INVALID_ARG, qta.QTA_ERR_ALIGNMENT, qta.QTA_ERR_UNSUPPORTED
+    assert L.qta_chan_bytes(256) == 3 * 256 * 4 and L.qta_chan_bytes(0) == 0 and L.qta_chan_bytes(-5) == 0
+    d = ctypes.byref(qta.desc(0, 128, 4, 256))
+    f = L.taco_channel_amax
+    assert f(d, 0x100000, 7, 0x200000, None) == UNS                    # dtype
+    assert f(d, None, 0, 0x200000, None) == INV
+    assert f(d, 0x100000, 0, None, None) == INV
+    assert f(d, 0x100008, 0, 0x200000, None) == ALN
+    assert f(d, 0x100000, 0, 0x200004, None) == ALN
+    assert f(d, 0x100000, 0, 0x100000 + 1024, None) == INV             # chan inside x
+    assert f(ctypes.byref(qta.desc(0, 128, 0, 256)), None, 0, None, None) == OK   # empty
+    g = L.taco_ash_update
+    assert g(None, 0, None) == OK and g(None, -1, None) == INV and g(None, 4, None) == INV
+    assert g(0x200004, 4, None) == ALN
+    # the factors go with TACO only, 16-byte aligned (checked before anything runs)
+    q = ctypes.byref(qta.QTensorC(0x100000, 0x200000, 0x300000, 0x400000, 0x500000))
+    assert L.taco_compress(ctypes.byref(qta.desc(1, 64, 4, 256)), 0x600000, 0, q, 0, None) == UNS
+    qm = ctypes.byref(qta.QTensorC(0x100000, 0x200000, 0x300000, 0x400000, 0x500008))
+    assert L.taco_compress(d, 0x600000, 0, qm, 0, None) == ALN
+    # the ring hops take no rescaling
+    out = ctypes.byref(qta.QTensorC(0x700000, 0x800000, 0x900000, 0xA00000, None))
+    assert L.qar_dequant_add_requant(d, q, 0x600000, 0, out, 0, None) == UNS
+    assert L.qar_dequant_add(d, q, 0x600000, 0, 0xB00000, None) == UNS

@@ -92,3 +92,41 @@ def test_every_call_writes_only_its_outputs(scheme, B, gscheme, gB):
         qta.taco_update_scale(q.state, n)
     g.check()
     assert qta.qta_device_error() == 0
+
+
+def test_rescaling_calls_write_only_their_outputs():
+    # the channel amax writes only the amax part of the state; the update
+    # writes the state; the codec calls with the factors write their outputs
+    dev = device()
+    g = Guarded(dev)
+    n, rows, cols = 3, 14, 768
+    rng = np.random.default_rng(5)
+    x = to_dtype_cpu(random_values(rng, (n, rows, cols), "mixed"), qta.BF16).to(dev)
+    raw = torch.full((3 * cols * 4 + 2 * PAD,), CANARY, dtype=torch.uint8, device=dev)
+    chan = raw[PAD:PAD + 3 * cols * 4].view(torch.float32)
+    chan[:2 * cols] = 1.0
+    chan[2 * cols:] = 0.0
+    fill = raw[PAD:PAD + 2 * cols * 4].clone()
+    d_in = qta.desc("taco_fp8", 128, rows, cols, batch=n)
+    qta.taco_channel_amax(d_in, x, qta.BF16, chan)
+    torch.cuda.synchronize()
+    assert torch.equal(raw[PAD:PAD + 2 * cols * 4], fill)           # down and up untouched
+    qta.taco_ash_update(chan, cols)
+    torch.cuda.synchronize()
+    assert bool((raw[:PAD] == CANARY).all()) and bool((raw[PAD + 3 * cols * 4:] == CANARY).all())
+    q = g.qtensor(d_in)
+    q.chan = chan
+    qta.taco_compress(d_in, x, qta.BF16, q, qta.SCALE_CURRENT)
+    d_sh = qta.desc("taco_fp8", 128, rows, cols)
+    shards = [q.shard(r) for r in range(n)]
+    s = g.floats(rows * cols)
+    qta.qar_reduce(d_sh, shards, 0, rows, s)
+    d_g = qta.desc("taco_fp8", 256, 7, cols, batch=2)
+    gq = g.qtensor(d_g, 0.01)
+    gq.chan = chan
+    qta.qar_reduce_requant(d_sh, shards, 0, rows, d_g, gq, qta.SCALE_CURRENT)
+    y = g.bytes(2 * rows * cols).view(torch.bfloat16)
+    qta.taco_decompress(d_g, gq, y, qta.BF16)
+    g.check()
+    assert bool((raw[:PAD] == CANARY).all()) and bool((raw[PAD + 3 * cols * 4:] == CANARY).all())
+    assert qta.qta_device_error() == 0

@@ -245,3 +245,41 @@ def test_qwen_grad_16_steps_full_size(dev, pool):
     assert_same("final compress state", q.state, np.stack([np.array(S1, np.float32),
                                                             np.zeros(N, np.float32)], axis=1).reshape(-1))
     assert qta.qta_device_error() == 0
+
+
+# ------------------------------------------------------------------ tiny per-tensor scales
+@pytest.mark.parametrize("B", [64, 128, 256])
+def test_tiny_scales_take_the_unfolded_inverse(dev, B):
+    # The decompress and the FP32 reduce fold 1/B into the block scale only
+    # while every per-tensor scale S is at least 2^-71; tensors with smaller
+    # S (here 2^-83 and 2^-100, with inputs of that size) take the plain
+    # multiply at the end.  Both paths, also inside one warp tile (tensor
+    # boundaries inside tiles), must give the oracle's bits.
+    batch, rows, cols = 3, 11, 768
+    rng = np.random.default_rng(B)
+    x = random_values(rng, (batch, rows, cols), "mixed")
+    x[0] *= np.float32(2.0 ** -75)
+    x[2] *= np.float32(2.0 ** -92)
+    xt = torch.from_numpy(x.astype(np.float32))
+    state = np.array([2.0 ** -83, 0.0, 0.01, 0.0, 2.0 ** -100, 0.0], dtype=np.float32)
+    d, q = gpu_compress(qta.TACO_FP8, B, xt, qta.FP32, batch, rows, cols, qta.SCALE_DELAYED, state=state, dev=dev)
+    ref = oracle_compress(qta.TACO_FP8, B, xt, qta.FP32, batch, rows, cols, orc.DELAYED, state=state)
+    torch.cuda.synchronize()
+    compare_qtensor("tiny S", q, ref)
+    for od, tdt in ((qta.FP32, torch.float32), (qta.BF16, torch.bfloat16)):
+        y = torch.empty((batch, rows, cols), dtype=tdt, device=dev)
+        qta.taco_decompress(d, q, y, od)
+        yo = orc.decompress(orc.TACO_FP8, B, *ref, batch, rows, cols, orc.FP32 if od == qta.FP32 else orc.BF16)
+        torch.cuda.synchronize()
+        assert_same(f"decompress {od}", y, yo)
+    E, nb = rows * cols, rows * cols // B
+    shards = [(ref[0][r * E:(r + 1) * E], ref[1][r * nb:(r + 1) * nb], None, ref[3][2 * r:2 * r + 2])
+              for r in range(batch)]
+    d1 = qta.desc(qta.TACO_FP8, B, rows, cols)
+    for sel in ([0, 1, 2], [1], [0], [1, 2]):
+        s = torch.empty((rows, cols), dtype=torch.float32, device=dev)
+        qta.qar_reduce(d1, [q.shard(r) for r in sel], 0, rows, s)
+        so = orc.reduce(orc.TACO_FP8, B, [shards[r] for r in sel], rows, cols)
+        torch.cuda.synchronize()
+        assert_same(f"reduce {sel}", s, so)
+    assert qta.qta_device_error() == 0
