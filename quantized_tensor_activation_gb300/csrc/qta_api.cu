@@ -22,6 +22,7 @@ constexpr int MAX_DEVICES = 64;
 struct DeviceInfo {
     std::atomic<int> sms{0};
     std::atomic<int> smem_per_sm{0};
+    std::atomic<int> smem_optin{0};
     std::atomic<unsigned int*> err{nullptr};
 };
 DeviceInfo g_dev[MAX_DEVICES];
@@ -37,10 +38,13 @@ cudaError_t device_info(int* sms, int* smem_per_sm, unsigned int** err)
     if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
     DeviceInfo& d = g_dev[dev];
     if (d.sms.load() == 0) {
-        int a = 0, b = 0;
+        int a = 0, b = 0, o = 0;
         if ((e = cudaDeviceGetAttribute(&a, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
         if ((e = cudaDeviceGetAttribute(&b, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess)
             return e;
+        if ((e = cudaDeviceGetAttribute(&o, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+            return e;
+        d.smem_optin.store(o);
         void* p = nullptr;
         if ((e = cudaGetSymbolAddress(&p, g_error_flags)) != cudaSuccess) return e;
         d.smem_per_sm.store(b);
@@ -51,6 +55,15 @@ cudaError_t device_info(int* sms, int* smem_per_sm, unsigned int** err)
     *smem_per_sm = d.smem_per_sm.load();
     *err = d.err.load();
     return cudaSuccess;
+}
+
+// Dynamic shared memory a launch may use: the opt-in maximum less a margin
+// for the kernels' static shared memory (at most 64 bytes).
+int smem_optin()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return 0;
+    return g_dev[dev].smem_optin.load() - 256;
 }
 
 bool encoder_ready()
@@ -208,6 +221,10 @@ qta_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QTA_OK : QTA_E
 
 }  // namespace
 
+// The dynamic shared-memory limit of a kernel is raised once per device to
+// the device's opt-in maximum less the kernel's static shared memory, so that
+// launches of any size up to it (the kernel's own layout plus an optional
+// copy of the channel factors) pass.
 cudaError_t ensure_smem_attr(const void* func, int smem, std::atomic<unsigned>* done_mask)
 {
     int dev = 0;
@@ -215,7 +232,14 @@ cudaError_t ensure_smem_attr(const void* func, int smem, std::atomic<unsigned>* 
     if (e != cudaSuccess) return e;
     const unsigned bit = dev < 32 ? (1u << dev) : 0u;
     if (bit && (done_mask->load() & bit)) return cudaSuccess;
-    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, func);
+    if (e != cudaSuccess) return e;
+    const int dyn = optin - static_cast<int>(fa.sharedSizeBytes);
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn > smem ? dyn : smem);
     if (e == cudaSuccess && bit) done_mask->fetch_or(bit);
     return e;
 }
@@ -468,8 +492,10 @@ static qta_status compress_impl(const qta_desc* d, const void* x, int32_t x_dtyp
     p.chan = out->chan;
     p.seg_per_row = make_fastdiv(static_cast<uint32_t>(d->cols / 64));
     const int sch = d->scheme;  // qta_scheme values equal the kernel scheme kinds
-    const int grid =
-        grid_for(p.n_warp_tiles, compress_warps(x_dtype), compress_smem(x_dtype, sch), sms, smem_sm, d->max_sms);
+    const int chan_bytes = static_cast<int>(d->cols) * 4;
+    p.chan_smem = (out->chan && compress_smem(x_dtype, sch) + chan_bytes <= smem_optin()) ? 1 : 0;
+    const int grid = grid_for(p.n_warp_tiles, compress_warps(x_dtype),
+                              compress_smem(x_dtype, sch) + (p.chan_smem ? chan_bytes : 0), sms, smem_sm, d->max_sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (d->scheme == QTA_TACO_FP8 && base_mode == QTA_SCALE_CURRENT) {
         cudaError_t e = launch_state(out->state, d->batch, STATE_RESET_AMAX, s);
@@ -523,8 +549,11 @@ qta_status taco_decompress(const qta_desc* d, const qta_qtensor* in, void* y, in
     p.seg_per_tensor = make_fastdiv(static_cast<uint32_t>(d->rows * d->cols / 64));
     p.chan_up = in->chan ? in->chan + d->cols : nullptr;
     p.seg_per_row = make_fastdiv(static_cast<uint32_t>(d->cols / 64));
-    const int grid = grid_for(p.n_warp_tiles, decompress_warps(y_dtype), decompress_smem(d->scheme, y_dtype), sms,
-                              smem_sm, d->max_sms);
+    const int chan_bytes = static_cast<int>(d->cols) * 4;
+    p.chan_smem = (in->chan && decompress_smem(d->scheme, y_dtype) + chan_bytes <= smem_optin()) ? 1 : 0;
+    const int grid = grid_for(p.n_warp_tiles, decompress_warps(y_dtype),
+                              decompress_smem(d->scheme, y_dtype) + (p.chan_smem ? chan_bytes : 0), sms, smem_sm,
+                              d->max_sms);
     return cuda_status(launch_decompress(d->scheme, y_dtype, p, grid, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -633,8 +662,11 @@ qta_status qar_reduce(const qta_desc* d, const qta_qtensor* shards, int32_t n_ra
     if (!aligned(sum_out, 16)) return QTA_ERR_ALIGNMENT;
     if ((st = reduce_fill(d, shards, n_ranks, row_begin, row_end, &p, &sms, &smem_sm)) != QTA_OK) return st;
     if (!map_f32(&p.out_map, sum_out, static_cast<uint64_t>(p.M_out))) return QTA_ERR_CUDA;
-    const int grid =
-        grid_for(p.n_warp_tiles, reduce_warps(), reduce_smem(d->scheme, OUT_F32), sms, smem_sm, d->max_sms);
+    const int chan_bytes = static_cast<int>(d->cols) * 4;
+    p.chan_smem = (p.chan_up && reduce_smem(d->scheme, OUT_F32) + chan_bytes <= smem_optin()) ? 1 : 0;
+    const int grid = grid_for(p.n_warp_tiles, reduce_warps(),
+                              reduce_smem(d->scheme, OUT_F32) + (p.chan_smem ? chan_bytes : 0), sms, smem_sm,
+                              d->max_sms);
     return cuda_status(launch_reduce(d->scheme, p, grid, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -17,15 +17,16 @@ int compress_smem(int in_kind, int scheme)
     return a4 ? CompressCfg<IN_BF16, S_ASYM4>::SMEM : CompressCfg<IN_BF16, S_TACO>::SMEM;
 }
 
-template <int IN, int SCH, bool AMAX, int LG = -1>
+template <int IN, int SCH, bool AMAX, int LG = -1, bool CH = false>
 static cudaError_t launch_one(const CompressParams& p, int grid, cudaStream_t stream)
 {
     using C = CompressCfg<IN, SCH>;
     static std::atomic<unsigned> done{0};
-    auto fn = compress_kernel<IN, SCH, AMAX, LG>;
+    auto fn = compress_kernel<IN, SCH, AMAX, LG, CH>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(fn), C::SMEM, &done);
     if (e != cudaSuccess) return e;
-    return launch_pdl(fn, dim3(grid), dim3(C::WARPS * 32), C::SMEM, stream, p);
+    const int extra = (CH && p.chan_smem) ? static_cast<int>(p.seg_per_row.d) * SEG * 4 : 0;
+    return launch_pdl(fn, dim3(grid), dim3(C::WARPS * 32), C::SMEM + extra, stream, p);
 }
 
 // TACO with 4 lanes per block (B = 256) runs a kernel compiled for that
@@ -33,9 +34,15 @@ static cudaError_t launch_one(const CompressParams& p, int grid, cudaStream_t st
 // specialisation for 2 lanes (B = 128) ran slower than the kernel that reads
 // the block size at run time (141 against 129 us on 8192 x 4096 x 8), so
 // B = 64 and 128 keep the run-time kernel.
+// With the adaptive rescaling (p.chan) a separate instantiation applies the
+// channel factors, so that the kernels without them keep their registers.
 template <int IN, bool AMAX>
 static cudaError_t launch_taco(const CompressParams& p, int grid, cudaStream_t s)
 {
+    if (p.chan) {
+        if (p.lanes_log2 == 2) return launch_one<IN, S_TACO, AMAX, 2, true>(p, grid, s);
+        return launch_one<IN, S_TACO, AMAX, -1, true>(p, grid, s);
+    }
     if (p.lanes_log2 == 2) return launch_one<IN, S_TACO, AMAX, 2>(p, grid, s);
     return launch_one<IN, S_TACO, AMAX, -1>(p, grid, s);
 }

@@ -17,15 +17,16 @@ int decompress_smem(int scheme, int out_kind)
 }
 
 
-template <int SCH, int OUT, int LG = -1>
+template <int SCH, int OUT, int LG = -1, bool CH = false>
 static cudaError_t launch_d(const DecompressParams& p, int grid, cudaStream_t stream)
 {
     using C = DecompressCfg<SCH, OUT>;
     static std::atomic<unsigned> done{0};
-    auto fn = decompress_kernel<SCH, OUT, LG>;
+    auto fn = decompress_kernel<SCH, OUT, LG, CH>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(fn), C::SMEM, &done);
     if (e != cudaSuccess) return e;
-    return launch_pdl(fn, dim3(grid), dim3(C::WARPS * 32), C::SMEM, stream, p);
+    const int extra = (CH && p.chan_smem) ? static_cast<int>(p.seg_per_row.d) * SEG * 4 : 0;
+    return launch_pdl(fn, dim3(grid), dim3(C::WARPS * 32), C::SMEM + extra, stream, p);
 }
 
 // TACO kernels are compiled per block size (1, 2 or 4 lanes per block).
@@ -34,6 +35,13 @@ static cudaError_t launch_d_lanes(const DecompressParams& p, int grid, cudaStrea
 {
     if constexpr (SCH != S_TACO) {
         return launch_d<SCH, OUT>(p, grid, s);
+    } else if (p.chan_up) {   // the adaptive rescaling: its own instantiation
+        switch (p.lanes_log2) {
+        case 0: return launch_d<SCH, OUT, 0, true>(p, grid, s);
+        case 1: return launch_d<SCH, OUT, 1, true>(p, grid, s);
+        case 2: return launch_d<SCH, OUT, 2, true>(p, grid, s);
+        default: return cudaErrorInvalidValue;
+        }
     } else {
         switch (p.lanes_log2) {
         case 0: return launch_d<SCH, OUT, 0>(p, grid, s);

@@ -43,6 +43,7 @@ struct CompressParams {
     int round_up;         // TACO: block scales rounded up (QTA_SCALE_ROUND_UP)
     const float* chan;    // TACO adaptive rescaling: per-channel factors down[cols] (NULL: none)
     FastDiv seg_per_row;  // cols / 64
+    int chan_smem;        // the factors are copied into shared memory (cols * 4 extra bytes)
 };
 
 struct DecompressParams {
@@ -60,6 +61,7 @@ struct DecompressParams {
     FastDiv seg_per_tensor;
     const float* chan_up; // TACO adaptive rescaling: per-channel factors up[cols] (NULL: none)
     FastDiv seg_per_row;  // cols / 64
+    int chan_smem;        // the factors are copied into shared memory (cols * 4 extra bytes)
 };
 
 struct ReduceParams {
@@ -86,6 +88,7 @@ struct ReduceParams {
     int q_round_up;
     const float* chan_up; // TACO FP32 sum: per-channel factors up[cols] (NULL: none)
     FastDiv seg_per_row;  // cols / 64
+    int chan_smem;        // the factors are copied into shared memory (cols * 4 extra bytes)
 };
 
 // One ring hop: the incoming quantized partial sum plus the local tensor x,
@@ -129,6 +132,7 @@ struct CompressCfg {
     static constexpr int WARP_SMEM = STAGES * IN_BYTES + OUT_BUFS * OUT_BYTES;
     static constexpr int AMAX_BYTES = (SCH == S_TACO) ? 4 * AMAX_SLOTS_CFG : 0;
     static constexpr int SMEM = WARPS * WARP_SMEM + WARPS * STAGES * 8 + AMAX_BYTES + 1024;
+    static constexpr int CHAN_OFF = WARPS * WARP_SMEM + WARPS * STAGES * 8 + AMAX_BYTES;   // 16-byte aligned
 };
 
 template <int SCH, int OUT>
@@ -142,6 +146,7 @@ struct DecompressCfg {
     static constexpr int OUT_BUFS = 1;
     static constexpr int WARP_SMEM = STAGES * IN_BYTES + OUT_BUFS * OUT_BYTES;
     static constexpr int SMEM = WARPS * WARP_SMEM + WARPS * STAGES * 8 + 1024;
+    static constexpr int CHAN_OFF = WARPS * WARP_SMEM + WARPS * STAGES * 8;
 };
 
 // OSCH: OUT_F32 for the FP32 sum (qar_reduce), else the requantization scheme
@@ -171,6 +176,7 @@ struct ReduceCfg {
     static constexpr int WARP_SMEM = STAGES * STAGE_BYTES + OUT_BUFS * OUT_BYTES;
     static constexpr int AMAX_BYTES = (OSCH == S_TACO) ? 4 * AMAX_SLOTS_CFG : 0;
     static constexpr int SMEM = WARPS * WARP_SMEM + WARPS * STAGES * 8 + AMAX_BYTES + 1024;
+    static constexpr int CHAN_OFF = WARPS * WARP_SMEM + WARPS * STAGES * 8 + AMAX_BYTES;
 };
 
 // Ring hop: a stage holds a warp tile of incoming codes (2 KB slot) and of
@@ -395,16 +401,6 @@ __device__ __forceinline__ void store_out16or32(const CUtensorMap* map, const ui
     }
 }
 
-// ------------------------------------------------------------ 1/B folded into the scale
-// The inverse transform ends with a multiply by 1/B (a power of two).  When
-// every per-tensor scale S of the values involved is at least 2^-71, every
-// block scale s_b = S r_b with r_b >= 2^-9 is at least 2^-80 and every
-// nonzero value the butterfly forms is a multiple of 2^-23 s_b 2^-9 >= 2^-112;
-// scaled by 1/B >= 2^-8 it stays a normal float.  In that range multiplying
-// by a power of two commutes with every rounding, so s_b / B in place of s_b,
-// and no multiply at the end, gives the same bits.
-constexpr float FOLD_MIN_S = 0x1p-71f;
-
 // ------------------------------------------------------------ adaptive rescaling
 // Column of the first element of segment g (cols = 64 * spr.d per row).
 __device__ __forceinline__ int seg_col0(int g, const FastDiv& spr)
@@ -438,6 +434,51 @@ __device__ __forceinline__ void scale_xl(u64 (&v)[32], const float* __restrict__
         const int g = j >> (5 - lg);
         const int pos = static_cast<int>(xm) + 2 * (j & ((1 << (5 - lg)) - 1));
         const float4 c = __ldg(reinterpret_cast<const float4*>(f + colb + SEG * xl_group_row(g, lg) + pos));
+        v[j] = mul2(v[j], pk2(c.x, c.y));
+        v[j + 1] = mul2(v[j + 1], pk2(c.z, c.w));
+    }
+}
+
+// The factors in shared memory: the 16-byte chunk k (4 channels) of
+// segment-column j (64 channels) sits at chunk (j << 4) | (k ^ (j & 7)), so
+// that the lanes of a wavefront, which read neighbouring segment-columns,
+// hit different bank groups.  Every thread of the CTA copies a share, then
+// the CTA synchronises.
+__device__ __forceinline__ void chan_to_smem(float* fsm, const float* __restrict__ f, int cols)
+{
+    float4* d = reinterpret_cast<float4*>(fsm);
+    const float4* g = reinterpret_cast<const float4*>(f);
+    for (int i = threadIdx.x; i < cols / 4; i += blockDim.x) {
+        const int j = i >> 4, k = i & 15;
+        d[(j << 4) | (k ^ (j & 7))] = __ldg(g + i);
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ float4 chan_sm(const float* fsm, int j, int k)
+{
+    return reinterpret_cast<const float4*>(fsm)[(j << 4) | (k ^ (j & 7))];
+}
+
+// scale_slots from the shared copy; j = the segment-column of the lane's segment.
+__device__ __forceinline__ void scale_slots_sm(u64 (&v)[32], const float* fsm, int j, uint32_t xm)
+{
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        const float4 c = chan_sm(fsm, j, q ^ static_cast<int>(xm >> 2));
+        v[2 * q] = mul2(v[2 * q], pk2(c.x, c.y));
+        v[2 * q + 1] = mul2(v[2 * q + 1], pk2(c.z, c.w));
+    }
+}
+
+// scale_xl from the shared copy; jb = the segment-column of the block's first segment.
+__device__ __forceinline__ void scale_xl_sm(u64 (&v)[32], const float* fsm, int jb, int lg, uint32_t xm)
+{
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        const int g = j >> (5 - lg);
+        const int pos = static_cast<int>(xm) + 2 * (j & ((1 << (5 - lg)) - 1));
+        const float4 c = chan_sm(fsm, jb + xl_group_row(g, lg), pos >> 2);
         v[j] = mul2(v[j], pk2(c.x, c.y));
         v[j + 1] = mul2(v[j + 1], pk2(c.z, c.w));
     }
@@ -745,7 +786,8 @@ __device__ __forceinline__ void store_codes(uint8_t* ob, const CUtensorMap* map,
 // ------------------------------------------------------------ compress
 // taco_compress / qar_requant / CURRENT-mode amax pre-pass (AMAX_ONLY).
 // LG: log2 of the lanes per block when fixed at compile time (TACO), else -1.
-template <int IN, int SCH, bool AMAX_ONLY, int LG = -1>
+// CH: the adaptive rescaling's channel factors are applied (TACO, p.chan).
+template <int IN, int SCH, bool AMAX_ONLY, int LG = -1, bool CH = false>
 __global__ void __launch_bounds__(CompressCfg<IN, SCH>::WARPS * 32, 1)
 compress_kernel(const __grid_constant__ CompressParams p)
 {
@@ -767,6 +809,9 @@ compress_kernel(const __grid_constant__ CompressParams p)
     if constexpr (SCH == S_TACO) cta_amax_init(amax_tab);
     pdl_wait();
     pdl_trigger();
+    float* fsm = reinterpret_cast<float*>(smem + C::CHAN_OFF);
+    if constexpr (CH)
+        if (p.chan_smem) chan_to_smem(fsm, p.chan, static_cast<int>(p.seg_per_row.d) * SEG);
     if (lane == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             const int wt = first + s * W;
@@ -813,8 +858,13 @@ compress_kernel(const __grid_constant__ CompressParams p)
             phase ^= 1u;
         }
         // adaptive rescaling: the channel factors before the transform
-        if constexpr (SCH == S_TACO)
-            if (p.chan) scale_slots(v, p.chan, seg_col0(wt * 32 + lane, p.seg_per_row), xm);
+        if constexpr (CH) {
+            const int c0 = seg_col0(wt * 32 + lane, p.seg_per_row);
+            if (p.chan_smem)
+                scale_slots_sm(v, fsm, c0 / SEG, xm);
+            else
+                scale_slots(v, p.chan, c0, xm);
+        }
         uint32_t ow[16];
         quant.template run<AMAX_ONLY, XL>(v, qo, wt * 32, lane, ow, false, xm);
         if constexpr (!AMAX_ONLY)
@@ -867,7 +917,8 @@ struct SegMeta {
 };
 
 // LG: log2 of the lanes per block when fixed at compile time (TACO), else -1.
-template <int SCH, int OUT, int LG = -1>
+// CH: the adaptive rescaling's channel factors are applied (TACO, p.chan_up).
+template <int SCH, int OUT, int LG = -1, bool CH = false>
 __global__ void __launch_bounds__(DecompressCfg<SCH, OUT>::WARPS * 32, 1)
 decompress_kernel(const __grid_constant__ DecompressParams p)
 {
@@ -887,6 +938,9 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
     }
     pdl_wait();
     pdl_trigger();
+    float* fsm = reinterpret_cast<float*>(smem + C::CHAN_OFF);
+    if constexpr (CH)
+        if (p.chan_smem) chan_to_smem(fsm, p.chan_up, static_cast<int>(p.seg_per_row.d) * SEG);
     if (lane == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             const int wt = first + s * W;
@@ -925,12 +979,6 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
         }
         float s, z;
         cur.decode(s, z);
-        // TACO: 1/B folded into the block scale when every lane's S allows it
-        bool fold = false;
-        if constexpr (SCH == S_TACO) {
-            fold = __all_sync(0xffffffffu, cur.S >= FOLD_MIN_S);
-            if (fold) s = __fmul_rn(s, p.inv_block);
-        }
         u64 v[32];
         dequant_segment<SCH, 0>(wb + stage * C::IN_BYTES, lane, s, z, v, static_cast<uint16_t>(cur.raw), xm);
         __syncwarp();
@@ -949,13 +997,16 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
         if constexpr (SCH == S_TACO) {
             fwht64_local_xl(v, xm);
             fwht_cross_xl(v, L, lane);
-            if (!fold) {
-                const u64 ib = pk2(p.inv_block, p.inv_block);
+            const u64 ib = pk2(p.inv_block, p.inv_block);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = mul2(v[j], ib);
+            for (int j = 0; j < 32; ++j) v[j] = mul2(v[j], ib);
+            if constexpr (CH) {
+                const int cb = seg_col0(wt * 32 + (lane & ~(L - 1)), p.seg_per_row);
+                if (p.chan_smem)
+                    scale_xl_sm(v, fsm, cb / SEG, lg, xm);
+                else
+                    scale_xl(v, p.chan_up, cb, lg, xm);
             }
-            if (p.chan_up)
-                scale_xl(v, p.chan_up, seg_col0(wt * 32 + (lane & ~(L - 1)), p.seg_per_row), lg, xm);
         }
         uint8_t* ob = outb + (k % C::OUT_BUFS) * C::OUT_BYTES;
         if (lane == 0) {
@@ -1051,7 +1102,9 @@ __device__ __forceinline__ void reduce_meta_load(const ReduceParams& p, int t, i
 // domain sum is requantized directly.
 // LG: log2 of the shards' lanes per block when fixed at compile time (the
 // TACO FP32 sum, which inverts the transform with the halved exchange), else -1.
-template <int SCH, int OSCH, bool AMAX_ONLY, int LG = -1>
+// CH: the adaptive rescaling's channel factors are applied to the TACO FP32
+// sum (p.chan_up).
+template <int SCH, int OSCH, bool AMAX_ONLY, int LG = -1, bool CH = false>
 __global__ void __launch_bounds__(ReduceCfg<SCH, OSCH>::WARPS * 32, 1)
 reduce_kernel(const __grid_constant__ ReduceParams p)
 {
@@ -1083,12 +1136,9 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
         if (threadIdx.x < p.n_ranks) sS[threadIdx.x] = __ldg(p.state[threadIdx.x]);
         __syncthreads();
     }
-    // TACO FP32 sum: 1/B folded into the shards' block scales (FOLD_MIN_S)
-    bool fold = false;
-    if constexpr (SCH == S_TACO && OSCH == OUT_F32) {
-        fold = true;
-        for (int r = 0; r < n; ++r) fold = fold && (sS[r] >= FOLD_MIN_S);
-    }
+    float* fsm = reinterpret_cast<float*>(smem + C::CHAN_OFF);
+    if constexpr (CH)
+        if (p.chan_smem) chan_to_smem(fsm, p.chan_up, static_cast<int>(p.seg_per_row.d) * SEG);
     if (lane == 0) {
         for (int u = 0; u < C::STAGES && u < total_units; ++u) {
             reduce_issue<SCH, OSCH>(p, wb, bars, u, next_unit, first, W);
@@ -1141,7 +1191,6 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                 float s, z;
                 if constexpr (SCH == S_TACO) {
                     s = __fmul_rn(sS[r], e4m3_decode(cur[kk].raw));
-                    if (fold) s = __fmul_rn(s, p.inv_block);
                     z = 0.0f;
                 } else {
                     cur[kk].decode(s, z);
@@ -1181,16 +1230,16 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                 fwht_cross(acc, L, lane);
             }
             if constexpr (OSCH == OUT_F32) {
-                if (!fold) {
-                    const u64 ib = pk2(p.inv_block, p.inv_block);
+                const u64 ib = pk2(p.inv_block, p.inv_block);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) acc[j] = mul2(acc[j], ib);
+                for (int j = 0; j < 32; ++j) acc[j] = mul2(acc[j], ib);
+                if constexpr (CH && XL) {
+                    const int cb = seg_col0(p.seg_begin + wt * 32 + (lane & ~(L - 1)), p.seg_per_row);
+                    if (p.chan_smem)
+                        scale_xl_sm(acc, fsm, cb / SEG, (LG >= 0) ? LG : p.lanes_log2, xm);
+                    else
+                        scale_xl(acc, p.chan_up, cb, (LG >= 0) ? LG : p.lanes_log2, xm);
                 }
-                if constexpr (XL)
-                    if (p.chan_up)
-                        scale_xl(acc, p.chan_up,
-                                 seg_col0(p.seg_begin + wt * 32 + (lane & ~(L - 1)), p.seg_per_row),
-                                 (LG >= 0) ? LG : p.lanes_log2, xm);
             } else {
                 // scalar rounded multiplies: the requantizer's butterfly adds
                 // follow, and a packed multiply would be contracted into them

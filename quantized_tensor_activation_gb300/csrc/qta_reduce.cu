@@ -20,21 +20,30 @@ int reduce_smem(int scheme, int out_scheme)
 
 bool reduce_requant_supported(int scheme, int out_scheme) { return reduce_smem(scheme, out_scheme) > 0 && out_scheme != OUT_F32; }
 
-template <int SCH, int OSCH, bool AMAX, int LG = -1>
+template <int SCH, int OSCH, bool AMAX, int LG = -1, bool CH = false>
 static cudaError_t launch_r(const ReduceParams& p, int grid, cudaStream_t stream)
 {
     using C = ReduceCfg<SCH, OSCH>;
     static std::atomic<unsigned> done{0};
-    auto fn = reduce_kernel<SCH, OSCH, AMAX, LG>;
+    auto fn = reduce_kernel<SCH, OSCH, AMAX, LG, CH>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(fn), C::SMEM, &done);
     if (e != cudaSuccess) return e;
-    return launch_pdl(fn, dim3(grid), dim3(C::WARPS * 32), C::SMEM, stream, p);
+    const int extra = (CH && p.chan_smem) ? static_cast<int>(p.seg_per_row.d) * SEG * 4 : 0;
+    return launch_pdl(fn, dim3(grid), dim3(C::WARPS * 32), C::SMEM + extra, stream, p);
 }
 
 cudaError_t launch_reduce(int scheme, const ReduceParams& p, int grid, cudaStream_t stream)
 {
     switch (scheme) {
     case S_TACO:   // compiled per block size: the inverse transform's strips are constants
+        if (p.chan_up) {   // the adaptive rescaling: its own instantiation
+            switch (p.lanes_log2) {
+            case 0: return launch_r<S_TACO, OUT_F32, false, 0, true>(p, grid, stream);
+            case 1: return launch_r<S_TACO, OUT_F32, false, 1, true>(p, grid, stream);
+            case 2: return launch_r<S_TACO, OUT_F32, false, 2, true>(p, grid, stream);
+            default: return cudaErrorInvalidValue;
+            }
+        }
         switch (p.lanes_log2) {
         case 0: return launch_r<S_TACO, OUT_F32, false, 0>(p, grid, stream);
         case 1: return launch_r<S_TACO, OUT_F32, false, 1>(p, grid, stream);

@@ -249,12 +249,12 @@ def test_qwen_grad_16_steps_full_size(dev, pool):
 
 # ------------------------------------------------------------------ tiny per-tensor scales
 @pytest.mark.parametrize("B", [64, 128, 256])
-def test_tiny_scales_take_the_unfolded_inverse(dev, B):
-    # The decompress and the FP32 reduce fold 1/B into the block scale only
-    # while every per-tensor scale S is at least 2^-71; tensors with smaller
-    # S (here 2^-83 and 2^-100, with inputs of that size) take the plain
-    # multiply at the end.  Both paths, also inside one warp tile (tensor
-    # boundaries inside tiles), must give the oracle's bits.
+def test_tiny_per_tensor_scales(dev, B):
+    # Per-tensor scales far below the usual range (2^-83 and 2^-100, with
+    # inputs of that size) next to an ordinary one, with tensor boundaries
+    # inside warp tiles: the decompress and the FP32 reduce must give the
+    # oracle's bits (every multiply by 1/B and by the block scale keeps its
+    # own rounding, also near the subnormal range).
     batch, rows, cols = 3, 11, 768
     rng = np.random.default_rng(B)
     x = random_values(rng, (batch, rows, cols), "mixed")
