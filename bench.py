@@ -379,12 +379,23 @@ def _cpu_rows(w, target_elems: int) -> int:
     return max(rows, w.ranks)
 
 
-def cpu_baseline(w, rows: int, seed: int):
-    dt_s, nbytes, threads = _cpu_oracle_path(w, rows, seed=seed)
-    return {"value": nbytes / dt_s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+def cpu_baseline(w, rows: int, seed: int, min_s: float = 0.0, max_reps: int = 8):
+    """The oracle's whole path on a row sample of every rank, repeated on new
+    seeds until min_s seconds of CPU work are reached (at most max_reps)."""
+    total_s, total_b, reps = 0.0, 0, 0
+    stages = {}
+    while reps < max_reps and (reps == 0 or total_s < min_s):
+        dt_s, nbytes, threads = _cpu_oracle_path(w, rows, seed=seed + reps)
+        total_s += dt_s
+        total_b += nbytes
+        reps += 1
+        for k, v in _cpu_oracle_path.stages.items():
+            stages[k] = stages.get(k, 0.0) + v
+    return {"value": total_b / total_s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"{rows} of {w.rows} rows of each of the {w.ranks} ranks "
-                      f"({w.ranks * rows * w.cols} elements), full path, {dt_s:.1f} s",
-            "stages": dict(_cpu_oracle_path.stages), "host": _host_cpu()}
+                      f"({w.ranks * rows * w.cols} elements), full path, {reps} pass(es) on different seeds, "
+                      f"{total_s:.1f} s",
+            "stages": stages, "host": _host_cpu()}
 
 
 def measure_workload(qta, w, args, dev, ws: int, local: int, headline: bool) -> dict:
@@ -941,7 +952,7 @@ def run_qta(args, w):
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, args.cpu_rows or _cpu_rows(w, 4e8), args.seed)
+        cpu = cpu_baseline(w, args.cpu_rows or _cpu_rows(w, 4e8), args.seed, min_s=10.0)
         for name, rep in per_config.items():
             wc = workloads.WORKLOADS[name]
             rep["cpu_baseline"] = cpu_baseline(wc, _cpu_rows(wc, 6e7), args.seed)
