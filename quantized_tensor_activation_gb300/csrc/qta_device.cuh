@@ -503,45 +503,83 @@ __device__ __forceinline__ void fwht64_local_xl(u64 (&v)[32], uint32_t xm)
 // Strides 64 and 128 with the halved exchange, on the permuted slots.  Stage
 // d pairs lane c with c ^ d.  Each lane keeps the lower half of every group of
 // registers and ships the upper half, which holds the partner's kept
-// positions.  With a = the kept value, o = the partner's value there and
-// s = +1 in the upper lane (else -1): lower row a+o, upper row
-// fma(o, s, -s*a) = (lower - upper), both rounded once as in fwht_cross
-// (-s*a is exact; a sign-bit XOR in its place measured slower).  Afterwards,
-// with 4 lanes per block, registers 0-7, 8-15, 16-23, 24-31 hold rows 0, 2,
-// 1, 3 of the block; with 2 lanes, registers 0-15 and 16-31 hold rows 0 and
-// 1.  Register 2i+t of a group holds position xm + 2i + t.
+// positions.  With a = the lane's kept value and o = the partner's value at
+// the same position, the pair's outputs are (lower + upper, lower - upper),
+// each rounded once as in fwht_cross.
+// SWAP = false: every lane writes the sum to the lower half of the group and
+// the difference to the upper half: a + o, and fma(o, s, -s*a) with s = +1
+// in the lane that holds the upper row (else -1), which is lower - upper in
+// both lanes (-s*a is exact).  Afterwards, with 4 lanes per block, registers
+// 0-7, 8-15, 16-23, 24-31 hold rows 0, 2, 1, 3 of the block; with 2 lanes,
+// registers 0-15 and 16-31 hold rows 0 and 1.
+// SWAP = true: the lane whose stage bit is clear (a from the lower row)
+// writes fma(a, +1, o) and fma(o, -1, a); the lane whose bit is set (a from
+// the upper row) writes the difference first, fma(a, -1, o) = o - a, then
+// fma(o, +1, a) = o + a.  The same adds and subtracts, zero signs included,
+// one instruction fewer per register pair, and the row order swapped by the
+// lane's position in its block (xl_group_row with that position), so that the
+// lanes of a block write rows of different parity in one store instruction.
+// Register 2i+t of a group holds position xm + 2i + t.
+template <bool SWAP = false>
 __device__ __forceinline__ void fwht_cross_xl(u64 (&v)[32], int lanes_per_block, int lane)
 {
     if (lanes_per_block >= 2) {
-        const float s = (lane & 1) ? 1.0f : -1.0f;
-        const u64 s2 = pk2(s, s), ns2 = pk2(-s, -s);
+        if constexpr (SWAP) {
+            const float s = (lane & 1) ? -1.0f : 1.0f;
+            const u64 s2 = pk2(s, s), ns2 = pk2(-s, -s);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const u64 o = __shfl_xor_sync(0xffffffffu, v[16 + j], 1);
-            const u64 a = v[j];
-            v[j] = add2(a, o);
-            v[16 + j] = fma2(o, s2, mul2(a, ns2));
+            for (int j = 0; j < 16; ++j) {
+                const u64 o = __shfl_xor_sync(0xffffffffu, v[16 + j], 1);
+                const u64 a = v[j];
+                v[j] = fma2(a, s2, o);
+                v[16 + j] = fma2(o, ns2, a);
+            }
+        } else {
+            const float s = (lane & 1) ? 1.0f : -1.0f;
+            const u64 s2 = pk2(s, s), ns2 = pk2(-s, -s);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const u64 o = __shfl_xor_sync(0xffffffffu, v[16 + j], 1);
+                const u64 a = v[j];
+                v[j] = add2(a, o);
+                v[16 + j] = fma2(o, s2, mul2(a, ns2));
+            }
         }
     }
     if (lanes_per_block == 4) {
-        const float s = (lane & 2) ? 1.0f : -1.0f;
-        const u64 s2 = pk2(s, s), ns2 = pk2(-s, -s);
+        if constexpr (SWAP) {
+            const float s = (lane & 2) ? -1.0f : 1.0f;
+            const u64 s2 = pk2(s, s), ns2 = pk2(-s, -s);
 #pragma unroll
-        for (int h = 0; h < 32; h += 16)
+            for (int h = 0; h < 32; h += 16)
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const u64 o = __shfl_xor_sync(0xffffffffu, v[h + 8 + j], 2);
-                const u64 a = v[h + j];
-                v[h + j] = add2(a, o);
-                v[h + 8 + j] = fma2(o, s2, mul2(a, ns2));
-            }
+                for (int j = 0; j < 8; ++j) {
+                    const u64 o = __shfl_xor_sync(0xffffffffu, v[h + 8 + j], 2);
+                    const u64 a = v[h + j];
+                    v[h + j] = fma2(a, s2, o);
+                    v[h + 8 + j] = fma2(o, ns2, a);
+                }
+        } else {
+            const float s = (lane & 2) ? 1.0f : -1.0f;
+            const u64 s2 = pk2(s, s), ns2 = pk2(-s, -s);
+#pragma unroll
+            for (int h = 0; h < 32; h += 16)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const u64 o = __shfl_xor_sync(0xffffffffu, v[h + 8 + j], 2);
+                    const u64 a = v[h + j];
+                    v[h + j] = add2(a, o);
+                    v[h + 8 + j] = fma2(o, s2, mul2(a, ns2));
+                }
+        }
     }
 }
 
-// Block row (0 .. lanes-1) held by register group g after fwht_cross_xl.
-__device__ __forceinline__ int xl_group_row(int g, int lanes_log2)
+// Block row (0 .. lanes-1) held by register group g after fwht_cross_xl: p is
+// the lane's position in its block with SWAP, 0 without.
+__device__ __forceinline__ int xl_group_row(int g, int lanes_log2, int p)
 {
-    return lanes_log2 == 2 ? (((g & 1) << 1) | (g >> 1)) : g;
+    return (lanes_log2 == 2 ? (((g & 1) << 1) | (g >> 1)) : g) ^ p;
 }
 
 __device__ __forceinline__ float group_max(float m, int lanes_per_block)

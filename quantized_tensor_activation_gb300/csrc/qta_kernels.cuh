@@ -257,11 +257,12 @@ __device__ __forceinline__ void store_segment(uint8_t* ob, int lane, const u64 (
 }
 
 // Output of fwht_cross_xl into the staging rows: register group g (32/L
-// pairs) goes to row (lane & ~(L-1)) + xl_group_row(g) of the warp tile,
-// positions xm .. xm + 64/L - 1.
+// pairs) goes to row (lane & ~(L-1)) + xl_group_row(g, lg, p) of the warp
+// tile (p: the lane's position in its block after a swapping exchange, else
+// 0), positions xm .. xm + 64/L - 1.
 template <int OUT>
 __device__ __forceinline__ void store_segment_xl(uint8_t* ob, int lane, const u64 (&v)[32], int lanes_log2,
-                                                 uint32_t xm)
+                                                 uint32_t xm, int p)
 {
     const int base = lane & ~((1 << lanes_log2) - 1);
     if constexpr (OUT == IN_FP32) {
@@ -269,7 +270,7 @@ __device__ __forceinline__ void store_segment_xl(uint8_t* ob, int lane, const u6
 #pragma unroll
         for (int sc = 0; sc < 16; ++sc) {
             const int g = sc >> kl;
-            const uint32_t row = base + xl_group_row(g, lanes_log2);
+            const uint32_t row = base + xl_group_row(g, lanes_log2, p);
             const uint32_t pc = (xm >> 2) + (sc & ((1 << kl) - 1));
             const u64 a = v[sc * 2], b = v[sc * 2 + 1];
             sts128(ob + (pc >> 3) * 4096, sw128(row, pc & 7u), make_uint4(lo32(a), hi32(a), lo32(b), hi32(b)));
@@ -279,7 +280,7 @@ __device__ __forceinline__ void store_segment_xl(uint8_t* ob, int lane, const u6
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
             const int g = c >> kl;
-            const uint32_t row = base + xl_group_row(g, lanes_log2);
+            const uint32_t row = base + xl_group_row(g, lanes_log2, p);
             const uint32_t pc = (xm >> 3) + (c & ((1 << kl) - 1));
             uint32_t w[4];
 #pragma unroll
@@ -424,16 +425,17 @@ __device__ __forceinline__ void scale_slots(u64 (&v)[32], const float* __restric
 }
 
 // The same for values in the layout fwht_cross_xl leaves: pair j holds row
-// group g = j >> (5 - lg) of the block (segment base + xl_group_row(g)) at
-// positions xm + 2 (j mod 2^(5-lg)); colb is the column of the block's first
-// element.
-__device__ __forceinline__ void scale_xl(u64 (&v)[32], const float* __restrict__ f, int colb, int lg, uint32_t xm)
+// group g = j >> (5 - lg) of the block (segment base + xl_group_row(g, lg, p),
+// p = the lane's position in its block) at positions xm + 2 (j mod 2^(5-lg));
+// colb is the column of the block's first element.
+__device__ __forceinline__ void scale_xl(u64 (&v)[32], const float* __restrict__ f, int colb, int lg, uint32_t xm,
+                                         int p)
 {
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
         const int g = j >> (5 - lg);
         const int pos = static_cast<int>(xm) + 2 * (j & ((1 << (5 - lg)) - 1));
-        const float4 c = __ldg(reinterpret_cast<const float4*>(f + colb + SEG * xl_group_row(g, lg) + pos));
+        const float4 c = __ldg(reinterpret_cast<const float4*>(f + colb + SEG * xl_group_row(g, lg, p) + pos));
         v[j] = mul2(v[j], pk2(c.x, c.y));
         v[j + 1] = mul2(v[j + 1], pk2(c.z, c.w));
     }
@@ -472,13 +474,13 @@ __device__ __forceinline__ void scale_slots_sm(u64 (&v)[32], const float* fsm, i
 }
 
 // scale_xl from the shared copy; jb = the segment-column of the block's first segment.
-__device__ __forceinline__ void scale_xl_sm(u64 (&v)[32], const float* fsm, int jb, int lg, uint32_t xm)
+__device__ __forceinline__ void scale_xl_sm(u64 (&v)[32], const float* fsm, int jb, int lg, uint32_t xm, int p)
 {
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
         const int g = j >> (5 - lg);
         const int pos = static_cast<int>(xm) + 2 * (j & ((1 << (5 - lg)) - 1));
-        const float4 c = chan_sm(fsm, jb + xl_group_row(g, lg), pos >> 2);
+        const float4 c = chan_sm(fsm, jb + xl_group_row(g, lg, p), pos >> 2);
         v[j] = mul2(v[j], pk2(c.x, c.y));
         v[j + 1] = mul2(v[j + 1], pk2(c.z, c.w));
     }
@@ -744,8 +746,9 @@ struct Quantizer {
 
 // Stage one warp tile of code words in shared memory and store it with one
 // TMA tensor store (8-bit codes: 64 B rows, SW64; 4-bit: 32 B rows, SW32).
-// XL: ow is in the layout of fwht_cross_xl: word group g (16/L words) goes
-// to row (lane & ~(L-1)) + xl_group_row(g), codes xm .. xm + 64/L - 1.
+// XL: ow is in the layout of fwht_cross_xl (without the row swap): word
+// group g (16/L words) goes to row (lane & ~(L-1)) + xl_group_row(g, lg, 0),
+// codes xm .. xm + 64/L - 1.
 template <int SCH, int OUT_BUFS, bool XL = false>
 __device__ __forceinline__ void store_codes(uint8_t* ob, const CUtensorMap* map, int row, int lane,
                                             const uint32_t (&ow)[16], int lanes_log2 = 0, uint32_t xm = 0)
@@ -762,7 +765,7 @@ __device__ __forceinline__ void store_codes(uint8_t* ob, const CUtensorMap* map,
         const int kl = 2 - lanes_log2;   // log2 of the 16-byte chunks per group
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            const uint32_t r = base + xl_group_row(c >> kl, lanes_log2);
+            const uint32_t r = base + xl_group_row(c >> kl, lanes_log2, 0);
             const uint32_t pc = (xm >> 4) + (c & ((1 << kl) - 1));
             sts128(ob, sw64(r, pc), make_uint4(ow[4 * c], ow[4 * c + 1], ow[4 * c + 2], ow[4 * c + 3]));
         }
@@ -996,16 +999,16 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
         }
         if constexpr (SCH == S_TACO) {
             fwht64_local_xl(v, xm);
-            fwht_cross_xl(v, L, lane);
+            fwht_cross_xl<true>(v, L, lane);
             const u64 ib = pk2(p.inv_block, p.inv_block);
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = mul2(v[j], ib);
             if constexpr (CH) {
                 const int cb = seg_col0(wt * 32 + (lane & ~(L - 1)), p.seg_per_row);
                 if (p.chan_smem)
-                    scale_xl_sm(v, fsm, cb / SEG, lg, xm);
+                    scale_xl_sm(v, fsm, cb / SEG, lg, xm, lane & (L - 1));
                 else
-                    scale_xl(v, p.chan_up, cb, lg, xm);
+                    scale_xl(v, p.chan_up, cb, lg, xm, lane & (L - 1));
             }
         }
         uint8_t* ob = outb + (k % C::OUT_BUFS) * C::OUT_BYTES;
@@ -1017,7 +1020,7 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
         }
         __syncwarp();
         if constexpr (SCH == S_TACO)
-            store_segment_xl<OUT>(ob, lane, v, lg, xm);
+            store_segment_xl<OUT>(ob, lane, v, lg, xm, lane & (L - 1));
         else
             store_segment<OUT>(ob, lane, v);
         fence_proxy_async_smem();
@@ -1236,9 +1239,9 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                 if constexpr (CH && XL) {
                     const int cb = seg_col0(p.seg_begin + wt * 32 + (lane & ~(L - 1)), p.seg_per_row);
                     if (p.chan_smem)
-                        scale_xl_sm(acc, fsm, cb / SEG, (LG >= 0) ? LG : p.lanes_log2, xm);
+                        scale_xl_sm(acc, fsm, cb / SEG, (LG >= 0) ? LG : p.lanes_log2, xm, 0);
                     else
-                        scale_xl(acc, p.chan_up, cb, (LG >= 0) ? LG : p.lanes_log2, xm);
+                        scale_xl(acc, p.chan_up, cb, (LG >= 0) ? LG : p.lanes_log2, xm, 0);
                 }
             } else {
                 // scalar rounded multiplies: the requantizer's butterfly adds
@@ -1254,7 +1257,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
             if (lane == 0) bulk_wait_read<0>();
             __syncwarp();
             if constexpr (XL)
-                store_segment_xl<IN_FP32>(outb, lane, acc, (LG >= 0) ? LG : p.lanes_log2, xm);
+                store_segment_xl<IN_FP32>(outb, lane, acc, (LG >= 0) ? LG : p.lanes_log2, xm, 0);
             else
                 store_segment<IN_FP32>(outb, lane, acc);
             fence_proxy_async_smem();
