@@ -1039,7 +1039,7 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-rows", type=int, default=0,
                     help="oracle row sample per rank of the headline's CPU baseline (0: about 4e8 elements)")
-    ap.add_argument("--ref-rows", type=int, default=256)
+    ap.add_argument("--ref-rows", type=int, default=1024)
     ap.add_argument("--rows", type=int, default=0,
                     help="rows per rank of the headline workload (0: the workload's own; profiling captures of a "
                          "smaller case)")
