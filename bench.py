@@ -766,6 +766,39 @@ def measure_workload(qta, w, args, dev, ws: int, local: int, headline: bool) -> 
         torch.cuda.synchronize()
         assert qta.qta_device_error() == 0
 
+    # K4 beside the plain copy kernel K0 moving the same number of bytes (half
+    # read, half written), both timed the same way: single launches after an
+    # L2 flush that only reads (so that no dirty lines are left to write
+    # back), mean of 40 CUDA-event intervals each
+    k4_copy = None
+    if not getattr(args, "no_k0", False):
+        nb = (int(alg["K4"]) // 2) & ~4095
+        csrc_ = torch.empty(nb, dtype=torch.uint8, device=dev)
+        cdst = torch.empty_like(csrc_)
+        flush_buf = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+
+        def single_ms(fn, reps=40):
+            fn()
+            ts = []
+            for _ in range(reps):
+                flush_buf.sum()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b))
+            return statistics.mean(ts)
+
+        k4_ms = single_ms(lambda: qta.taco_decompress(d_g, g, y, in_dt))
+        k0_ms = single_ms(lambda: qta.qta_copy(csrc_, cdst, nb))
+        k4_copy = {"k4_bytes": alg["K4"], "k4_ms": k4_ms, "k4_gb_s": alg["K4"] / (k4_ms * 1e-3) / 1e9,
+                   "k0_bytes": 2 * nb, "k0_ms": k0_ms, "k0_gb_s": 2 * nb / (k0_ms * 1e-3) / 1e9,
+                   "note": "single launches after a 256 MB read-only L2 flush, mean of 40 CUDA-event intervals; "
+                           "K0 (qta_copy) copies k0_bytes / 2"}
+        del csrc_, cdst, flush_buf
+        assert qta.qta_device_error() == 0
+
     rep = {
         "config": _config(w),
         "ms_per_step": ms_step,
@@ -790,6 +823,7 @@ def measure_workload(qta, w, args, dev, ws: int, local: int, headline: bool) -> 
                        "ms_per_step": other_ms, "value": in_bytes / (other_ms * 1e-3) / 1e9 * ws,
                        "kernels": kernel_table(evs2, not fused)},
         "recon": recon,
+        "k4_beside_copy": k4_copy,
         "clocks": clk,
         "gpu_launches": n_launch,
         "inputs": (f"{n_in} per-step inputs resident in HBM ({n_in * in_bytes / 1e9:.2f} GB), cycled: step i "

@@ -370,6 +370,24 @@ __device__ __forceinline__ void u4x8_dequant(uint32_t w, uint16_t s, float z, fl
     fma_f16_pair(h37, s, z, f[3], f[7]);
 }
 
+// The same values scaled by 2^-24 (the low nibble of each byte) and 2^-20
+// (the high nibble), for a sum that is scaled back once at its end.  A
+// nibble masked in place, without the magic pattern, is the fp16 subnormal
+// n 2^-24 (low) or 16 n 2^-24 = n 2^-20 (high): one AND yields two fp16
+// operands and nothing is subtracted.  With zlo = z 2^-24 and zhi = z 2^-20
+// (exact), the mixed-precision fma gives RN(2^-24 (n s + z)).  s and z are
+// fp16 values, so n s + z is a multiple of 2^-24 and its scaled value is zero
+// or a normal FP32 number: the rounding commutes with the power-of-two scale,
+// and the result is 2^-24 fmaf(n, s, z) bit for bit.
+__device__ __forceinline__ void u4x8_dequant_scaled(uint32_t w, uint16_t s, float zlo, float zhi, float (&f)[8])
+{
+    const uint32_t w8 = w >> 8;
+    fma_f16_pair(w & 0x000F000Fu, s, zlo, f[0], f[4]);    // n0, n4 (2^-24)
+    fma_f16_pair(w & 0x00F000F0u, s, zhi, f[1], f[5]);    // n1, n5 (2^-20)
+    fma_f16_pair(w8 & 0x000F000Fu, s, zlo, f[2], f[6]);   // n2, n6
+    fma_f16_pair(w8 & 0x00F000F0u, s, zhi, f[3], f[7]);   // n3, n7
+}
+
 // Round-to-nearest-even to an integer through the FP32 adder: for |y| < 2^22
 // the bits of y + 1.5*2^23 are 0x4B400000 + rint(y); the low byte of those
 // bits is rint(y) mod 256.

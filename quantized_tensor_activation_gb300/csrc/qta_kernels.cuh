@@ -153,19 +153,24 @@ struct DecompressCfg {
 // of the fused reduce + requant.
 constexpr int OUT_F32 = -1;
 
-template <int SCH, int OSCH = OUT_F32>
+// LG: log2 of the lanes per block of a kernel compiled for one block size, else -1.
+template <int SCH, int OSCH = OUT_F32, int LG = -1>
 struct ReduceCfg {
     // the INT4 kernels and the fused TACO -> TACO reduce fit 128 registers
     // and run 16 warps (the INT4 decode is issue-bound; the TACO one fits
-    // with 2-rank metadata chunks and 6 stages); the others run 12
+    // with 2-rank metadata chunks and 6 stages of one rank, or 3 of two);
+    // the others run 12
     static constexpr bool W16 = (SCH == S_ASYM4) || (SCH == S_TACO && OSCH == S_TACO);
     static constexpr int WARPS = W16 ? 16 : 12;
     static constexpr int IN_SEG = (SCH == S_ASYM4) ? 32 : 64;
     static constexpr int OUT_SEG = (OSCH == OUT_F32) ? 256 : (OSCH == S_ASYM4) ? 32 : 64;
     // ranks whose warp tiles share one stage (one load barrier, one wait):
-    // the 1 KB INT4 tiles of the fused kernel are loaded two ranks at a time
-    static constexpr int RPU = (SCH == S_ASYM4 && OSCH != OUT_F32) ? 2 : 1;
-    static constexpr int STAGES = (OSCH == OUT_F32) ? 4 : ((SCH == S_ASYM4) ? 12 / RPU : (W16 ? 6 : 8));
+    // the 1 KB INT4 tiles of the fused kernel, and the TACO tiles of the fused
+    // kernel compiled for 4-lane blocks, are loaded two ranks at a time (the
+    // stages halve, so the bytes in flight stay the same)
+    static constexpr bool PAIRS = (SCH == S_ASYM4 && OSCH != OUT_F32) || (SCH == S_TACO && OSCH == S_TACO && LG == 2);
+    static constexpr int RPU = PAIRS ? 2 : 1;
+    static constexpr int STAGES = (OSCH == OUT_F32) ? 4 : ((SCH == S_ASYM4) ? 12 / RPU : (W16 ? 6 / RPU : 8));
     // ranks whose scale metadata is fetched together, one chunk ahead
     static constexpr int RANK_CHUNK = (SCH == S_ASYM4) ? 8 : (W16 ? 2 : 4);
     static_assert(RANK_CHUNK % RPU == 0, "a stage never spans two metadata chunks");
@@ -323,13 +328,15 @@ __device__ __forceinline__ void load_codes4(const uint8_t* st, int lane, uint32_
 //                      ASYM fmaf(q, s, z)
 // MODE 1 (accumulate): TACO/INT8 v = fmaf(code, s, v)
 //                      ASYM      v = v + fmaf(q, s, z)
-// INT4 takes its scale as the fp16 bits s16 (mixed-precision multiply-add).
+// INT4 takes its scale as the fp16 bits s16 (mixed-precision multiply-add);
+// SC: its values come scaled by (2^-24, 2^-20) per pair (u4x8_dequant_scaled),
+// and the caller scales the sum back.
 // ptxas contracts a packed multiply into a packed add that consumes it in
 // the same basic block.  The products of MODE 0 are only ever consumed by a
 // fused multiply-add, a scalar add.rn (the first butterfly stage, which is
 // never contracted), a multiply, a conversion or a store, so they keep their
 // own rounding as defined.
-template <int SCH, int MODE>
+template <int SCH, int MODE, bool SC = false>
 __device__ __forceinline__ void dequant_segment(const uint8_t* st, int lane, float s, float z, u64 (&v)[32],
                                                 uint16_t s16, uint32_t xm = 0)
 {
@@ -344,14 +351,27 @@ __device__ __forceinline__ void dequant_segment(const uint8_t* st, int lane, flo
     if constexpr (SCH == S_ASYM4) {
         uint32_t q[8];
         load_codes4(st, lane, q);
-#pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            float f[8];
-            u4x8_dequant(q[w], s16, z, f);
+        auto put = [&](int w, const float (&f)[8]) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const u64 d = pk2(f[2 * k], f[2 * k + 1]);
                 v[w * 4 + k] = (MODE == 0) ? d : add2(v[w * 4 + k], d);
+            }
+        };
+        if constexpr (SC) {
+            const float zlo = __fmul_rn(z, 0x1p-24f), zhi = __fmul_rn(z, 0x1p-20f);
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                float f[8];
+                u4x8_dequant_scaled(q[w], s16, zlo, zhi, f);
+                put(w, f);
+            }
+        } else {
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                float f[8];
+                u4x8_dequant(q[w], s16, z, f);
+                put(w, f);
             }
         }
     } else {
@@ -1051,11 +1071,11 @@ struct UnitCursor {
     }
 };
 
-template <int SCH, int OSCH>
+template <int SCH, int OSCH, int LG>
 __device__ __forceinline__ void reduce_issue(const ReduceParams& p, uint8_t* wb, uint64_t* bars,
                                              int stage, const UnitCursor& u, int first, int W)
 {
-    using C = ReduceCfg<SCH, OSCH>;
+    using C = ReduceCfg<SCH, OSCH, LG>;
     const int wt = first + u.t * W;
     const int nr = min(C::RPU, p.n_ranks - u.r);
     mbar_arrive_expect_tx(&bars[stage], nr * C::IN_BYTES);
@@ -1108,10 +1128,10 @@ __device__ __forceinline__ void reduce_meta_load(const ReduceParams& p, int t, i
 // CH: the adaptive rescaling's channel factors are applied to the TACO FP32
 // sum (p.chan_up).
 template <int SCH, int OSCH, bool AMAX_ONLY, int LG = -1, bool CH = false>
-__global__ void __launch_bounds__(ReduceCfg<SCH, OSCH>::WARPS * 32, 1)
+__global__ void __launch_bounds__(ReduceCfg<SCH, OSCH, LG>::WARPS * 32, 1)
 reduce_kernel(const __grid_constant__ ReduceParams p)
 {
-    using C = ReduceCfg<SCH, OSCH>;
+    using C = ReduceCfg<SCH, OSCH, LG>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = aligned_smem(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1144,7 +1164,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
         if (p.chan_smem) chan_to_smem(fsm, p.chan_up, static_cast<int>(p.seg_per_row.d) * SEG);
     if (lane == 0) {
         for (int u = 0; u < C::STAGES && u < total_units; ++u) {
-            reduce_issue<SCH, OSCH>(p, wb, bars, u, next_unit, first, W);
+            reduce_issue<SCH, OSCH, LG>(p, wb, bars, u, next_unit, first, W);
             next_unit.advance(n, C::RPU);
         }
     }
@@ -1155,6 +1175,9 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
     const uint32_t xm = XL ? xl_mask(L, lane) : 0u;
     constexpr int RANK_CHUNK = C::RANK_CHUNK;
     const int n_chunks = (n + RANK_CHUNK - 1) / RANK_CHUNK;
+    // INT4: the rank terms and partial sums are formed scaled by powers of two
+    // (no nibble subtraction) and the sum is scaled back after the last rank
+    constexpr bool SCALED4 = SCH == S_ASYM4;
     int stage = 0;
     uint32_t phase = 0;
     int unit = 0;
@@ -1201,14 +1224,14 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                 const uint16_t s16 = static_cast<uint16_t>(cur[kk].raw);
                 const uint8_t* tile = wb + stage * C::STAGE_BYTES + slot * C::IN_BYTES;
                 if (r == 0)
-                    dequant_segment<SCH, 0>(tile, lane, s, z, acc, s16, xm);
+                    dequant_segment<SCH, 0, SCALED4>(tile, lane, s, z, acc, s16, xm);
                 else
-                    dequant_segment<SCH, 1>(tile, lane, s, z, acc, s16, xm);
+                    dequant_segment<SCH, 1, SCALED4>(tile, lane, s, z, acc, s16, xm);
                 if (slot == C::RPU - 1 || r == n - 1) {
                     __syncwarp();
                     if (lane == 0 && unit + C::STAGES < total_units) {
                         fence_proxy_async_smem();
-                        reduce_issue<SCH, OSCH>(p, wb, bars, stage, next_unit, first, W);
+                        reduce_issue<SCH, OSCH, LG>(p, wb, bars, stage, next_unit, first, W);
                         next_unit.advance(n, C::RPU);
                     }
                     ++unit;
@@ -1220,6 +1243,12 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
             }
         }
         if (aborted) break;
+        if constexpr (SCALED4) {
+            // the INT4 sums back from their (2^-24, 2^-20) scales (exact)
+            const u64 un = pk2(0x1p24f, 0x1p20f);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = mul2(acc[j], un);
+        }
         // TACO -> TACO with equal blocks: the sums already are the Hadamard
         // transform of the reduced rows, so they are requantized as they are
         // (the inverse and forward transforms cancel and are skipped).

@@ -23,7 +23,7 @@ bool reduce_requant_supported(int scheme, int out_scheme) { return reduce_smem(s
 template <int SCH, int OSCH, bool AMAX, int LG = -1, bool CH = false>
 static cudaError_t launch_r(const ReduceParams& p, int grid, cudaStream_t stream)
 {
-    using C = ReduceCfg<SCH, OSCH>;
+    using C = ReduceCfg<SCH, OSCH, LG>;
     static std::atomic<unsigned> done{0};
     auto fn = reduce_kernel<SCH, OSCH, AMAX, LG, CH>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(fn), C::SMEM, &done);
@@ -63,8 +63,10 @@ cudaError_t launch_reduce_requant(int scheme, int out_scheme, bool amax_only, co
     switch (scheme * 4 + out_scheme) {
     case S_TACO * 4 + S_TACO:
         // equal blocks of 4 lanes (B = 256, no transform): compiled for that
-        // block size, 45.1 -> 43.6 us on 4 x 8192 x 5120; the same for
-        // 2 lanes measured slower (59.6 -> 60.7 us on 8 x 8192 x 4096)
+        // block size, 45.1 -> 43.6 us on 4 x 8192 x 5120, and with two ranks'
+        // tiles per stage, 45.0 -> 44.2 us in the step; the same for 2 lanes
+        // measured slower (59.6 -> 60.7 us on 8 x 8192 x 4096), and two ranks
+        // per stage did not change it (60.5 us)
         if (p.q_lanes_log2 == 2 && p.lanes_log2 == 2)
             return amax_only ? launch_r<S_TACO, S_TACO, true, 2>(p, grid, stream)
                              : launch_r<S_TACO, S_TACO, false, 2>(p, grid, stream);

@@ -13,7 +13,12 @@
   the later ones DELAYED with the scales taco_update_scale left (TACO Core
   claim: stability across training steps); every step's per-tensor states
   of both stages are compared with the oracle's over whole tensors, and
-  sampled rows of every output bit for bit.
+  sampled rows of every output bit for bit;
+* INT4 groups at the edges of the reduce's scaled decode (terms and partial
+  sums formed scaled by 2^-24 / 2^-20, the sum scaled back at the end):
+  zero-points far below the scale, minima exactly 0, constant groups (s = 0)
+  and groups of fp16 subnormals (subnormal scale and zero-point), through
+  the FP32 reduce, the fused reduce + INT8 requant and the decompress.
 """
 import multiprocessing as mp
 import os
@@ -282,4 +287,67 @@ def test_tiny_per_tensor_scales(dev, B):
         so = orc.reduce(orc.TACO_FP8, B, [shards[r] for r in sel], rows, cols)
         torch.cuda.synchronize()
         assert_same(f"reduce {sel}", s, so)
+    assert qta.qta_device_error() == 0
+
+
+def _int4_edge_data(rng, rows, cols):
+    """Rows of 128-groups: N(0, 1) groups, and on every eighth row from row 3
+    groups in [1e-6, 1] (an fp16-subnormal zero-point far below the scale),
+    groups with minimum exactly 0, constant groups (s = 0) and groups in
+    [0, 1e-6] (fp16 subnormals: subnormal scale and zero-point)."""
+    x = rng.standard_normal((rows, cols)).astype(np.float32)
+    g = x.reshape(rows, cols // 128, 128)
+    for r in range(3, rows, 8):
+        g[r, 0::4] = rng.uniform(0.0, 1.0, g[r, 0::4].shape)
+        g[r, 0::4, 0] = 1e-6
+        g[r, 1::4] = np.abs(g[r, 1::4])
+        g[r, 1::4, 5] = 0.0
+        g[r, 2::4] = 0.75
+        g[r, 3::4] = rng.uniform(0.0, 1e-6, g[r, 3::4].shape)
+    return x
+
+
+def test_int4_edge_groups(dev):
+    rows, cols, n = 256, 1024, 3
+    rng = np.random.default_rng(41)
+    shards, dsh = [], []
+    d = qta.desc(qta.INT4_ASYM_G128, 128, rows, cols)
+    for r in range(n):
+        xt = to_dtype_cpu(_int4_edge_data(rng, rows, cols) * (1.0 + r), qta.FP16)
+        c, s_, z, st = oracle_compress(qta.INT4_ASYM_G128, 128, xt, qta.FP16, 1, rows, cols)
+        shards.append((c, s_, z, st))
+        dsh.append(qta.QTensor(d, torch.from_numpy(c.view(np.uint8).copy()).to(dev),
+                               torch.from_numpy(s_.view(np.uint8).copy()).to(dev),
+                               torch.from_numpy(z.view(np.uint8).copy()).to(dev), None))
+    # the data has the edge groups: subnormal fp16 scales and zero-points,
+    # zero scales, zero zero-points
+    s0 = shards[0][1].view(np.float16)
+    z0 = shards[0][2].view(np.float16)
+    tiny = np.float16(2.0 ** -14)
+    assert ((s0 > 0) & (s0 < tiny)).any() and ((z0 > 0) & (z0 < tiny)).any()
+    assert (s0 == 0).any() and (z0 == 0).any()
+
+    out = torch.empty((rows, cols), dtype=torch.float32, device=dev)
+    qta.qar_reduce(d, dsh, 0, rows, out)
+    ref = orc.reduce(orc.INT4_ASYM, 128, shards, rows, cols)
+    torch.cuda.synchronize()
+    assert_same("int4 reduce, edge groups", out, ref)
+
+    nb = 4
+    dg = qta.desc(qta.INT8_ASYM_G128, 128, rows // nb, cols, batch=nb)
+    g = qta.alloc_qtensor(dg, dev)
+    qta.qar_reduce_requant(d, dsh, 0, rows, dg, g, qta.SCALE_CURRENT)
+    c, s_, z = orc.reduce_requant(orc.INT4_ASYM, 128, shards, rows, cols, 0, rows, orc.INT8_ASYM, 128, nb, None,
+                                  orc.CURRENT)
+    torch.cuda.synchronize()
+    compare_qtensor("int4 -> int8 fused, edge groups", g, (c, s_, z, None))
+
+    for out_dt, tdt in ((qta.FP32, torch.float32), (qta.BF16, torch.bfloat16)):
+        y = torch.empty((rows, cols), dtype=tdt, device=dev)
+        qta.taco_decompress(d, dsh[0], y, out_dt)
+        c0, s0b, z0b, _ = shards[0]
+        ref = orc.decompress(orc.INT4_ASYM, 128, c0, s0b, z0b, None, 1, rows, cols,
+                             orc.FP32 if out_dt == qta.FP32 else orc.BF16)
+        torch.cuda.synchronize()
+        assert_same(f"int4 decompress ({tdt}), edge groups", y, ref)
     assert qta.qta_device_error() == 0
