@@ -259,14 +259,16 @@ def test_tiny_per_tensor_scales(dev, B):
     # inputs of that size) next to an ordinary one, with tensor boundaries
     # inside warp tiles: the decompress and the FP32 reduce must give the
     # oracle's bits (every multiply by 1/B and by the block scale keeps its
-    # own rounding, also near the subnormal range).
-    batch, rows, cols = 3, 11, 768
+    # own rounding, also near the subnormal range).  The fourth tensor's
+    # block scales lie near 2^-78, between the two.
+    batch, rows, cols = 4, 11, 768
     rng = np.random.default_rng(B)
     x = random_values(rng, (batch, rows, cols), "mixed")
     x[0] *= np.float32(2.0 ** -75)
     x[2] *= np.float32(2.0 ** -92)
+    x[3] *= np.float32(2.0 ** -70)
     xt = torch.from_numpy(x.astype(np.float32))
-    state = np.array([2.0 ** -83, 0.0, 0.01, 0.0, 2.0 ** -100, 0.0], dtype=np.float32)
+    state = np.array([2.0 ** -83, 0.0, 0.01, 0.0, 2.0 ** -100, 0.0, 2.0 ** -79, 0.0], dtype=np.float32)
     d, q = gpu_compress(qta.TACO_FP8, B, xt, qta.FP32, batch, rows, cols, qta.SCALE_DELAYED, state=state, dev=dev)
     ref = oracle_compress(qta.TACO_FP8, B, xt, qta.FP32, batch, rows, cols, orc.DELAYED, state=state)
     torch.cuda.synchronize()
