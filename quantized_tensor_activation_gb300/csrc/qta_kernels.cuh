@@ -161,7 +161,11 @@ struct ReduceCfg {
     // with 2-rank metadata chunks and 6 stages of one rank, or 3 of two);
     // the others run 12
     static constexpr bool W16 = (SCH == S_ASYM4) || (SCH == S_TACO && OSCH == S_TACO);
-    static constexpr int WARPS = W16 ? 16 : 12;
+    // the fused TACO reduce compiled for 4-lane blocks runs 15: on 4 x 8192 x
+    // 5120 its 20480 warp tiles take 9 rounds over 152 CTAs with 16 warps or
+    // 15, the last round nearly full with 15, and fewer warps share a
+    // scheduler (43.1 -> 42.3 us)
+    static constexpr int WARPS = (SCH == S_TACO && OSCH == S_TACO && LG == 2) ? 15 : (W16 ? 16 : 12);
     static constexpr int IN_SEG = (SCH == S_ASYM4) ? 32 : 64;
     static constexpr int OUT_SEG = (OSCH == OUT_F32) ? 256 : (OSCH == S_ASYM4) ? 32 : 64;
     // ranks whose warp tiles share one stage (one load barrier, one wait):
