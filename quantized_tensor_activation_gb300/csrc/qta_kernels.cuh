@@ -1077,11 +1077,11 @@ struct UnitCursor {
 
 template <int SCH, int OSCH, int LG>
 __device__ __forceinline__ void reduce_issue(const ReduceParams& p, uint8_t* wb, uint64_t* bars,
-                                             int stage, const UnitCursor& u, int first, int W)
+                                             int stage, const UnitCursor& u, int first, int W, int n)
 {
     using C = ReduceCfg<SCH, OSCH, LG>;
     const int wt = first + u.t * W;
-    const int nr = min(C::RPU, p.n_ranks - u.r);
+    const int nr = min(C::RPU, n - u.r);
     mbar_arrive_expect_tx(&bars[stage], nr * C::IN_BYTES);
 #pragma unroll
     for (int i = 0; i < C::RPU; ++i)
@@ -1096,7 +1096,7 @@ __device__ __forceinline__ void reduce_issue(const ReduceParams& p, uint8_t* wb,
 // copy when a rank is decoded).
 template <int SCH, int RANK_CHUNK>
 __device__ __forceinline__ void reduce_meta_load(const ReduceParams& p, int t, int c, int first, int W, int lane,
-                                                 SegMeta<SCH> (&m)[RANK_CHUNK])
+                                                 int n, SegMeta<SCH> (&m)[RANK_CHUNK])
 {
     const int o = (first + t * W) * 32 + lane;
     const int g = p.seg_begin + o;
@@ -1104,7 +1104,7 @@ __device__ __forceinline__ void reduce_meta_load(const ReduceParams& p, int t, i
 #pragma unroll
     for (int k = 0; k < RANK_CHUNK; ++k) {
         const int r = c * RANK_CHUNK + k;
-        if (valid && r < p.n_ranks) {
+        if (valid && r < n) {
             if constexpr (SCH == S_TACO) {
                 m[k].raw = __ldg(static_cast<const uint8_t*>(p.scales[r]) + (g >> p.lanes_log2));
             } else if constexpr (SCH == S_INT8SYM) {
@@ -1131,7 +1131,10 @@ __device__ __forceinline__ void reduce_meta_load(const ReduceParams& p, int t, i
 // TACO FP32 sum, which inverts the transform with the halved exchange), else -1.
 // CH: the adaptive rescaling's channel factors are applied to the TACO FP32
 // sum (p.chan_up).
-template <int SCH, int OSCH, bool AMAX_ONLY, int LG = -1, bool CH = false>
+// NR: the number of shards when compiled in (> 0; it must equal p.n_ranks),
+// else 0.  With it the rank loop unrolls completely, and the shard of every
+// metadata load and TMA load is a constant.
+template <int SCH, int OSCH, bool AMAX_ONLY, int LG = -1, bool CH = false, int NR = 0>
 __global__ void __launch_bounds__(ReduceCfg<SCH, OSCH, LG>::WARPS * 32, 1)
 reduce_kernel(const __grid_constant__ ReduceParams p)
 {
@@ -1146,7 +1149,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
     const int W = gridDim.x * C::WARPS;
     // warp-major: the tiles of the last, partial round spread over all CTAs
     const int first = warp * gridDim.x + blockIdx.x;
-    const int n = p.n_ranks;
+    const int n = NR > 0 ? NR : p.n_ranks;
     const int my_tiles = (first < p.n_warp_tiles) ? (p.n_warp_tiles - first + W - 1) / W : 0;
     const int total_units = my_tiles * ((n + C::RPU - 1) / C::RPU);
     UnitCursor next_unit;   // next unit to load (meaningful in lane 0)
@@ -1168,7 +1171,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
         if (p.chan_smem) chan_to_smem(fsm, p.chan_up, static_cast<int>(p.seg_per_row.d) * SEG);
     if (lane == 0) {
         for (int u = 0; u < C::STAGES && u < total_units; ++u) {
-            reduce_issue<SCH, OSCH, LG>(p, wb, bars, u, next_unit, first, W);
+            reduce_issue<SCH, OSCH, LG>(p, wb, bars, u, next_unit, first, W, n);
             next_unit.advance(n, C::RPU);
         }
     }
@@ -1179,6 +1182,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
     const uint32_t xm = XL ? xl_mask(L, lane) : 0u;
     constexpr int RANK_CHUNK = C::RANK_CHUNK;
     const int n_chunks = (n + RANK_CHUNK - 1) / RANK_CHUNK;
+    constexpr int CHUNKS_NR = NR > 0 ? (NR + RANK_CHUNK - 1) / RANK_CHUNK : 1;
     // INT4: the rank terms and partial sums are formed scaled by powers of two
     // (no nibble subtraction) and the sum is scaled back after the last rank
     constexpr bool SCALED4 = SCH == S_ASYM4;
@@ -1193,19 +1197,19 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                       (OSCH == S_TACO) ? cta_amax_slots(p.M_out, p.q_seg_per_tensor) : 0};
     Quantizer<(OSCH == OUT_F32) ? S_TACO : OSCH> quant;
     SegMeta<SCH> nxt[RANK_CHUNK];
-    if (my_tiles > 0) reduce_meta_load<SCH, RANK_CHUNK>(p, 0, 0, first, W, lane, nxt);
+    if (my_tiles > 0) reduce_meta_load<SCH, RANK_CHUNK>(p, 0, 0, first, W, lane, n, nxt);
     for (int t = 0; t < my_tiles && !aborted; ++t) {
         const int wt = first + t * W;
         if constexpr (OSCH != OUT_F32) quant.begin(qo, wt * 32, lane);
         u64 acc[32];
-        for (int c = 0; c < n_chunks && !aborted; ++c) {
+        auto chunk = [&](int c) {
             SegMeta<SCH> cur[RANK_CHUNK];
 #pragma unroll
             for (int kk = 0; kk < RANK_CHUNK; ++kk) cur[kk] = nxt[kk];
             if (c + 1 < n_chunks)
-                reduce_meta_load<SCH, RANK_CHUNK>(p, t, c + 1, first, W, lane, nxt);
+                reduce_meta_load<SCH, RANK_CHUNK>(p, t, c + 1, first, W, lane, n, nxt);
             else if (t + 1 < my_tiles)
-                reduce_meta_load<SCH, RANK_CHUNK>(p, t + 1, 0, first, W, lane, nxt);
+                reduce_meta_load<SCH, RANK_CHUNK>(p, t + 1, 0, first, W, lane, n, nxt);
 #pragma unroll
             for (int kk = 0; kk < RANK_CHUNK; ++kk) {
                 const int r = c * RANK_CHUNK + kk;
@@ -1233,9 +1237,19 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                     dequant_segment<SCH, 1, SCALED4>(tile, lane, s, z, acc, s16, xm);
                 if (slot == C::RPU - 1 || r == n - 1) {
                     __syncwarp();
-                    if (lane == 0 && unit + C::STAGES < total_units) {
+                    if constexpr (NR > 0) {
+                        // the unit STAGES ahead of this one: with the rank count
+                        // compiled in, its tile offset and shard are constants
+                        constexpr int U = (NR + C::RPU - 1) / C::RPU;
+                        const int ahead = (c * RANK_CHUNK + kk) / C::RPU + C::STAGES;
+                        const UnitCursor u{t + ahead / U, (ahead % U) * C::RPU};
+                        if (lane == 0 && u.t < my_tiles) {
+                            fence_proxy_async_smem();
+                            reduce_issue<SCH, OSCH, LG>(p, wb, bars, stage, u, first, W, n);
+                        }
+                    } else if (lane == 0 && unit + C::STAGES < total_units) {
                         fence_proxy_async_smem();
-                        reduce_issue<SCH, OSCH, LG>(p, wb, bars, stage, next_unit, first, W);
+                        reduce_issue<SCH, OSCH, LG>(p, wb, bars, stage, next_unit, first, W, n);
                         next_unit.advance(n, C::RPU);
                     }
                     ++unit;
@@ -1245,6 +1259,13 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                     }
                 }
             }
+        };
+        if constexpr (NR > 0) {
+#pragma unroll
+            for (int c = 0; c < CHUNKS_NR; ++c)
+                if (!aborted) chunk(c);
+        } else {
+            for (int c = 0; c < n_chunks && !aborted; ++c) chunk(c);
         }
         if (aborted) break;
         if constexpr (SCALED4) {

@@ -20,16 +20,31 @@ int reduce_smem(int scheme, int out_scheme)
 
 bool reduce_requant_supported(int scheme, int out_scheme) { return reduce_smem(scheme, out_scheme) > 0 && out_scheme != OUT_F32; }
 
-template <int SCH, int OSCH, bool AMAX, int LG = -1, bool CH = false>
+template <int SCH, int OSCH, bool AMAX, int LG = -1, bool CH = false, int NR = 0>
 static cudaError_t launch_r(const ReduceParams& p, int grid, cudaStream_t stream)
 {
     using C = ReduceCfg<SCH, OSCH, LG>;
     static std::atomic<unsigned> done{0};
-    auto fn = reduce_kernel<SCH, OSCH, AMAX, LG, CH>;
+    auto fn = reduce_kernel<SCH, OSCH, AMAX, LG, CH, NR>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(fn), C::SMEM, &done);
     if (e != cudaSuccess) return e;
     const int extra = (CH && p.chan_smem) ? static_cast<int>(p.seg_per_row.d) * SEG * 4 : 0;
     return launch_pdl(fn, dim3(grid), dim3(C::WARPS * 32), C::SMEM + extra, stream, p);
+}
+
+// The INT4 reduces (FP32 sum and fused) are also compiled for 4 and 8 shards:
+// the rank loop unrolled, every shard index a constant (flash_int4's fused
+// kernel 98.6 -> 84.5 us, its FP32 sum 103.0 -> 97.5 us).  Other counts run
+// the kernel that reads the count at run time.  The TACO fused kernels compiled that way were slower (gpt_tp
+// 60.5 -> 61.6 us, qwen_grad 43.3 -> 43.8 us) and the INT8 one no faster.
+template <int SCH, int OSCH, bool AMAX, int LG = -1>
+static cudaError_t launch_rn(const ReduceParams& p, int grid, cudaStream_t stream)
+{
+    switch (p.n_ranks) {
+    case 4: return launch_r<SCH, OSCH, AMAX, LG, false, 4>(p, grid, stream);
+    case 8: return launch_r<SCH, OSCH, AMAX, LG, false, 8>(p, grid, stream);
+    default: return launch_r<SCH, OSCH, AMAX, LG>(p, grid, stream);
+    }
 }
 
 cudaError_t launch_reduce(int scheme, const ReduceParams& p, int grid, cudaStream_t stream)
@@ -51,7 +66,7 @@ cudaError_t launch_reduce(int scheme, const ReduceParams& p, int grid, cudaStrea
         default: return cudaErrorInvalidValue;
         }
     case S_INT8SYM: return launch_r<S_INT8SYM, OUT_F32, false>(p, grid, stream);
-    case S_ASYM4: return launch_r<S_ASYM4, OUT_F32, false>(p, grid, stream);
+    case S_ASYM4: return launch_rn<S_ASYM4, OUT_F32, false>(p, grid, stream);
     case S_ASYM8: return launch_r<S_ASYM8, OUT_F32, false>(p, grid, stream);
     default: return cudaErrorInvalidValue;
     }
@@ -73,7 +88,7 @@ cudaError_t launch_reduce_requant(int scheme, int out_scheme, bool amax_only, co
         return amax_only ? launch_r<S_TACO, S_TACO, true>(p, grid, stream)
                          : launch_r<S_TACO, S_TACO, false>(p, grid, stream);
     case S_INT8SYM * 4 + S_INT8SYM: return launch_r<S_INT8SYM, S_INT8SYM, false>(p, grid, stream);
-    case S_ASYM4 * 4 + S_ASYM8: return launch_r<S_ASYM4, S_ASYM8, false>(p, grid, stream);
+    case S_ASYM4 * 4 + S_ASYM8: return launch_rn<S_ASYM4, S_ASYM8, false>(p, grid, stream);
     case S_ASYM8 * 4 + S_ASYM8: return launch_r<S_ASYM8, S_ASYM8, false>(p, grid, stream);
     default: return cudaErrorInvalidValue;
     }
