@@ -216,7 +216,7 @@ def _to_dev(scheme, B, rows, cols, shards, dev):
 @pytest.mark.parametrize("scheme,B", [(qta.TACO_FP8, 64), (qta.TACO_FP8, 128), (qta.TACO_FP8, 256),
                                       (qta.INT8_SYM_B64, 64), (qta.INT4_ASYM_G128, 128),
                                       (qta.INT8_ASYM_G128, 128)])
-@pytest.mark.parametrize("n", [1, 2, 3, 8, 16])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 16])
 def test_reduce(dev, scheme, B, n):
     rows, cols = 96, 1024
     rng = np.random.default_rng(hash((scheme, B, n)) % 2 ** 32)
@@ -243,6 +243,32 @@ def test_reduce_many_tiles(dev):
     ref = orc.reduce(orc.TACO_FP8, B, shards, rows, cols)
     torch.cuda.synchronize()
     assert_same("reduce many tiles", out, ref)
+
+
+@pytest.mark.parametrize("n", [4, 8])
+def test_reduce_int4_many_tiles(dev, n):
+    # the INT4 reduces compiled for 4 and 8 shards issue each TMA load from
+    # the unit's constant position STAGES units ahead: with the grid capped to
+    # 2 SMs every warp runs about 32 tiles, so that position crosses tiles
+    rows, cols = 1024, 2048
+    rng = np.random.default_rng(17 + n)
+    shards = _oracle_shards(qta.INT4_ASYM_G128, 128, n, rows, cols, rng, dtype=qta.FP16)
+    d, ds = _to_dev(qta.INT4_ASYM_G128, 128, rows, cols, shards, dev)
+    d.max_sms = 2
+    out = torch.empty((rows, cols), dtype=torch.float32, device=dev)
+    qta.qar_reduce(d, ds, 0, rows, out)
+    ref = orc.reduce(orc.INT4_ASYM, 128, shards, rows, cols)
+    torch.cuda.synchronize()
+    assert_same(f"int4 reduce, {n} shards, many tiles", out, ref)
+    nb = 4
+    dg = qta.desc(qta.INT8_ASYM_G128, 128, rows // nb, cols, batch=nb)
+    g = qta.alloc_qtensor(dg, dev)
+    qta.qar_reduce_requant(d, ds, 0, rows, dg, g, qta.SCALE_CURRENT)
+    c, s_, z = orc.reduce_requant(orc.INT4_ASYM, 128, shards, rows, cols, 0, rows, orc.INT8_ASYM, 128, nb, None,
+                                  orc.CURRENT)
+    torch.cuda.synchronize()
+    compare_qtensor(f"int4 -> int8 fused, {n} shards, many tiles", g, (c, s_, z, None))
+    assert qta.qta_device_error() == 0
 
 
 def test_taco_steps_with_drift(dev):
@@ -340,7 +366,7 @@ def test_copy_kernel(dev):
                                                  (qta.INT8_SYM_B64, 64, qta.INT8_SYM_B64, 64),
                                                  (qta.INT4_ASYM_G128, 128, qta.INT8_ASYM_G128, 128),
                                                  (qta.INT8_ASYM_G128, 128, qta.INT8_ASYM_G128, 128)])
-@pytest.mark.parametrize("n", [1, 3, 8])
+@pytest.mark.parametrize("n", [1, 3, 4, 8])
 @pytest.mark.parametrize("mode", [qta.SCALE_CURRENT, qta.SCALE_DELAYED])
 def test_reduce_requant_fused(dev, scheme, B, gscheme, gB, n, mode):
     # the fused call against the oracle's fused reduce + requant (TACO ->
