@@ -471,10 +471,18 @@ __device__ __forceinline__ void fwht_cross(u64 (&v)[32], int lanes_per_block, in
 // instead of 64, and afterwards the lanes of a block own a block-wide strip
 // of positions in every row rather than a row each.  To let both partners ship
 // the same registers, lane c of a block keeps position j of its row in slot
-// j ^ xm(c), xm = 32 (c & 1) + 16 (c >> 1 & 1) (the second term only when
-// 4 lanes share a block).
+// j ^ xm(c), c the lane's position in its block: xm = 32 c with 2 lanes per
+// block.  With 4 there are two layouts.  N4 (the kernels compiled for 4-lane
+// blocks): xm = 16 c, lane bit 0 mapped to xm bit 16 and lane bit 1 to xm bit
+// 32, so the 8 lanes of one shared-memory wavefront read 8 different 16-byte
+// bank groups of their rows under the 64- and 128-byte swizzles (the code and
+// bf16 segment loads).  Otherwise (the kernels that read the block size at run
+// time): xm = 32 (c & 1) + 16 (c >> 1 & 1), which gives them shorter code.
+template <bool N4 = false>
 __device__ __forceinline__ uint32_t xl_mask(int lanes_per_block, int lane)
 {
+    if constexpr (N4)
+        return lanes_per_block == 4 ? (lane & 3) * 16u : (lanes_per_block == 2 ? (lane & 1) * 32u : 0u);
     return (lanes_per_block >= 2 ? (lane & 1) * 32u : 0u) | (lanes_per_block == 4 ? ((lane >> 1) & 1) * 16u : 0u);
 }
 
@@ -518,85 +526,81 @@ __device__ __forceinline__ void fwht64_local_xl(u64 (&v)[32], uint32_t xm)
     }
 }
 
-// Strides 64 and 128 with the halved exchange, on the permuted slots.  Stage
-// d pairs lane c with c ^ d.  Each lane keeps the lower half of every group of
-// registers and ships the upper half, which holds the partner's kept
-// positions.  With a = the lane's kept value and o = the partner's value at
-// the same position, the pair's outputs are (lower + upper, lower - upper),
-// each rounded once as in fwht_cross.
-// SWAP = false: every lane writes the sum to the lower half of the group and
-// the difference to the upper half: a + o, and fma(o, s, -s*a) with s = +1
-// in the lane that holds the upper row (else -1), which is lower - upper in
-// both lanes (-s*a is exact).  Afterwards, with 4 lanes per block, registers
-// 0-7, 8-15, 16-23, 24-31 hold rows 0, 2, 1, 3 of the block; with 2 lanes,
-// registers 0-15 and 16-31 hold rows 0 and 1.
+// One cross-lane stage of the halved exchange, on the permuted slots: lane c
+// pairs with c ^ d.  Registers come in groups of 2H; each lane keeps the lower
+// H registers of every group and ships the upper H, which hold the partner's
+// kept positions (the xm bit of lane bit d sets which half that is).  With
+// a = the lane's kept value and o = the partner's value at the same
+// position, the pair's outputs are (lower + upper, lower - upper), each
+// rounded once as in fwht_cross.
+// SWAP = false: every lane writes the sum to the kept register and the
+// difference to the shipped one: a + o, and fma(o, s, -s*a) with s = +1 in
+// the lane that holds the upper row (else -1), which is lower - upper in both
+// lanes (-s*a is exact).
 // SWAP = true: the lane whose stage bit is clear (a from the lower row)
 // writes fma(a, +1, o) and fma(o, -1, a); the lane whose bit is set (a from
 // the upper row) writes the difference first, fma(a, -1, o) = o - a, then
 // fma(o, +1, a) = o + a.  The same adds and subtracts, zero signs included,
-// one instruction fewer per register pair, and the row order swapped by the
-// lane's position in its block (xl_group_row with that position), so that the
-// lanes of a block write rows of different parity in one store instruction.
+// one instruction fewer per register pair, and the rows of the pair swapped
+// in the lanes whose stage bit is set.
+template <bool SWAP, int H>
+__device__ __forceinline__ void xl_stage(u64 (&v)[32], int lane, int d)
+{
+    if constexpr (SWAP) {
+        const float s = (lane & d) ? -1.0f : 1.0f;
+        const u64 s2 = pk2(s, s), ns2 = pk2(-s, -s);
+#pragma unroll
+        for (int h = 0; h < 32; h += 2 * H)
+#pragma unroll
+            for (int j = 0; j < H; ++j) {
+                const u64 o = __shfl_xor_sync(0xffffffffu, v[h + H + j], d);
+                const u64 a = v[h + j];
+                v[h + j] = fma2(a, s2, o);
+                v[h + H + j] = fma2(o, ns2, a);
+            }
+    } else {
+        const float s = (lane & d) ? 1.0f : -1.0f;
+        const u64 s2 = pk2(s, s), ns2 = pk2(-s, -s);
+#pragma unroll
+        for (int h = 0; h < 32; h += 2 * H)
+#pragma unroll
+            for (int j = 0; j < H; ++j) {
+                const u64 o = __shfl_xor_sync(0xffffffffu, v[h + H + j], d);
+                const u64 a = v[h + j];
+                v[h + j] = add2(a, o);
+                v[h + H + j] = fma2(o, s2, mul2(a, ns2));
+            }
+    }
+}
+
+// Strides 64 and 128 with the halved exchange.  With 2 lanes per block, the
+// stride-64 stage pairs lane c with c ^ 1 and ships registers 16-31 (xm bit
+// 32).  With 4 and N4 (xm = 16 c), the stride-64 stage (c ^ 1) ships
+// registers 8-15 and 24-31 (xm bit 16), then the stride-128 stage (c ^ 2)
+// ships registers 16-31 (xm bit 32).  Without N4 the stride-64 stage ships
+// registers 16-31 and the stride-128 stage 8-15 and 24-31.  Afterwards lane c
+// of a block holds positions xm .. xm + 64/L - 1 of every row of the block in
+// register groups of 32 / L registers (xl_group_row gives the row of each).
 // Register 2i+t of a group holds position xm + 2i + t.
-template <bool SWAP = false>
+template <bool SWAP = false, bool N4 = false>
 __device__ __forceinline__ void fwht_cross_xl(u64 (&v)[32], int lanes_per_block, int lane)
 {
-    if (lanes_per_block >= 2) {
-        if constexpr (SWAP) {
-            const float s = (lane & 1) ? -1.0f : 1.0f;
-            const u64 s2 = pk2(s, s), ns2 = pk2(-s, -s);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const u64 o = __shfl_xor_sync(0xffffffffu, v[16 + j], 1);
-                const u64 a = v[j];
-                v[j] = fma2(a, s2, o);
-                v[16 + j] = fma2(o, ns2, a);
-            }
-        } else {
-            const float s = (lane & 1) ? 1.0f : -1.0f;
-            const u64 s2 = pk2(s, s), ns2 = pk2(-s, -s);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const u64 o = __shfl_xor_sync(0xffffffffu, v[16 + j], 1);
-                const u64 a = v[j];
-                v[j] = add2(a, o);
-                v[16 + j] = fma2(o, s2, mul2(a, ns2));
-            }
-        }
-    }
-    if (lanes_per_block == 4) {
-        if constexpr (SWAP) {
-            const float s = (lane & 2) ? -1.0f : 1.0f;
-            const u64 s2 = pk2(s, s), ns2 = pk2(-s, -s);
-#pragma unroll
-            for (int h = 0; h < 32; h += 16)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const u64 o = __shfl_xor_sync(0xffffffffu, v[h + 8 + j], 2);
-                    const u64 a = v[h + j];
-                    v[h + j] = fma2(a, s2, o);
-                    v[h + 8 + j] = fma2(o, ns2, a);
-                }
-        } else {
-            const float s = (lane & 2) ? 1.0f : -1.0f;
-            const u64 s2 = pk2(s, s), ns2 = pk2(-s, -s);
-#pragma unroll
-            for (int h = 0; h < 32; h += 16)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const u64 o = __shfl_xor_sync(0xffffffffu, v[h + 8 + j], 2);
-                    const u64 a = v[h + j];
-                    v[h + j] = add2(a, o);
-                    v[h + 8 + j] = fma2(o, s2, mul2(a, ns2));
-                }
-        }
+    if constexpr (N4) {
+        if (lanes_per_block == 4) xl_stage<SWAP, 8>(v, lane, 1);
+        if (lanes_per_block >= 2) xl_stage<SWAP, 16>(v, lane, lanes_per_block == 4 ? 2 : 1);
+    } else {
+        if (lanes_per_block >= 2) xl_stage<SWAP, 16>(v, lane, 1);
+        if (lanes_per_block == 4) xl_stage<SWAP, 8>(v, lane, 2);
     }
 }
 
 // Block row (0 .. lanes-1) held by register group g after fwht_cross_xl: p is
-// the lane's position in its block with SWAP, 0 without.
+// the lane's position in its block with SWAP, 0 without.  Group g holds row g
+// (N4 or 2 lanes); without N4, the 4-lane groups hold rows 0, 2, 1, 3.
+template <bool N4 = false>
 __device__ __forceinline__ int xl_group_row(int g, int lanes_log2, int p)
 {
+    if constexpr (N4) return g ^ p;
     return (lanes_log2 == 2 ? (((g & 1) << 1) | (g >> 1)) : g) ^ p;
 }
 

@@ -268,8 +268,8 @@ __device__ __forceinline__ void store_segment(uint8_t* ob, int lane, const u64 (
 // Output of fwht_cross_xl into the staging rows: register group g (32/L
 // pairs) goes to row (lane & ~(L-1)) + xl_group_row(g, lg, p) of the warp
 // tile (p: the lane's position in its block after a swapping exchange, else
-// 0), positions xm .. xm + 64/L - 1.
-template <int OUT>
+// 0), positions xm .. xm + 64/L - 1.  N4: the layout of xl_mask<true>.
+template <int OUT, bool N4 = false>
 __device__ __forceinline__ void store_segment_xl(uint8_t* ob, int lane, const u64 (&v)[32], int lanes_log2,
                                                  uint32_t xm, int p)
 {
@@ -279,7 +279,7 @@ __device__ __forceinline__ void store_segment_xl(uint8_t* ob, int lane, const u6
 #pragma unroll
         for (int sc = 0; sc < 16; ++sc) {
             const int g = sc >> kl;
-            const uint32_t row = base + xl_group_row(g, lanes_log2, p);
+            const uint32_t row = base + xl_group_row<N4>(g, lanes_log2, p);
             const uint32_t pc = (xm >> 2) + (sc & ((1 << kl) - 1));
             const u64 a = v[sc * 2], b = v[sc * 2 + 1];
             sts128(ob + (pc >> 3) * 4096, sw128(row, pc & 7u), make_uint4(lo32(a), hi32(a), lo32(b), hi32(b)));
@@ -289,7 +289,7 @@ __device__ __forceinline__ void store_segment_xl(uint8_t* ob, int lane, const u6
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
             const int g = c >> kl;
-            const uint32_t row = base + xl_group_row(g, lanes_log2, p);
+            const uint32_t row = base + xl_group_row<N4>(g, lanes_log2, p);
             const uint32_t pc = (xm >> 3) + (c & ((1 << kl) - 1));
             uint32_t w[4];
 #pragma unroll
@@ -451,7 +451,8 @@ __device__ __forceinline__ void scale_slots(u64 (&v)[32], const float* __restric
 // The same for values in the layout fwht_cross_xl leaves: pair j holds row
 // group g = j >> (5 - lg) of the block (segment base + xl_group_row(g, lg, p),
 // p = the lane's position in its block) at positions xm + 2 (j mod 2^(5-lg));
-// colb is the column of the block's first element.
+// colb is the column of the block's first element.  N4: the layout of xl_mask<true>.
+template <bool N4 = false>
 __device__ __forceinline__ void scale_xl(u64 (&v)[32], const float* __restrict__ f, int colb, int lg, uint32_t xm,
                                          int p)
 {
@@ -459,7 +460,7 @@ __device__ __forceinline__ void scale_xl(u64 (&v)[32], const float* __restrict__
     for (int j = 0; j < 32; j += 2) {
         const int g = j >> (5 - lg);
         const int pos = static_cast<int>(xm) + 2 * (j & ((1 << (5 - lg)) - 1));
-        const float4 c = __ldg(reinterpret_cast<const float4*>(f + colb + SEG * xl_group_row(g, lg, p) + pos));
+        const float4 c = __ldg(reinterpret_cast<const float4*>(f + colb + SEG * xl_group_row<N4>(g, lg, p) + pos));
         v[j] = mul2(v[j], pk2(c.x, c.y));
         v[j + 1] = mul2(v[j + 1], pk2(c.z, c.w));
     }
@@ -498,13 +499,14 @@ __device__ __forceinline__ void scale_slots_sm(u64 (&v)[32], const float* fsm, i
 }
 
 // scale_xl from the shared copy; jb = the segment-column of the block's first segment.
+template <bool N4 = false>
 __device__ __forceinline__ void scale_xl_sm(u64 (&v)[32], const float* fsm, int jb, int lg, uint32_t xm, int p)
 {
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
         const int g = j >> (5 - lg);
         const int pos = static_cast<int>(xm) + 2 * (j & ((1 << (5 - lg)) - 1));
-        const float4 c = chan_sm(fsm, jb + xl_group_row(g, lg, p), pos >> 2);
+        const float4 c = chan_sm(fsm, jb + xl_group_row<N4>(g, lg, p), pos >> 2);
         v[j] = mul2(v[j], pk2(c.x, c.y));
         v[j + 1] = mul2(v[j + 1], pk2(c.z, c.w));
     }
@@ -644,8 +646,8 @@ struct Quantizer {
     // transformed (TACO): v already holds the Hadamard-domain values.
     // XL (TACO): v holds the lane's row in the permuted slots of xl_mask, the
     // transform runs with the halved exchange, and ow comes out in its
-    // layout (store_codes<..., true>).
-    template <bool AMAX_ONLY, bool XL = false>
+    // layout (store_codes<..., true>); N4: the layout of xl_mask<true>.
+    template <bool AMAX_ONLY, bool XL = false, bool N4 = false>
     __device__ __forceinline__ void run(u64 (&v)[32], const QuantOut& o, int tile_first, int lane,
                                         uint32_t (&ow)[16], bool transformed = false, uint32_t xm = 0)
     {
@@ -655,7 +657,7 @@ struct Quantizer {
         if constexpr (SCH == S_TACO) {
             if constexpr (XL) {
                 fwht64_local_xl(v, xm);
-                fwht_cross_xl(v, L, lane);
+                fwht_cross_xl<false, N4>(v, L, lane);
             } else if (!transformed) {
                 fwht64_local(v);
                 fwht_cross(v, L, lane);
@@ -772,8 +774,8 @@ struct Quantizer {
 // TMA tensor store (8-bit codes: 64 B rows, SW64; 4-bit: 32 B rows, SW32).
 // XL: ow is in the layout of fwht_cross_xl (without the row swap): word
 // group g (16/L words) goes to row (lane & ~(L-1)) + xl_group_row(g, lg, 0),
-// codes xm .. xm + 64/L - 1.
-template <int SCH, int OUT_BUFS, bool XL = false>
+// codes xm .. xm + 64/L - 1.  N4: the layout of xl_mask<true>.
+template <int SCH, int OUT_BUFS, bool XL = false, bool N4 = false>
 __device__ __forceinline__ void store_codes(uint8_t* ob, const CUtensorMap* map, int row, int lane,
                                             const uint32_t (&ow)[16], int lanes_log2 = 0, uint32_t xm = 0)
 {
@@ -789,7 +791,7 @@ __device__ __forceinline__ void store_codes(uint8_t* ob, const CUtensorMap* map,
         const int kl = 2 - lanes_log2;   // log2 of the 16-byte chunks per group
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            const uint32_t r = base + xl_group_row(c >> kl, lanes_log2, 0);
+            const uint32_t r = base + xl_group_row<N4>(c >> kl, lanes_log2, 0);
             const uint32_t pc = (xm >> 4) + (c & ((1 << kl) - 1));
             sts128(ob, sw64(r, pc), make_uint4(ow[4 * c], ow[4 * c + 1], ow[4 * c + 2], ow[4 * c + 3]));
         }
@@ -856,7 +858,9 @@ compress_kernel(const __grid_constant__ CompressParams p)
     // TACO: the rows are loaded into the permuted slots of the halved
     // cross-lane exchange
     constexpr bool XL = (SCH == S_TACO);
-    const uint32_t xm = XL ? xl_mask(L, lane) : 0u;
+    // the exchange layout for 4-lane blocks when compiled for them
+    constexpr bool N4 = (LG == 2);
+    const uint32_t xm = XL ? xl_mask<N4>(L, lane) : 0u;
     int stage = 0;
     uint32_t phase = 0;
     int k = 0;
@@ -893,9 +897,9 @@ compress_kernel(const __grid_constant__ CompressParams p)
                 scale_slots(v, p.chan, c0, xm);
         }
         uint32_t ow[16];
-        quant.template run<AMAX_ONLY, XL>(v, qo, wt * 32, lane, ow, false, xm);
+        quant.template run<AMAX_ONLY, XL, N4>(v, qo, wt * 32, lane, ow, false, xm);
         if constexpr (!AMAX_ONLY)
-            store_codes<SCH, C::OUT_BUFS, XL>(outb + (k % C::OUT_BUFS) * C::OUT_BYTES, &p.out_map, wt * 32, lane,
+            store_codes<SCH, C::OUT_BUFS, XL, N4>(outb + (k % C::OUT_BUFS) * C::OUT_BYTES, &p.out_map, wt * 32, lane,
                                               ow, lg, xm);
     }
     quant.finish(qo, lane);
@@ -981,7 +985,9 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
     const int L = 1 << lg;
     // TACO: the codes are read into the permuted slots of the halved
     // cross-lane exchange
-    const uint32_t xm = (SCH == S_TACO) ? xl_mask(L, lane) : 0u;
+    // the exchange layout for 4-lane blocks when compiled for them
+    constexpr bool N4 = (LG == 2);
+    const uint32_t xm = (SCH == S_TACO) ? xl_mask<N4>(L, lane) : 0u;
     int stage = 0;
     uint32_t phase = 0;
     int k = 0;
@@ -1023,16 +1029,16 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
         }
         if constexpr (SCH == S_TACO) {
             fwht64_local_xl(v, xm);
-            fwht_cross_xl<true>(v, L, lane);
+            fwht_cross_xl<true, N4>(v, L, lane);
             const u64 ib = pk2(p.inv_block, p.inv_block);
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = mul2(v[j], ib);
             if constexpr (CH) {
                 const int cb = seg_col0(wt * 32 + (lane & ~(L - 1)), p.seg_per_row);
                 if (p.chan_smem)
-                    scale_xl_sm(v, fsm, cb / SEG, lg, xm, lane & (L - 1));
+                    scale_xl_sm<N4>(v, fsm, cb / SEG, lg, xm, lane & (L - 1));
                 else
-                    scale_xl(v, p.chan_up, cb, lg, xm, lane & (L - 1));
+                    scale_xl<N4>(v, p.chan_up, cb, lg, xm, lane & (L - 1));
             }
         }
         uint8_t* ob = outb + (k % C::OUT_BUFS) * C::OUT_BYTES;
@@ -1044,7 +1050,7 @@ decompress_kernel(const __grid_constant__ DecompressParams p)
         }
         __syncwarp();
         if constexpr (SCH == S_TACO)
-            store_segment_xl<OUT>(ob, lane, v, lg, xm, lane & (L - 1));
+            store_segment_xl<OUT, N4>(ob, lane, v, lg, xm, lane & (L - 1));
         else
             store_segment<OUT>(ob, lane, v);
         fence_proxy_async_smem();
@@ -1179,7 +1185,9 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
     const int L = (LG >= 0) ? (1 << LG) : p.lanes_per_block;
     // TACO FP32 sum: codes read into the permuted slots of the halved exchange
     constexpr bool XL = (SCH == S_TACO) && (OSCH == OUT_F32);
-    const uint32_t xm = XL ? xl_mask(L, lane) : 0u;
+    // the exchange layout for 4-lane blocks when compiled for them
+    constexpr bool N4 = (LG == 2);
+    const uint32_t xm = XL ? xl_mask<N4>(L, lane) : 0u;
     constexpr int RANK_CHUNK = C::RANK_CHUNK;
     const int n_chunks = (n + RANK_CHUNK - 1) / RANK_CHUNK;
     constexpr int CHUNKS_NR = NR > 0 ? (NR + RANK_CHUNK - 1) / RANK_CHUNK : 1;
@@ -1281,7 +1289,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
         if (SCH == S_TACO && !direct) {
             if constexpr (XL) {
                 fwht64_local_xl(acc, xm);
-                fwht_cross_xl(acc, L, lane);
+                fwht_cross_xl<false, N4>(acc, L, lane);
             } else {
                 fwht64_local(acc);
                 fwht_cross(acc, L, lane);
@@ -1293,9 +1301,9 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                 if constexpr (CH && XL) {
                     const int cb = seg_col0(p.seg_begin + wt * 32 + (lane & ~(L - 1)), p.seg_per_row);
                     if (p.chan_smem)
-                        scale_xl_sm(acc, fsm, cb / SEG, (LG >= 0) ? LG : p.lanes_log2, xm, 0);
+                        scale_xl_sm<N4>(acc, fsm, cb / SEG, (LG >= 0) ? LG : p.lanes_log2, xm, 0);
                     else
-                        scale_xl(acc, p.chan_up, cb, (LG >= 0) ? LG : p.lanes_log2, xm, 0);
+                        scale_xl<N4>(acc, p.chan_up, cb, (LG >= 0) ? LG : p.lanes_log2, xm, 0);
                 }
             } else {
                 // scalar rounded multiplies: the requantizer's butterfly adds
@@ -1311,7 +1319,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
             if (lane == 0) bulk_wait_read<0>();
             __syncwarp();
             if constexpr (XL)
-                store_segment_xl<IN_FP32>(outb, lane, acc, (LG >= 0) ? LG : p.lanes_log2, xm, 0);
+                store_segment_xl<IN_FP32, N4>(outb, lane, acc, (LG >= 0) ? LG : p.lanes_log2, xm, 0);
             else
                 store_segment<IN_FP32>(outb, lane, acc);
             fence_proxy_async_smem();
