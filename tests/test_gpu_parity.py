@@ -271,6 +271,34 @@ def test_reduce_int4_many_tiles(dev, n):
     assert qta.qta_device_error() == 0
 
 
+@pytest.mark.parametrize("n", [4, 8])
+def test_reduce_int4_staged_metadata_and_fallback(dev, n):
+    # 10 segments per row and 63 rows: the row ranges starting at rows 0 and
+    # 16 start on a multiple of 16 segments, so the 4- and 8-shard INT4 reduces
+    # stage their scales and zeros through shared memory by TMA (the last warp
+    # tile of rows 0:63 reaches past the end of the arrays, which TMA fills
+    # with zeros); rows 3:50 start at segment 30 and take the per-lane loads
+    rows, cols = 63, 640
+    rng = np.random.default_rng(23 + n)
+    shards = _oracle_shards(qta.INT4_ASYM_G128, 128, n, rows, cols, rng, dtype=qta.FP16)
+    d, ds = _to_dev(qta.INT4_ASYM_G128, 128, rows, cols, shards, dev)
+    for rb, re_ in ((0, rows), (16, 48), (3, 50)):
+        out = torch.empty((re_ - rb, cols), dtype=torch.float32, device=dev)
+        qta.qar_reduce(d, ds, rb, re_, out)
+        ref = orc.reduce(orc.INT4_ASYM, 128, shards, rows, cols, rb, re_)
+        torch.cuda.synchronize()
+        assert_same(f"int4 reduce rows {rb}:{re_}, {n} shards", out, ref)
+        nb = 1
+        dg = qta.desc(qta.INT8_ASYM_G128, 128, re_ - rb, cols, batch=nb)
+        g = qta.alloc_qtensor(dg, dev)
+        qta.qar_reduce_requant(d, ds, rb, re_, dg, g, qta.SCALE_CURRENT)
+        c, s_, z = orc.reduce_requant(orc.INT4_ASYM, 128, shards, rows, cols, rb, re_, orc.INT8_ASYM, 128, nb, None,
+                                      orc.CURRENT)
+        torch.cuda.synchronize()
+        compare_qtensor(f"int4 -> int8 fused rows {rb}:{re_}, {n} shards", g, (c, s_, z, None))
+    assert qta.qta_device_error() == 0
+
+
 def test_taco_steps_with_drift(dev):
     # successive steps with a per-step magnitude drift: step 0 CURRENT, later
     # steps DELAYED with the scale left by taco_update_scale of the previous
