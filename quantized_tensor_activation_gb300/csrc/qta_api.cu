@@ -80,13 +80,13 @@ bool encoder_ready()
 }
 
 // 2D map over rows of `inner` elements (row stride = inner * elem bytes),
-// box = {inner, 32 rows}.
+// box = {inner, box_rows rows}.
 bool map_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t inner,
-            uint64_t rows, CUtensorMapSwizzle sw)
+            uint64_t rows, CUtensorMapSwizzle sw, uint32_t box_rows = 32)
 {
     cuuint64_t dims[2] = {inner, rows};
     cuuint64_t strides[1] = {inner * elem_bytes};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(inner), 32};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(inner), box_rows};
     cuuint32_t es[2] = {1, 1};
     return g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -118,6 +118,14 @@ bool map_codes(CUtensorMap* m, int scheme, const void* base, uint64_t segs)
     if (scheme == QTA_INT4_ASYM_G128)
         return map_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, 32, segs, CU_TENSOR_MAP_SWIZZLE_32B);
     return map_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, 64, segs, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+// The same 4-bit codes as rows of two segments (64 B), box = one warp tile
+// (16 rows, 1 KB), 64-byte swizzle: the map of the INT4 FP32-sum reduce.
+// segs is even (a row holds a multiple of 128 codes).
+bool map_codes4_rows64(CUtensorMap* m, const void* base, uint64_t segs)
+{
+    return map_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, 64, segs / 2, CU_TENSOR_MAP_SWIZZLE_64B, 16);
 }
 
 // 1D map of n fp16 values (INT4 scales or zeros), box = 16 values (32 B).
@@ -590,8 +598,10 @@ static qta_status reduce_params(const qta_desc* d, const qta_qtensor* shards, in
     return QTA_OK;
 }
 
+// f32_sum: the launch stores the FP32 sum (its INT4 shards are mapped as
+// 64-byte rows, as the kernels with that output read them).
 static qta_status reduce_fill(const qta_desc* d, const qta_qtensor* shards, int32_t n_ranks, int64_t row_begin,
-                              int64_t row_end, ReduceParams* p, int* sms, int* smem_sm)
+                              int64_t row_end, ReduceParams* p, int* sms, int* smem_sm, bool f32_sum)
 {
     if (!encoder_ready()) return QTA_ERR_CUDA;
     unsigned int* err = nullptr;
@@ -600,7 +610,10 @@ static qta_status reduce_fill(const qta_desc* d, const qta_qtensor* shards, int3
     const int64_t per_row = d->cols / 64;
     std::memset(p, 0, sizeof(*p));
     for (int r = 0; r < n_ranks; ++r) {
-        if (!map_codes(&p->in_map[r], d->scheme, shards[r].codes, segs)) return QTA_ERR_CUDA;
+        const bool ok = (f32_sum && d->scheme == QTA_INT4_ASYM_G128)
+                            ? map_codes4_rows64(&p->in_map[r], shards[r].codes, static_cast<uint64_t>(segs))
+                            : map_codes(&p->in_map[r], d->scheme, shards[r].codes, segs);
+        if (!ok) return QTA_ERR_CUDA;
         p->scales[r] = shards[r].scales;
         p->zeros[r] = shards[r].zeros;
         p->state[r] = shards[r].state;
@@ -651,7 +664,7 @@ qta_status qar_reduce_requant(const qta_desc* d, const qta_qtensor* shards, int3
     // the requantized sum keeps the shards' channel factors: with one set on
     // both sides the rescaling cancels between the reduce and the requant
     if (out->chan != shards[0].chan) return QTA_ERR_UNSUPPORTED;
-    if ((st = reduce_fill(d, shards, n_ranks, row_begin, row_end, &p, &sms, &smem_sm)) != QTA_OK) return st;
+    if ((st = reduce_fill(d, shards, n_ranks, row_begin, row_end, &p, &sms, &smem_sm, false)) != QTA_OK) return st;
     p.chan_up = nullptr;
     if (!map_codes(&p.out_map, od->scheme, out->codes, static_cast<uint64_t>(p.M_out))) return QTA_ERR_CUDA;
     p.q_scales = out->scales;
@@ -683,7 +696,7 @@ qta_status qar_reduce(const qta_desc* d, const qta_qtensor* shards, int32_t n_ra
     if (st != QTA_OK || empty) return st;
     if (!sum_out) return QTA_ERR_INVALID_ARG;
     if (!aligned(sum_out, 16)) return QTA_ERR_ALIGNMENT;
-    if ((st = reduce_fill(d, shards, n_ranks, row_begin, row_end, &p, &sms, &smem_sm)) != QTA_OK) return st;
+    if ((st = reduce_fill(d, shards, n_ranks, row_begin, row_end, &p, &sms, &smem_sm, true)) != QTA_OK) return st;
     if (!map_f32(&p.out_map, sum_out, static_cast<uint64_t>(p.M_out))) return QTA_ERR_CUDA;
     const int chan_bytes = static_cast<int>(d->cols) * 4;
     p.chan_smem = (p.chan_up && reduce_smem(d->scheme, OUT_F32) + chan_bytes <= smem_optin()) ? 1 : 0;

@@ -625,16 +625,40 @@ __device__ __forceinline__ float group_min(float m, int lanes_per_block)
     return m;
 }
 
-// max |v| over the 64 values of a lane.
+// max |v| over the 64 values of a lane (NaNs ignored, 0 if none is a
+// number).  The maximum is exact in any order, so it runs as four
+// independent chains of eight, then two combining steps: 34 three-input max
+// instead of 32, with a dependent depth of 10 instead of 32.
 __device__ __forceinline__ float absmax64(const u64 (&v)[32])
 {
-    float m = 0.0f;
+    float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
         const float2 t = up2(v[j]);
-        m = max3f(m, fabsf(t.x), fabsf(t.y));
+        m[j & 3] = max3f(m[j & 3], fabsf(t.x), fabsf(t.y));
     }
-    return m;
+    return fmaxf(max3f(m[0], m[1], m[2]), m[3]);
+}
+
+// min and max over the 64 values of a lane (NaNs ignored), as four
+// independent chains each, like absmax64.
+__device__ __forceinline__ void minmax64(const u64 (&v)[32], float& mn, float& mx)
+{
+    float lo[4], hi[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const float2 t = up2(v[c]);
+        lo[c] = fminf(t.x, t.y);
+        hi[c] = fmaxf(t.x, t.y);
+    }
+#pragma unroll
+    for (int j = 4; j < 32; ++j) {
+        const float2 t = up2(v[j]);
+        lo[j & 3] = min3f(lo[j & 3], t.x, t.y);
+        hi[j & 3] = max3f(hi[j & 3], t.x, t.y);
+    }
+    mn = fminf(min3f(lo[0], lo[1], lo[2]), lo[3]);
+    mx = fmaxf(max3f(hi[0], hi[1], hi[2]), hi[3]);
 }
 
 }  // namespace qta

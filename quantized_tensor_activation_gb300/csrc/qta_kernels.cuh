@@ -195,6 +195,11 @@ struct ReduceCfg {
     static constexpr int RANK_CHUNK = (SCH == S_ASYM4) ? 8 : (W16 ? 2 : 4);
     static_assert(RANK_CHUNK % RPU == 0, "a stage never spans two metadata chunks");
     static constexpr int IN_BYTES = 32 * IN_SEG;
+    // INT4 shards of the FP32-sum reduce: a warp tile is loaded as 16 rows of
+    // two segments (64 B, 64-byte swizzle) instead of 32 rows of one; the
+    // fused kernel keeps the 32-byte rows (INT4 FP32 sum 94.7 -> 88.1 us on
+    // 8 x 8192 x 8192, the fused kernel 81.9 -> 84.7 us with 64-byte rows)
+    static constexpr bool ROWS64 = (SCH == S_ASYM4) && (OSCH == OUT_F32);
     static constexpr int STAGE_BYTES = RPU * IN_BYTES;
     static constexpr int OUT_BYTES = 32 * OUT_SEG;
     static constexpr int OUT_BUFS = 1;
@@ -340,11 +345,15 @@ __device__ __forceinline__ void load_codes8(const uint8_t* st, int lane, uint32_
 }
 
 // Nibble codes of one segment (32 bytes, SW32) into 8 words.
+// ROWS64: the tile as 16 rows of 64 B under the 64-byte swizzle, lane l's
+// segment the half l & 1 of row l >> 1 (the 8 lanes of a wavefront still
+// read 8 different 16-byte bank groups).
+template <bool ROWS64 = false>
 __device__ __forceinline__ void load_codes4(const uint8_t* st, int lane, uint32_t (&q)[8])
 {
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-        const uint4 w = lds128(st, sw32(lane, c));
+        const uint4 w = lds128(st, ROWS64 ? sw64(lane >> 1, 2 * (lane & 1) + c) : sw32(lane, c));
         q[c * 4 + 0] = w.x;
         q[c * 4 + 1] = w.y;
         q[c * 4 + 2] = w.z;
@@ -365,7 +374,7 @@ __device__ __forceinline__ void load_codes4(const uint8_t* st, int lane, uint32_
 // fused multiply-add, a scalar add.rn (the first butterfly stage, which is
 // never contracted), a multiply, a conversion or a store, so they keep their
 // own rounding as defined.
-template <int SCH, int MODE, bool SC = false>
+template <int SCH, int MODE, bool SC = false, bool ROWS64 = false>
 __device__ __forceinline__ void dequant_segment(const uint8_t* st, int lane, float s, float z, u64 (&v)[32],
                                                 uint16_t s16, uint32_t xm = 0)
 {
@@ -379,7 +388,7 @@ __device__ __forceinline__ void dequant_segment(const uint8_t* st, int lane, flo
     };
     if constexpr (SCH == S_ASYM4) {
         uint32_t q[8];
-        load_codes4(st, lane, q);
+        load_codes4<ROWS64>(st, lane, q);
         auto put = [&](int w, const float (&f)[8]) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -740,13 +749,8 @@ struct Quantizer {
             if (valid) static_cast<float*>(o.scales)[g] = s;
         } else {
             constexpr float Q = (SCH == S_ASYM4) ? 15.0f : 255.0f;
-            float mn = up2(v[0]).x, mx = mn;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float2 t = up2(v[j]);
-                mn = min3f(mn, t.x, t.y);
-                mx = max3f(mx, t.x, t.y);
-            }
+            float mn, mx;
+            minmax64(v, mn, mx);
             mn = group_min(mn, 2);
             mx = group_max(mx, 2);
             float sf = __fadd_rn(__fdiv_rn(__fsub_rn(mx, mn), Q), 0.0f);
@@ -1124,7 +1128,7 @@ __device__ __forceinline__ void reduce_issue(const ReduceParams& p, uint8_t* wb,
     for (int i = 0; i < C::RPU; ++i)
         if (i < nr)
             tma_load_2d(wb + stage * C::STAGE_BYTES + i * C::IN_BYTES, &p.in_map[u.r + i], 0,
-                        p.seg_begin + wt * 32, &bars[stage]);
+                        C::ROWS64 ? (p.seg_begin + wt * 32) >> 1 : p.seg_begin + wt * 32, &bars[stage]);
     if constexpr (MS) {
         if (meta) {
             uint8_t* md = mb + (u.t % NB) * n * C::META_RANK;
@@ -1307,9 +1311,9 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                 const uint16_t s16 = static_cast<uint16_t>(cur[kk].raw);
                 const uint8_t* tile = wb + stage * C::STAGE_BYTES + slot * C::IN_BYTES;
                 if (r == 0)
-                    dequant_segment<SCH, 0, SCALED4>(tile, lane, s, z, acc, s16, xm);
+                    dequant_segment<SCH, 0, SCALED4, C::ROWS64>(tile, lane, s, z, acc, s16, xm);
                 else
-                    dequant_segment<SCH, 1, SCALED4>(tile, lane, s, z, acc, s16, xm);
+                    dequant_segment<SCH, 1, SCALED4, C::ROWS64>(tile, lane, s, z, acc, s16, xm);
                 if (slot == C::RPU - 1 || r == n - 1) {
                     __syncwarp();
                     if constexpr (NR > 0) {
