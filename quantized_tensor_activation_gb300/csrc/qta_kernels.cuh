@@ -171,9 +171,8 @@ constexpr int OUT_F32 = -1;
 template <int SCH, int OSCH = OUT_F32, int LG = -1>
 struct ReduceCfg {
     // the INT4 kernels and the fused TACO -> TACO reduce fit 128 registers
-    // and run 16 warps (the INT4 decode is issue-bound; the TACO one fits
-    // with 2-rank metadata chunks and 6 stages of one rank, or 3 of two);
-    // the others run 12
+    // and run 16 warps (the TACO one with 2-rank metadata chunks); the
+    // others run 12
     static constexpr bool W16 = (SCH == S_ASYM4) || (SCH == S_TACO && OSCH == S_TACO);
     // the fused TACO reduce compiled for 4-lane blocks runs 15: on 4 x 8192 x
     // 5120 its 20480 warp tiles take 9 rounds over 152 CTAs with 16 warps or
@@ -184,13 +183,20 @@ struct ReduceCfg {
     static constexpr int OUT_SEG = (OSCH == OUT_F32) ? 256 : (OSCH == S_ASYM4) ? 32 : 64;
     // ranks whose warp tiles share one stage (one load barrier, one wait):
     // the 1 KB INT4 tiles of the fused kernel, and the TACO tiles of the fused
-    // kernel compiled for 4-lane blocks, are loaded two ranks at a time (the
-    // stages halve, so the bytes in flight stay the same)
+    // kernel compiled for 4-lane blocks, are loaded two ranks at a time
     static constexpr bool PAIRS = (SCH == S_ASYM4 && OSCH != OUT_F32) || (SCH == S_TACO && OSCH == S_TACO && LG == 2);
     static constexpr int RPU = PAIRS ? 2 : 1;
-    // the INT4 fused kernel keeps 5 stages of two ranks, so that the staged
-    // metadata (below) fits
-    static constexpr int STAGES = (OSCH == OUT_F32) ? 4 : ((SCH == S_ASYM4) ? 10 / RPU : (W16 ? 6 / RPU : 8));
+    // Stages per warp, measured per kernel in the step (each beside the next
+    // larger and smaller count): more stages than these put more loads in
+    // flight at once and make every kernel slower, fewer starve it.
+    //   FP32 sum: INT8 2 (272 -> 250 us with 4, 8 x 16384 x 8192), TACO with
+    //   1- or 2-lane blocks 3 (67.8 -> 66.6 us), INT4 and 4-lane TACO 4;
+    //   fused: INT4 3 stages of two ranks (82.0 -> 79.8 us with 5), TACO 4
+    //   (60.3 -> 58.1 us with 6), 4-lane TACO 2 of two ranks (42.8 -> 41.5
+    //   us with 3), INT8 5 (209.3 -> 205.4 us with 8).
+    static constexpr int STAGES =
+        (OSCH == OUT_F32) ? ((SCH == S_INT8SYM) ? 2 : (SCH == S_TACO && LG != 2) ? 3 : 4)
+                          : ((SCH == S_ASYM4) ? 6 / RPU : (W16 ? 4 / RPU : 5));
     // ranks whose scale metadata is fetched together, one chunk ahead
     static constexpr int RANK_CHUNK = (SCH == S_ASYM4) ? 8 : (W16 ? 2 : 4);
     static_assert(RANK_CHUNK % RPU == 0, "a stage never spans two metadata chunks");
