@@ -121,7 +121,7 @@ bool map_codes(CUtensorMap* m, int scheme, const void* base, uint64_t segs)
 }
 
 // The same 4-bit codes as rows of two segments (64 B), box = one warp tile
-// (16 rows, 1 KB), 64-byte swizzle: the map of the INT4 FP32-sum reduce.
+// (16 rows, 1 KB), 64-byte swizzle: the map of the INT4 reduce's shards.
 // segs is even (a row holds a multiple of 128 codes).
 bool map_codes4_rows64(CUtensorMap* m, const void* base, uint64_t segs)
 {
@@ -598,10 +598,8 @@ static qta_status reduce_params(const qta_desc* d, const qta_qtensor* shards, in
     return QTA_OK;
 }
 
-// f32_sum: the launch stores the FP32 sum (its INT4 shards are mapped as
-// 64-byte rows, as the kernels with that output read them).
 static qta_status reduce_fill(const qta_desc* d, const qta_qtensor* shards, int32_t n_ranks, int64_t row_begin,
-                              int64_t row_end, ReduceParams* p, int* sms, int* smem_sm, bool f32_sum)
+                              int64_t row_end, ReduceParams* p, int* sms, int* smem_sm)
 {
     if (!encoder_ready()) return QTA_ERR_CUDA;
     unsigned int* err = nullptr;
@@ -610,7 +608,7 @@ static qta_status reduce_fill(const qta_desc* d, const qta_qtensor* shards, int3
     const int64_t per_row = d->cols / 64;
     std::memset(p, 0, sizeof(*p));
     for (int r = 0; r < n_ranks; ++r) {
-        const bool ok = (f32_sum && d->scheme == QTA_INT4_ASYM_G128)
+        const bool ok = (d->scheme == QTA_INT4_ASYM_G128)
                             ? map_codes4_rows64(&p->in_map[r], shards[r].codes, static_cast<uint64_t>(segs))
                             : map_codes(&p->in_map[r], d->scheme, shards[r].codes, segs);
         if (!ok) return QTA_ERR_CUDA;
@@ -664,7 +662,7 @@ qta_status qar_reduce_requant(const qta_desc* d, const qta_qtensor* shards, int3
     // the requantized sum keeps the shards' channel factors: with one set on
     // both sides the rescaling cancels between the reduce and the requant
     if (out->chan != shards[0].chan) return QTA_ERR_UNSUPPORTED;
-    if ((st = reduce_fill(d, shards, n_ranks, row_begin, row_end, &p, &sms, &smem_sm, false)) != QTA_OK) return st;
+    if ((st = reduce_fill(d, shards, n_ranks, row_begin, row_end, &p, &sms, &smem_sm)) != QTA_OK) return st;
     p.chan_up = nullptr;
     if (!map_codes(&p.out_map, od->scheme, out->codes, static_cast<uint64_t>(p.M_out))) return QTA_ERR_CUDA;
     p.q_scales = out->scales;
@@ -696,7 +694,7 @@ qta_status qar_reduce(const qta_desc* d, const qta_qtensor* shards, int32_t n_ra
     if (st != QTA_OK || empty) return st;
     if (!sum_out) return QTA_ERR_INVALID_ARG;
     if (!aligned(sum_out, 16)) return QTA_ERR_ALIGNMENT;
-    if ((st = reduce_fill(d, shards, n_ranks, row_begin, row_end, &p, &sms, &smem_sm, true)) != QTA_OK) return st;
+    if ((st = reduce_fill(d, shards, n_ranks, row_begin, row_end, &p, &sms, &smem_sm)) != QTA_OK) return st;
     if (!map_f32(&p.out_map, sum_out, static_cast<uint64_t>(p.M_out))) return QTA_ERR_CUDA;
     const int chan_bytes = static_cast<int>(d->cols) * 4;
     p.chan_smem = (p.chan_up && reduce_smem(d->scheme, OUT_F32) + chan_bytes <= smem_optin()) ? 1 : 0;

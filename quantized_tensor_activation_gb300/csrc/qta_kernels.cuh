@@ -154,7 +154,10 @@ struct DecompressCfg {
     static constexpr int WARPS = (OUT == IN_FP32) ? 12 : 16;
     static constexpr int IN_SEG = (SCH == S_ASYM4) ? 32 : 64;
     static constexpr int OUT_SEG = (OUT == IN_FP32) ? 256 : 128;
-    static constexpr int STAGES = 4;
+    // 2 stages: fewer loads in flight made the TACO decompress faster
+    // (gpt_tp 21.3 -> 20.3 us, qwen_grad 26.6 -> 25.3 us against 4) and left
+    // the INT8 ones unchanged
+    static constexpr int STAGES = 2;
     static constexpr int IN_BYTES = 32 * IN_SEG;
     static constexpr int OUT_BYTES = 32 * OUT_SEG;
     static constexpr int OUT_BUFS = 1;
@@ -201,11 +204,10 @@ struct ReduceCfg {
     static constexpr int RANK_CHUNK = (SCH == S_ASYM4) ? 8 : (W16 ? 2 : 4);
     static_assert(RANK_CHUNK % RPU == 0, "a stage never spans two metadata chunks");
     static constexpr int IN_BYTES = 32 * IN_SEG;
-    // INT4 shards of the FP32-sum reduce: a warp tile is loaded as 16 rows of
-    // two segments (64 B, 64-byte swizzle) instead of 32 rows of one; the
-    // fused kernel keeps the 32-byte rows (INT4 FP32 sum 94.7 -> 88.1 us on
-    // 8 x 8192 x 8192, the fused kernel 81.9 -> 84.7 us with 64-byte rows)
-    static constexpr bool ROWS64 = (SCH == S_ASYM4) && (OSCH == OUT_F32);
+    // INT4 shards: a warp tile is loaded as 16 rows of two segments (64 B,
+    // 64-byte swizzle) instead of 32 rows of one (on 8 x 8192 x 8192: FP32
+    // sum 94.7 -> 88.1 us, fused kernel 79.8 -> 78.6 us)
+    static constexpr bool ROWS64 = (SCH == S_ASYM4);
     static constexpr int STAGE_BYTES = RPU * IN_BYTES;
     static constexpr int OUT_BYTES = 32 * OUT_SEG;
     static constexpr int OUT_BUFS = 1;
