@@ -224,16 +224,16 @@ qta_status check_qtensor(const qta_desc* d, const qta_qtensor* q)
     return QTA_OK;
 }
 
-// Persistent grid: at most one CTA per SM it may use (max_sms > 0 caps the
-// SMs, see qta_desc), never more CTAs than warp tiles need.
-int grid_for(int n_warp_tiles, int warps, int smem, int sms, int smem_per_sm, int max_sms)
+// Persistent grid: one CTA per SM it may use (max_sms > 0 caps the SMs, see
+// qta_desc), never more CTAs than warp tiles need.  One CTA is all an SM
+// holds: every kernel runs 8-16 warps at 109-236 registers a thread, so the
+// register file takes a second CTA of none of them, even where its shared
+// memory would.
+int grid_for(int n_warp_tiles, int warps, int sms, int max_sms)
 {
     if (max_sms > 0 && max_sms < sms) sms = max_sms;
-    int per_sm = smem_per_sm / (smem + 1024);
-    if (per_sm < 1) per_sm = 1;
     const int ctas = (n_warp_tiles + warps - 1) / warps;
-    const int cap = sms * per_sm;
-    return ctas < cap ? ctas : cap;
+    return ctas < sms ? ctas : sms;
 }
 
 qta_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QTA_OK : QTA_ERR_CUDA; }
@@ -513,8 +513,7 @@ static qta_status compress_impl(const qta_desc* d, const void* x, int32_t x_dtyp
     const int sch = d->scheme;  // qta_scheme values equal the kernel scheme kinds
     const int chan_bytes = static_cast<int>(d->cols) * 4;
     p.chan_smem = (out->chan && compress_smem(x_dtype, sch) + chan_bytes <= smem_optin()) ? 1 : 0;
-    const int grid = grid_for(p.n_warp_tiles, compress_warps(x_dtype),
-                              compress_smem(x_dtype, sch) + (p.chan_smem ? chan_bytes : 0), sms, smem_sm, d->max_sms);
+    const int grid = grid_for(p.n_warp_tiles, compress_warps(x_dtype), sms, d->max_sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (d->scheme == QTA_TACO_FP8 && base_mode == QTA_SCALE_CURRENT) {
         cudaError_t e = launch_state(out->state, d->batch, STATE_RESET_AMAX, s);
@@ -570,9 +569,7 @@ qta_status taco_decompress(const qta_desc* d, const qta_qtensor* in, void* y, in
     p.seg_per_row = make_fastdiv(static_cast<uint32_t>(d->cols / 64));
     const int chan_bytes = static_cast<int>(d->cols) * 4;
     p.chan_smem = (in->chan && decompress_smem(d->scheme, y_dtype) + chan_bytes <= smem_optin()) ? 1 : 0;
-    const int grid = grid_for(p.n_warp_tiles, decompress_warps(y_dtype),
-                              decompress_smem(d->scheme, y_dtype) + (p.chan_smem ? chan_bytes : 0), sms, smem_sm,
-                              d->max_sms);
+    const int grid = grid_for(p.n_warp_tiles, decompress_warps(y_dtype), sms, d->max_sms);
     return cuda_status(launch_decompress(d->scheme, y_dtype, p, grid, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -672,8 +669,7 @@ qta_status qar_reduce_requant(const qta_desc* d, const qta_qtensor* shards, int3
     p.q_lanes_log2 = log2i(p.q_lanes_per_block);
     p.q_seg_per_tensor = make_fastdiv(static_cast<uint32_t>(od->rows * od->cols / 64));
     p.q_round_up = (mode & QTA_SCALE_ROUND_UP) ? 1 : 0;
-    const int grid = grid_for(p.n_warp_tiles, reduce_warps(), reduce_smem(d->scheme, od->scheme), sms, smem_sm,
-                              d->max_sms);
+    const int grid = grid_for(p.n_warp_tiles, reduce_warps(), sms, d->max_sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (od->scheme == QTA_TACO_FP8 && base_mode == QTA_SCALE_CURRENT) {
         cudaError_t e = launch_state(out->state, od->batch, STATE_RESET_AMAX, s);
@@ -698,9 +694,7 @@ qta_status qar_reduce(const qta_desc* d, const qta_qtensor* shards, int32_t n_ra
     if (!map_f32(&p.out_map, sum_out, static_cast<uint64_t>(p.M_out))) return QTA_ERR_CUDA;
     const int chan_bytes = static_cast<int>(d->cols) * 4;
     p.chan_smem = (p.chan_up && reduce_smem(d->scheme, OUT_F32) + chan_bytes <= smem_optin()) ? 1 : 0;
-    const int grid = grid_for(p.n_warp_tiles, reduce_warps(),
-                              reduce_smem(d->scheme, OUT_F32) + (p.chan_smem ? chan_bytes : 0), sms, smem_sm,
-                              d->max_sms);
+    const int grid = grid_for(p.n_warp_tiles, reduce_warps(), sms, d->max_sms);
     return cuda_status(launch_reduce(d->scheme, p, grid, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -773,7 +767,7 @@ static qta_status accum_impl(const qta_desc* d, const qta_qtensor* in, const voi
     }
     int a_warps = 0, a_smem = 0;
     accum_cfg(d->scheme, x_dtype, requant, a_warps, a_smem);
-    const int grid = grid_for(p.n_warp_tiles, a_warps, a_smem, sms, smem_sm, d->max_sms);
+    const int grid = grid_for(p.n_warp_tiles, a_warps, sms, d->max_sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (requant && d->scheme == QTA_TACO_FP8 && base_mode == QTA_SCALE_CURRENT) {
         cudaError_t e = launch_state(out->state, d->batch, STATE_RESET_AMAX, s);
