@@ -189,9 +189,9 @@ struct ReduceCfg {
     // kernel compiled for 4-lane blocks, are loaded two ranks at a time
     static constexpr bool PAIRS = (SCH == S_ASYM4 && OSCH != OUT_F32) || (SCH == S_TACO && OSCH == S_TACO && LG == 2);
     static constexpr int RPU = PAIRS ? 2 : 1;
-    // Stages per warp, measured per kernel in the step (each beside the next
-    // larger and smaller count): more stages than these put more loads in
-    // flight at once and make every kernel slower, fewer starve it.
+    // Stages per warp, the fastest of those measured per kernel in the step
+    // (2 to 8): more stages than these put more loads in flight at once and
+    // make every kernel slower.
     //   FP32 sum: INT8 2 (272 -> 250 us with 4, 8 x 16384 x 8192), TACO with
     //   1- or 2-lane blocks 3 (67.8 -> 66.6 us), INT4 and 4-lane TACO 4;
     //   fused: INT4 3 stages of two ranks (82.0 -> 79.8 us with 5), TACO 4
