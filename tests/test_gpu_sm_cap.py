@@ -27,8 +27,12 @@ def _step(scheme, B, gscheme, gB, x, n, rows, cols, max_sms):
     qta.taco_decompress(d_g, g, y, qta.BF16)
     h = torch.empty((rows, cols), dtype=torch.float32, device=dev)
     qta.qar_dequant_add(d_g, g, y, qta.BF16, h)
+    # the shards themselves decompressed: with one or seven SMs every warp's
+    # stage ring wraps many times (INT4 included)
+    xq = torch.empty((n, rows, cols), dtype=torch.bfloat16, device=dev)
+    qta.taco_decompress(d_in, q, xq, qta.BF16)
     torch.cuda.synchronize()
-    out = [q.codes, q.scales, g.codes, g.scales, s, y, h]
+    out = [q.codes, q.scales, g.codes, g.scales, s, y, h, xq]
     return [t.clone() for t in out if t is not None]
 
 
