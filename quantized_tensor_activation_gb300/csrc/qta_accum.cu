@@ -38,7 +38,10 @@ static cudaError_t launch_a1(const AccumParams& p, int grid, cudaStream_t stream
     auto fn = accum_kernel<SCH, XIN, OSCH, AMAX_ONLY, LG>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(fn), C::SMEM, &done);
     if (e != cudaSuccess) return e;
-    return launch_pdl(fn, dim3(grid), dim3(C::WARPS * 32), C::SMEM, stream, p);
+    static std::atomic<int> per_sm{0};
+    const int g = persistent_grid(reinterpret_cast<const void*>(fn), C::WARPS * 32, C::SMEM, grid, p.n_warp_tiles,
+                                  C::WARPS, &per_sm);
+    return launch_pdl(fn, dim3(g), dim3(C::WARPS * 32), C::SMEM, stream, p);
 }
 
 template <int SCH, int XIN, int OSCH, bool AMAX_ONLY>

@@ -225,10 +225,9 @@ qta_status check_qtensor(const qta_desc* d, const qta_qtensor* q)
 }
 
 // Persistent grid: one CTA per SM it may use (max_sms > 0 caps the SMs, see
-// qta_desc), never more CTAs than warp tiles need.  One CTA is all an SM
-// holds: every kernel runs 8-16 warps at 109-236 registers a thread, so the
-// register file takes a second CTA of none of them, even where its shared
-// memory would.
+// qta_desc), never more CTAs than warp tiles need.  The launchers raise it to
+// as many CTAs per SM as the launched kernel's registers and shared memory
+// allow (persistent_grid).
 int grid_for(int n_warp_tiles, int warps, int sms, int max_sms)
 {
     if (max_sms > 0 && max_sms < sms) sms = max_sms;
@@ -244,6 +243,31 @@ qta_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QTA_OK : QTA_E
 // the device's opt-in maximum less the kernel's static shared memory, so that
 // launches of any size up to it (the kernel's own layout plus an optional
 // copy of the channel factors) pass.
+// grid_1 is one CTA per SM (grid_for).  When it spans every SM of the device
+// (no max_sms cap, enough tiles) and `per_sm` CTAs of the kernel fit on an SM
+// (its registers and `smem` bytes of dynamic shared memory, queried once per
+// kernel), the grid grows to that many per SM, never past the CTAs the warp
+// tiles need.  A capped call keeps one CTA per SM, so that its CTAs cannot
+// spread over more SMs than it may use.  Only the 8-warp ring hops fit two.
+int persistent_grid(const void* func, int threads, int smem, int grid_1, int n_warp_tiles, int warps,
+                    std::atomic<int>* per_sm_cache)
+{
+    int sms = 0, smem_sm = 0;
+    unsigned int* err = nullptr;
+    if (device_info(&sms, &smem_sm, &err) != cudaSuccess || grid_1 < sms) return grid_1;
+    int per_sm = per_sm_cache->load();
+    if (per_sm == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, func, threads, smem) != cudaSuccess)
+            per_sm = 1;
+        if (per_sm < 1) per_sm = 1;
+        per_sm_cache->store(per_sm);
+    }
+    const long long need = (static_cast<long long>(n_warp_tiles) + warps - 1) / warps;
+    const long long cap = static_cast<long long>(grid_1) * per_sm;
+    const long long g = need < cap ? need : cap;
+    return g > grid_1 ? static_cast<int>(g) : grid_1;
+}
+
 cudaError_t ensure_smem_attr(const void* func, int smem, std::atomic<unsigned>* done_mask)
 {
     int dev = 0;

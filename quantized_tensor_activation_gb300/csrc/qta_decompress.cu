@@ -26,7 +26,10 @@ static cudaError_t launch_d(const DecompressParams& p, int grid, cudaStream_t st
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(fn), C::SMEM, &done);
     if (e != cudaSuccess) return e;
     const int extra = (CH && p.chan_smem) ? static_cast<int>(p.seg_per_row.d) * SEG * 4 : 0;
-    return launch_pdl(fn, dim3(grid), dim3(C::WARPS * 32), C::SMEM + extra, stream, p);
+    static std::atomic<int> per_sm{0};
+    const int g = persistent_grid(reinterpret_cast<const void*>(fn), C::WARPS * 32, C::SMEM + extra, grid,
+                                  p.n_warp_tiles, C::WARPS, &per_sm);
+    return launch_pdl(fn, dim3(g), dim3(C::WARPS * 32), C::SMEM + extra, stream, p);
 }
 
 // TACO kernels are compiled per block size (1, 2 or 4 lanes per block).

@@ -54,5 +54,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // Per-device one-time setting of the dynamic shared-memory limit of a kernel.
 cudaError_t ensure_smem_attr(const void* func, int smem, std::atomic<unsigned>* done_mask);
+int persistent_grid(const void* func, int threads, int smem, int grid_1, int n_warp_tiles, int warps,
+                    std::atomic<int>* per_sm_cache);
 
 }  // namespace qta
