@@ -65,6 +65,23 @@ def test_dequant_add_requant(scheme, B, xdt, mode):
     assert qta.qta_device_error() == 0
 
 
+@pytest.mark.parametrize("scheme,B", [(qta.INT8_SYM_B64, 64), (qta.INT8_ASYM_G128, 128)])
+def test_dequant_add_requant_two_ctas_per_sm(scheme, B):
+    """The 8-warp INT8 hops run two CTAs per SM once a call spans the GPU:
+    8192 warp tiles here, several per warp at two CTAs on every SM."""
+    dev = device()
+    rng = np.random.default_rng(900 + scheme)
+    batch, rows, cols = 1, 8192, 2048
+    d, q, ref_in = _incoming(scheme, B, batch, rows, cols, rng, dev)
+    xt = to_dtype_cpu(random_values(rng, (batch, rows, cols), "mixed"), qta.BF16)
+    out = qta.alloc_qtensor(d, dev)
+    qta.qar_dequant_add_requant(d, q, xt.to(dev), qta.BF16, out, qta.SCALE_CURRENT)
+    s = orc.dequant_add(ORC_SCH[scheme], B, *ref_in, batch, rows, cols, oracle_bits_in(xt), ORC_DT[qta.BF16])
+    c, sc, z = orc.compress(ORC_SCH[scheme], B, s, orc.FP32, batch, rows, cols, None, qta.SCALE_CURRENT)
+    compare_qtensor("requant", out, (c, sc, z, None))
+    assert qta.qta_device_error() == 0
+
+
 def _ring_inputs(n, rows, cols, dtype, seed):
     rng = np.random.default_rng(seed)
     return to_dtype_cpu(random_values(rng, (n, rows, cols), "mixed"), dtype)
