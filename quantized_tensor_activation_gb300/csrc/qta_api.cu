@@ -248,7 +248,9 @@ qta_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QTA_OK : QTA_E
 // (its registers and `smem` bytes of dynamic shared memory, queried once per
 // kernel), the grid grows to that many per SM, never past the CTAs the warp
 // tiles need.  A capped call keeps one CTA per SM, so that its CTAs cannot
-// spread over more SMs than it may use.  Only the 8-warp ring hops fit two.
+// spread over more SMs than it may use.  With the present kernels every one
+// fits a single CTA per SM; the 8-warp INT8 ring hops come closest (two need
+// 256 bytes more shared memory than an SM has).
 int persistent_grid(const void* func, int threads, int smem, int grid_1, int n_warp_tiles, int warps,
                     std::atomic<int>* per_sm_cache)
 {

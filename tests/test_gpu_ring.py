@@ -66,9 +66,9 @@ def test_dequant_add_requant(scheme, B, xdt, mode):
 
 
 @pytest.mark.parametrize("scheme,B", [(qta.INT8_SYM_B64, 64), (qta.INT8_ASYM_G128, 128)])
-def test_dequant_add_requant_two_ctas_per_sm(scheme, B):
-    """The 8-warp INT8 hops run two CTAs per SM once a call spans the GPU:
-    8192 warp tiles here, several per warp at two CTAs on every SM."""
+def test_dequant_add_requant_many_tiles_per_warp(scheme, B):
+    """The 8-warp INT8 hops on a call that spans the whole GPU: 8192 warp
+    tiles, several per warp."""
     dev = device()
     rng = np.random.default_rng(900 + scheme)
     batch, rows, cols = 1, 8192, 2048
