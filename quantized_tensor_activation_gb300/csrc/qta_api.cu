@@ -129,16 +129,6 @@ bool map_codes4_rows64(CUtensorMap* m, const void* base, uint64_t segs)
 }
 
 // 1D map of n fp16 values (INT4 scales or zeros), box = 16 values (32 B).
-bool map_meta(CUtensorMap* m, const void* base, uint64_t n)
-{
-    cuuint64_t dims[1] = {n};
-    cuuint32_t box[1] = {16};
-    cuuint32_t es[1] = {1};
-    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 1, const_cast<void*>(base), dims, nullptr, box, es,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 FastDiv make_fastdiv(uint32_t d)
 {
     FastDiv f;
@@ -650,18 +640,6 @@ static qta_status reduce_fill(const qta_desc* d, const qta_qtensor* shards, int3
     p->inv_block = 1.0f / static_cast<float>(d->block);
     p->chan_up = shards[0].chan ? shards[0].chan + d->cols : nullptr;
     p->seg_per_row = make_fastdiv(static_cast<uint32_t>(d->cols / 64));
-    // INT4 shards of the counts the reduce is compiled for: their scales and
-    // zeros are staged through shared memory by TMA when every warp tile's 16
-    // groups start on a 16-byte boundary (the first segment a multiple of 16)
-    // and the arrays are 16-byte aligned; otherwise each lane loads its own
-    if (d->scheme == QTA_INT4_ASYM_G128 && (n_ranks == 4 || n_ranks == 8) && p->seg_begin % 16 == 0) {
-        bool ok = true;
-        for (int r = 0; r < n_ranks && ok; ++r)
-            ok = aligned(shards[r].scales, 16) && aligned(shards[r].zeros, 16) &&
-                 map_meta(&p->meta_map[2 * r], shards[r].scales, static_cast<uint64_t>(segs / 2)) &&
-                 map_meta(&p->meta_map[2 * r + 1], shards[r].zeros, static_cast<uint64_t>(segs / 2));
-        p->meta_smem = ok ? 1 : 0;
-    }
     return QTA_OK;
 }
 

@@ -67,10 +67,6 @@ struct DecompressParams {
 struct ReduceParams {
     CUtensorMap in_map[MAX_RANKS];  // codes of each shard
     CUtensorMap out_map;            // fp32 sum {32,2,M_out}, or the requantized codes
-    // INT4 with the metadata staged through shared memory (meta_smem): 1D
-    // maps of shard r's fp16 scales (2r) and zeros (2r + 1), box = the 16
-    // groups of one warp tile
-    CUtensorMap meta_map[2 * MAX_RANKS];
     const void* scales[MAX_RANKS];
     const void* zeros[MAX_RANKS];
     const float* state[MAX_RANKS];
@@ -93,7 +89,6 @@ struct ReduceParams {
     const float* chan_up; // TACO FP32 sum: per-channel factors up[cols] (NULL: none)
     FastDiv seg_per_row;  // cols / 64
     int chan_smem;        // the factors are copied into shared memory (cols * 4 extra bytes)
-    int meta_smem;        // meta_map is filled (INT4; seg_begin a multiple of 16)
 };
 
 // One ring hop: the incoming quantized partial sum plus the local tensor x,
@@ -117,15 +112,6 @@ struct AccumParams {
     float* q_state;
     int round_up;
 };
-
-// Ranks whose INT4 metadata a reduce can stage through shared memory.
-constexpr int MAX_RANKS_STAGED = 8;
-
-// Staged metadata buffers of a warp: the tiles that can have units in flight
-// when a tile's first wait returns, its own and those of the next stages - 1
-// units (units of rpu ranks, nr ranks per tile).
-constexpr int meta_buffers(int stages, int rpu, int nr) { return (stages - 1) / ((nr + rpu - 1) / rpu) + 1; }
-constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
 // Per-tensor amax slots of a CTA's shared-memory table (see AMAX_SLOTS).
 constexpr int AMAX_SLOTS_CFG = 64;
@@ -213,17 +199,8 @@ struct ReduceCfg {
     static constexpr int OUT_BUFS = 1;
     static constexpr int WARP_SMEM = STAGES * STAGE_BYTES + OUT_BUFS * OUT_BYTES;
     static constexpr int AMAX_BYTES = (OSCH == S_TACO) ? 4 * AMAX_SLOTS_CFG : 0;
-    // INT4, metadata staged through shared memory: per warp, the buffers of
-    // the tiles in flight (meta_buffers), each with every rank's 16 fp16
-    // scales and 16 fp16 zeros of its tile (64 B per rank)
-    static constexpr int META_RANK = 64;
-    static constexpr int META_BYTES =
-        (SCH == S_ASYM4) ? cmax(meta_buffers(STAGES, RPU, 4) * 4,
-                                meta_buffers(STAGES, RPU, MAX_RANKS_STAGED) * MAX_RANKS_STAGED) * META_RANK
-                         : 0;
-    static constexpr int META_OFF = WARPS * WARP_SMEM + WARPS * STAGES * 8 + AMAX_BYTES;
-    static constexpr int SMEM = META_OFF + WARPS * META_BYTES + 1024;
-    static constexpr int CHAN_OFF = META_OFF + WARPS * META_BYTES;
+    static constexpr int SMEM = WARPS * WARP_SMEM + WARPS * STAGES * 8 + AMAX_BYTES + 1024;
+    static constexpr int CHAN_OFF = WARPS * WARP_SMEM + WARPS * STAGES * 8 + AMAX_BYTES;
 };
 
 // Ring hop: a stage holds a warp tile of incoming codes (2 KB slot) and of
@@ -1118,35 +1095,19 @@ struct UnitCursor {
     }
 };
 
-// MS: the first unit of a tile also brings every rank's 16 scales and 16
-// zeros of the tile into the warp's metadata buffer u.t mod NB (NB buffers:
-// the tiles with units in flight), on the same barrier, whose wait comes
-// before any rank of the tile is decoded.
-template <int SCH, int OSCH, int LG, bool MS = false, int NB = 1>
+template <int SCH, int OSCH, int LG>
 __device__ __forceinline__ void reduce_issue(const ReduceParams& p, uint8_t* wb, uint64_t* bars,
-                                             int stage, const UnitCursor& u, int first, int W, int n,
-                                             uint8_t* mb = nullptr)
+                                             int stage, const UnitCursor& u, int first, int W, int n)
 {
     using C = ReduceCfg<SCH, OSCH, LG>;
     const int wt = first + u.t * W;
     const int nr = min(C::RPU, n - u.r);
-    const bool meta = MS && u.r == 0;
-    mbar_arrive_expect_tx(&bars[stage], nr * C::IN_BYTES + (meta ? n * C::META_RANK : 0));
+    mbar_arrive_expect_tx(&bars[stage], nr * C::IN_BYTES);
 #pragma unroll
     for (int i = 0; i < C::RPU; ++i)
         if (i < nr)
             tma_load_2d(wb + stage * C::STAGE_BYTES + i * C::IN_BYTES, &p.in_map[u.r + i], 0,
                         C::ROWS64 ? (p.seg_begin + wt * 32) >> 1 : p.seg_begin + wt * 32, &bars[stage]);
-    if constexpr (MS) {
-        if (meta) {
-            uint8_t* md = mb + (u.t % NB) * n * C::META_RANK;
-            const int x = (p.seg_begin + wt * 32) >> 1;   // first group of the tile
-            for (int r = 0; r < n; ++r) {
-                tma_load_1d(md + r * C::META_RANK, &p.meta_map[2 * r], x, &bars[stage]);
-                tma_load_1d(md + r * C::META_RANK + 32, &p.meta_map[2 * r + 1], x, &bars[stage]);
-            }
-        }
-    }
 }
 
 // Ranks are processed in chunks of RANK_CHUNK; the scale metadata of the next
@@ -1193,10 +1154,7 @@ __device__ __forceinline__ void reduce_meta_load(const ReduceParams& p, int t, i
 // NR: the number of shards when compiled in (> 0; it must equal p.n_ranks),
 // else 0.  With it the rank loop unrolls completely, and the shard of every
 // metadata load and TMA load is a constant.
-// MS (INT4, p.meta_smem): each stage also brings its ranks' scales and zeros
-// of the tile into shared memory, read there instead of by a global load per
-// lane and rank.
-template <int SCH, int OSCH, bool AMAX_ONLY, int LG = -1, bool CH = false, int NR = 0, bool MS = false>
+template <int SCH, int OSCH, bool AMAX_ONLY, int LG = -1, bool CH = false, int NR = 0>
 __global__ void __launch_bounds__(ReduceCfg<SCH, OSCH, LG>::WARPS * 32, 1)
 reduce_kernel(const __grid_constant__ ReduceParams p)
 {
@@ -1208,12 +1166,6 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
     uint8_t* outb = wb + C::STAGES * C::STAGE_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::WARPS * C::WARP_SMEM) + warp * C::STAGES;
     unsigned int* amax_tab = reinterpret_cast<unsigned int*>(smem + C::WARPS * C::WARP_SMEM + C::WARPS * C::STAGES * 8);
-    uint8_t* mb = smem + C::META_OFF + warp * C::META_BYTES;   // MS: metadata buffers
-    // MS: one metadata buffer per tile that can have units in flight when a
-    // tile's first wait returns (its own and those STAGES - 1 units ahead)
-    static_assert(!MS || (SCH == S_ASYM4 && NR > 0 && NR <= MAX_RANKS_STAGED), "metadata staged for INT4 only");
-    constexpr int META_NB = MS ? meta_buffers(C::STAGES, C::RPU, NR) : 1;
-    static_assert(!MS || META_NB * NR * C::META_RANK <= C::META_BYTES, "metadata buffers fit");
     const int W = gridDim.x * C::WARPS;
     // warp-major: the tiles of the last, partial round spread over all CTAs
     const int first = warp * gridDim.x + blockIdx.x;
@@ -1239,7 +1191,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
         if (p.chan_smem) chan_to_smem(fsm, p.chan_up, static_cast<int>(p.seg_per_row.d) * SEG);
     if (lane == 0) {
         for (int u = 0; u < C::STAGES && u < total_units; ++u) {
-            reduce_issue<SCH, OSCH, LG, MS, META_NB>(p, wb, bars, u, next_unit, first, W, n, mb);
+            reduce_issue<SCH, OSCH, LG>(p, wb, bars, u, next_unit, first, W, n);
             next_unit.advance(n, C::RPU);
         }
     }
@@ -1267,22 +1219,19 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                       (OSCH == S_TACO) ? cta_amax_slots(p.M_out, p.q_seg_per_tensor) : 0};
     Quantizer<(OSCH == OUT_F32) ? S_TACO : OSCH> quant;
     SegMeta<SCH> nxt[RANK_CHUNK];
-    if constexpr (!MS)
-        if (my_tiles > 0) reduce_meta_load<SCH, RANK_CHUNK>(p, 0, 0, first, W, lane, n, nxt);
+    if (my_tiles > 0) reduce_meta_load<SCH, RANK_CHUNK>(p, 0, 0, first, W, lane, n, nxt);
     for (int t = 0; t < my_tiles && !aborted; ++t) {
         const int wt = first + t * W;
         if constexpr (OSCH != OUT_F32) quant.begin(qo, wt * 32, lane);
         u64 acc[32];
         auto chunk = [&](int c) {
             SegMeta<SCH> cur[RANK_CHUNK];
-            if constexpr (!MS) {
 #pragma unroll
-                for (int kk = 0; kk < RANK_CHUNK; ++kk) cur[kk] = nxt[kk];
-                if (c + 1 < n_chunks)
-                    reduce_meta_load<SCH, RANK_CHUNK>(p, t, c + 1, first, W, lane, n, nxt);
-                else if (t + 1 < my_tiles)
-                    reduce_meta_load<SCH, RANK_CHUNK>(p, t + 1, 0, first, W, lane, n, nxt);
-            }
+            for (int kk = 0; kk < RANK_CHUNK; ++kk) cur[kk] = nxt[kk];
+            if (c + 1 < n_chunks)
+                reduce_meta_load<SCH, RANK_CHUNK>(p, t, c + 1, first, W, lane, n, nxt);
+            else if (t + 1 < my_tiles)
+                reduce_meta_load<SCH, RANK_CHUNK>(p, t + 1, 0, first, W, lane, n, nxt);
 #pragma unroll
             for (int kk = 0; kk < RANK_CHUNK; ++kk) {
                 const int r = c * RANK_CHUNK + kk;
@@ -1293,20 +1242,6 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                     if (!ok) {
                         aborted = true;
                         break;
-                    }
-                }
-                if constexpr (MS) {
-                    // after the tile's first wait: every rank's scale and zero
-                    // of the lane's group, from the tile's metadata buffer
-                    if (r == 0) {
-                        const uint8_t* mt = mb + (t % META_NB) * NR * C::META_RANK;
-#pragma unroll
-                        for (int k = 0; k < RANK_CHUNK; ++k) {
-                            const unsigned short* md = reinterpret_cast<const unsigned short*>(mt + k * C::META_RANK);
-                            cur[k].raw = (k < n) ? (static_cast<uint32_t>(md[lane >> 1]) |
-                                                    (static_cast<uint32_t>(md[16 + (lane >> 1)]) << 16))
-                                                 : 0u;
-                        }
                     }
                 }
                 float s, z;
@@ -1332,11 +1267,11 @@ reduce_kernel(const __grid_constant__ ReduceParams p)
                         const UnitCursor u{t + ahead / U, (ahead % U) * C::RPU};
                         if (lane == 0 && u.t < my_tiles) {
                             fence_proxy_async_smem();
-                            reduce_issue<SCH, OSCH, LG, MS, META_NB>(p, wb, bars, stage, u, first, W, n, mb);
+                            reduce_issue<SCH, OSCH, LG>(p, wb, bars, stage, u, first, W, n);
                         }
                     } else if (lane == 0 && unit + C::STAGES < total_units) {
                         fence_proxy_async_smem();
-                        reduce_issue<SCH, OSCH, LG, MS, META_NB>(p, wb, bars, stage, next_unit, first, W, n, mb);
+                        reduce_issue<SCH, OSCH, LG>(p, wb, bars, stage, next_unit, first, W, n);
                         next_unit.advance(n, C::RPU);
                     }
                     ++unit;

@@ -20,12 +20,12 @@ int reduce_smem(int scheme, int out_scheme)
 
 bool reduce_requant_supported(int scheme, int out_scheme) { return reduce_smem(scheme, out_scheme) > 0 && out_scheme != OUT_F32; }
 
-template <int SCH, int OSCH, bool AMAX, int LG = -1, bool CH = false, int NR = 0, bool MS = false>
+template <int SCH, int OSCH, bool AMAX, int LG = -1, bool CH = false, int NR = 0>
 static cudaError_t launch_r(const ReduceParams& p, int grid, cudaStream_t stream)
 {
     using C = ReduceCfg<SCH, OSCH, LG>;
     static std::atomic<unsigned> done{0};
-    auto fn = reduce_kernel<SCH, OSCH, AMAX, LG, CH, NR, MS>;
+    auto fn = reduce_kernel<SCH, OSCH, AMAX, LG, CH, NR>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(fn), C::SMEM, &done);
     if (e != cudaSuccess) return e;
     const int extra = (CH && p.chan_smem) ? static_cast<int>(p.seg_per_row.d) * SEG * 4 : 0;
@@ -43,12 +43,9 @@ static cudaError_t launch_r(const ReduceParams& p, int grid, cudaStream_t stream
 template <int SCH, int OSCH, bool AMAX, int LG = -1>
 static cudaError_t launch_rn(const ReduceParams& p, int grid, cudaStream_t stream)
 {
-    const bool ms = p.meta_smem != 0;
     switch (p.n_ranks) {
-    case 4: return ms ? launch_r<SCH, OSCH, AMAX, LG, false, 4, true>(p, grid, stream)
-                      : launch_r<SCH, OSCH, AMAX, LG, false, 4>(p, grid, stream);
-    case 8: return ms ? launch_r<SCH, OSCH, AMAX, LG, false, 8, true>(p, grid, stream)
-                      : launch_r<SCH, OSCH, AMAX, LG, false, 8>(p, grid, stream);
+    case 4: return launch_r<SCH, OSCH, AMAX, LG, false, 4>(p, grid, stream);
+    case 8: return launch_r<SCH, OSCH, AMAX, LG, false, 8>(p, grid, stream);
     default: return launch_r<SCH, OSCH, AMAX, LG>(p, grid, stream);
     }
 }

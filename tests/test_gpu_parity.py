@@ -272,12 +272,12 @@ def test_reduce_int4_many_tiles(dev, n):
 
 
 @pytest.mark.parametrize("n", [4, 8])
-def test_reduce_int4_staged_metadata_and_fallback(dev, n):
-    # 10 segments per row and 63 rows: the row ranges starting at rows 0 and
-    # 16 start on a multiple of 16 segments, so the 4- and 8-shard INT4 reduces
-    # stage their scales and zeros through shared memory by TMA (the last warp
-    # tile of rows 0:63 reaches past the end of the arrays, which TMA fills
-    # with zeros); rows 3:50 start at segment 30 and take the per-lane loads
+def test_reduce_int4_row_ranges(dev, n):
+    # 10 segments per row and 63 rows, reduced over rows 0:63, 16:48 and 3:50
+    # by the 4- and 8-shard INT4 reduces: tiles that start mid-row, a first
+    # segment that is not a multiple of 32 (rows 3:50 start at segment 30),
+    # and a last warp tile of 0:63 that reaches past the end of the arrays
+    # (its rows are read as zeros and its lanes store nothing)
     rows, cols = 63, 640
     rng = np.random.default_rng(23 + n)
     shards = _oracle_shards(qta.INT4_ASYM_G128, 128, n, rows, cols, rng, dtype=qta.FP16)
