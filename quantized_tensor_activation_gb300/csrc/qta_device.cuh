@@ -396,11 +396,23 @@ __device__ __forceinline__ u64 rint_bits2(u64 y)
     return add2(y, pk2(12582912.0f, 12582912.0f));
 }
 
-// Round to the nearest integer (ties to even) and clamp to [0, 255].
-__device__ __forceinline__ uint32_t cvt_rni_sat_u8(float y)
+// Round to the nearest integer (ties to even), saturating at the int32 range;
+// NaN gives 0.
+__device__ __forceinline__ uint32_t cvt_rni_s32(float y)
 {
     uint32_t r;
-    asm("cvt.rni.sat.u8.f32 %0, %1;" : "=r"(r) : "f"(y));
+    asm("cvt.rni.s32.f32 %0, %1;" : "=r"(r) : "f"(y));
+    return r;
+}
+
+// Four int32, each clamped to [0, 255], as the bytes [a b c d] of one word
+// (a lowest): two saturating pack conversions.  The clamp after the rounding
+// gives the codes of a rounding conversion that saturates to u8 directly.
+__device__ __forceinline__ uint32_t pack4_sat_u8(uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    uint32_t hi, r;
+    asm("cvt.pack.sat.u8.s32.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(d), "r"(c), "r"(0u));
+    asm("cvt.pack.sat.u8.s32.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(b), "r"(a), "r"(hi));
     return r;
 }
 

@@ -751,9 +751,11 @@ struct Quantizer {
             for (int j = 0; j < 32; ++j) {
                 const float2 y = up2(mul2(sub2(v[j], z2), inv2));
                 if constexpr (SCH == S_ASYM8) {
-                    // round to nearest even and clamp to [0, 255] in one conversion
-                    rb[2 * j] = cvt_rni_sat_u8(y.x);
-                    rb[2 * j + 1] = cvt_rni_sat_u8(y.y);
+                    // round to nearest even here, clamp to [0, 255] in the pack
+                    // below (flash_int4's fused reduce 79.7 -> 77.7 us against a
+                    // rounding conversion to u8 and three byte permutes per word)
+                    rb[2 * j] = cvt_rni_s32(y.x);
+                    rb[2 * j + 1] = cvt_rni_s32(y.y);
                 } else {
                     const u64 r = rint_bits2(pk2(fminf(fmaxf(y.x, 0.0f), Q), fminf(fmaxf(y.y, 0.0f), Q)));
                     rb[2 * j] = lo32(r);
@@ -769,7 +771,7 @@ struct Quantizer {
                 }
             } else {
 #pragma unroll
-                for (int w = 0; w < 16; ++w) ow[w] = bytes4(rb[4 * w], rb[4 * w + 1], rb[4 * w + 2], rb[4 * w + 3]);
+                for (int w = 0; w < 16; ++w) ow[w] = pack4_sat_u8(rb[4 * w], rb[4 * w + 1], rb[4 * w + 2], rb[4 * w + 3]);
             }
             if (valid && (lane & 1) == 0) {
                 static_cast<__half*>(o.scales)[g >> 1] = s16;
