@@ -63,6 +63,10 @@ NCU_TRAFFIC = {
     # captured on 4096 of the 16384 rows per rank; the input is read and the
     # codes written once per row, so a full launch moves four times as much
     ("taco_compress", "equarx_int8"): {"bytes": 4 * (536902912 + 250640896), "src": "ab617c98ab5262bf"},
+    ("taco_compress", "qwen_grad"): {"bytes": 335590912 + 133776128, "src": "ab617c98ab5262bf"},
+    # captured with the compress on all SMs; the bench runs it on 128, which
+    # moves the same bytes
+    ("taco_compress", "flash_int4"): {"bytes": 1073914368 + 265253376, "src": "ab617c98ab5262bf"},
 }
 
 
